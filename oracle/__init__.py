@@ -1,0 +1,177 @@
+"""ctypes binding of the plain-C CPU oracle (``lmoe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+benchmark's CPU-baseline leg may import this module; the product path never
+does.  The oracle shares no code with the CUDA library.  See the header of
+``lmoe_oracle.c`` for what each stage computes and which passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lmoe_oracle.c")
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+class OrDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
+
+
+def lib_path(plant: int = 0) -> str:
+    return os.path.join(_HERE, "liblmoe_oracle.so" if plant == 0 else f"liblmoe_oracle_plant{plant}.so")
+
+
+def build(plant: int = 0, force: bool = False) -> str:
+    out = lib_path(plant)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".{os.getpid()}.tmp"
+        flags = CFLAGS + ([f"-DLMOE_ORACLE_PLANT={plant}"] if plant else [])
+        subprocess.check_call(["gcc", *flags, _SRC, "-o", tmp, "-lm", "-lpthread"])
+        os.replace(tmp, out)
+    return out
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags.c_contiguous, "oracle wants C-contiguous numpy arrays"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """One loaded oracle library (the default build, or a planted-mistake variant)."""
+
+    def __init__(self, plant: int = 0, threads: int | None = None):
+        self.lib = ctypes.CDLL(build(plant))
+        L = self.lib
+        vp, dp = ctypes.c_void_p, ctypes.POINTER(OrDims)
+        L.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        L.oracle_bf16_rne.restype = ctypes.c_uint16
+        L.oracle_mxfp4_value.argtypes = [ctypes.c_uint, ctypes.c_uint]
+        L.oracle_mxfp4_value.restype = ctypes.c_float
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
+        L.oracle_get_threads.restype = ctypes.c_int
+        L.oracle_router_logits.argtypes = [dp, vp, vp, vp, vp, vp]
+        L.oracle_topk.argtypes = [dp, vp, vp, vp]
+        L.oracle_table.argtypes = [dp, vp, vp, vp, vp]
+        L.oracle_pool.argtypes = [dp, vp, vp, vp]
+        L.oracle_experts.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.oracle_norm_combine.argtypes = [dp, vp, vp, vp, vp, vp, vp]
+        L.oracle_unpool.argtypes = [dp, vp, vp, vp]
+        L.oracle_forward.argtypes = [dp] + [vp] * 16
+        for f in ("oracle_router_logits", "oracle_topk", "oracle_table", "oracle_pool", "oracle_experts",
+                  "oracle_norm_combine", "oracle_unpool", "oracle_forward", "oracle_set_threads"):
+            getattr(L, f).restype = None
+        self.set_threads(threads if threads else max(1, min(64, os.cpu_count() or 1)))
+
+    def set_threads(self, n: int):
+        self.lib.oracle_set_threads(int(n))
+
+    @property
+    def threads(self) -> int:
+        return self.lib.oracle_get_threads()
+
+    @staticmethod
+    def dims(d, T: int | None = None) -> OrDims:
+        return OrDims(d.T if T is None else T, d.H, d.L, d.I, d.E, d.k, d.eps)
+
+    # -- number formats -------------------------------------------------------------
+    def bf16_rne(self, f: float) -> int:
+        return int(self.lib.oracle_bf16_rne(f))
+
+    def mxfp4_value(self, code: int, scale: int) -> float:
+        return float(self.lib.oracle_mxfp4_value(code, scale))
+
+    # -- stages ---------------------------------------------------------------------
+    def router_logits(self, d, x, router_w, router_bias=None, want_absdot=False):
+        od = self.dims(d, x.shape[0])
+        logits = np.empty((od.T, d.E), np.float32)
+        absdot = np.empty((od.T, d.E), np.float64) if want_absdot else None
+        self.lib.oracle_router_logits(ctypes.byref(od), _p(x), _p(router_w), _p(router_bias), _p(logits), _p(absdot))
+        return (logits, absdot) if want_absdot else logits
+
+    def topk(self, d, logits):
+        od = self.dims(d, logits.shape[0])
+        idx = np.empty((od.T, d.k), np.int32)
+        w = np.empty((od.T, d.k), np.float32)
+        self.lib.oracle_topk(ctypes.byref(od), _p(np.ascontiguousarray(logits)), _p(idx), _p(w))
+        return idx, w
+
+    def table(self, d, topk_idx):
+        od = self.dims(d, topk_idx.shape[0])
+        R = od.T * d.k
+        offsets = np.empty(d.E + 1, np.int32)
+        sorted_rows = np.empty(R, np.int32)
+        row_pos = np.empty(R, np.int32)
+        self.lib.oracle_table(ctypes.byref(od), _p(np.ascontiguousarray(topk_idx)), _p(offsets), _p(sorted_rows), _p(row_pos))
+        return offsets, sorted_rows, row_pos
+
+    def pool(self, d, x, pooler_w):
+        od = self.dims(d, x.shape[0])
+        x_lat = np.empty((od.T, d.L), np.uint16)
+        self.lib.oracle_pool(ctypes.byref(od), _p(x), _p(pooler_w), _p(x_lat))
+        return x_lat
+
+    def experts(self, d, x_lat, topk_idx, w, want_intermediates=False):
+        od = self.dims(d, x_lat.shape[0])
+        R = od.T * d.k
+        y = np.empty((R, d.L), np.float32)
+        h = np.empty((R, d.I), np.uint16) if want_intermediates else None
+        gu = np.empty((R, 2 * d.I), np.float32) if want_intermediates else None
+        self.lib.oracle_experts(ctypes.byref(od), _p(x_lat), _p(np.ascontiguousarray(topk_idx)),
+                                _p(w["w13_q"]), _p(w["w13_s"]), _p(w["w2_q"]), _p(w["w2_s"]), _p(h), _p(gu), _p(y))
+        return (y, h, gu) if want_intermediates else y
+
+    def norm_combine(self, d, y, topk_idx, topk_w, norm_g, want_yhat=False):
+        T = topk_idx.shape[0]
+        od = self.dims(d, T)
+        z = np.empty((T, d.L), np.float32)
+        yhat = np.empty((T * d.k, d.L), np.float32) if want_yhat else None
+        self.lib.oracle_norm_combine(ctypes.byref(od), _p(y), _p(np.ascontiguousarray(topk_idx)),
+                                     _p(np.ascontiguousarray(topk_w)), _p(norm_g), _p(yhat), _p(z))
+        return (z, yhat) if want_yhat else z
+
+    def unpool(self, d, z, unpooler_w):
+        od = self.dims(d, z.shape[0])
+        out = np.empty((od.T, d.H), np.uint16)
+        self.lib.oracle_unpool(ctypes.byref(od), _p(z), _p(unpooler_w), _p(out))
+        return out
+
+    def forward(self, d, x, w):
+        """Whole layer; returns a dict of the output and every intermediate."""
+        T = x.shape[0]
+        od = self.dims(d, T)
+        R = T * d.k
+        res = {
+            "out": np.empty((T, d.H), np.uint16),
+            "topk_idx": np.empty((T, d.k), np.int32),
+            "topk_w": np.empty((T, d.k), np.float32),
+            "x_lat": np.empty((T, d.L), np.uint16),
+            "y": np.empty((R, d.L), np.float32),
+            "z": np.empty((T, d.L), np.float32),
+        }
+        self.lib.oracle_forward(ctypes.byref(od), _p(x), _p(w["router_w"]), _p(w.get("router_bias")),
+                                _p(w["pooler_w"]), _p(w["w13_q"]), _p(w["w13_s"]), _p(w["w2_q"]), _p(w["w2_s"]),
+                                _p(w["norm_g"]), _p(w["unpooler_w"]), _p(res["out"]), _p(res["topk_idx"]),
+                                _p(res["topk_w"]), _p(res["x_lat"]), _p(res["y"]), _p(res["z"]))
+        return res
+
+
+_default = None
+
+
+def get(threads: int | None = None) -> Oracle:
+    """The default (unplanted) oracle, loaded once."""
+    global _default
+    if _default is None:
+        _default = Oracle(0, threads)
+    elif threads:
+        _default.set_threads(threads)
+    return _default

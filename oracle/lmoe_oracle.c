@@ -1,0 +1,454 @@
+/*
+ * CPU oracle for the latent mixture-of-experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this code:
+ * only the tests, the package smoke check and the benchmark's CPU-baseline
+ * leg load it.  It shares no code with the CUDA library.
+ *
+ * What it computes follows the pages, stage by stage, in plain loops:
+ *
+ *  - "Muse Spark Open on Gaudi 2", section "What was built": the router is
+ *    fp32, 256 experts, top 8; experts run W4A16 (bf16 activations, MXFP4
+ *    weights), not W4A4.
+ *  - same page, "Why it needed a port": the MXFP4 checkpoint is read as packed
+ *    E2M1 nibbles plus E8M0 scale bytes.  The code table, the 32-element block
+ *    along K and the nibble order (low nibble = even element) are those of the
+ *    OCP Microscaling Formats (MX) v1.0 specification.
+ *  - same page, "The latent MoE: A' with a per-expert norm": every (token,
+ *    route) pair is its own row; post_expert_norm is applied to each row, the
+ *    rows are multiplied by the router weights and summed in fp32, then the
+ *    result is unpooled 4096 -> 8192.
+ *  - same page, "Correctness": the CPU reference keeps bf16 values with fp32
+ *    accumulation and dequantises MXFP4 exactly.
+ *  - "Soporte de dia 0 para Muse Spark Open en vLLM", section "MoE latente":
+ *    pooler (8192 -> 4096) and unpooler (4096 -> 8192) are learned
+ *    projections shared by all experts of the layer; experts work at 4096.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - router probabilities: softmax over all E logits, then the selected top-k
+ *    are renormalised to sum to one;
+ *  - top-k order: descending logit, ties to the lower expert index;
+ *  - router logit: the dot product is accumulated in fp64 and rounded once to
+ *    fp32 (the correctly rounded fp32 logit), then the optional bias is added
+ *    in fp32;
+ *  - expert MLP: rows 0..I-1 of W13 are the gate, rows I..2I-1 the up
+ *    projection, h = bf16(silu(gate) * up), y = h . W2^T, no bias or clamp;
+ *  - post_expert_norm: RMSNorm over the latent width with eps inside the
+ *    square root and a per-expert bf16 gain;
+ *  - bf16 round-to-nearest-even at x_lat, h, z (before the unpooler) and out;
+ *  - every weight matrix is stored [N_out][K_in], K contiguous.
+ *
+ * Sums run sequentially in index order in fp32 (compiled with
+ * -ffp-contract=off), so a result does not depend on the thread count.
+ *
+ * LMOE_ORACLE_PLANT (tests only): building with -DLMOE_ORACLE_PLANT=n plants
+ * one plausible mistake so the pin tests can show that they catch it.  The
+ * default build defines nothing and contains none of them.
+ *   1 nibble order swapped          2 gate and up swapped
+ *   3 W2 read transposed            4 block scale off by one
+ *   5 weights not renormalised      6 ties go to the higher index
+ *   7 norm applied to the sum       8 norm gain dropped
+ */
+#ifndef LMOE_ORACLE_PLANT
+#define LMOE_ORACLE_PLANT 0
+#endif
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  int32_t T, H, L, I, E, k;
+  float eps;
+} or_dims;
+
+/* ------------------------------------------------------------------------ */
+/* number formats                                                           */
+/* ------------------------------------------------------------------------ */
+
+static float bits_to_f32(uint32_t u) {
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static uint32_t f32_to_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return u;
+}
+
+/* bf16 -> fp32 is exact: the bf16 pattern is the top half of the fp32 one. */
+static float bf16_val(uint16_t b) { return bits_to_f32((uint32_t)b << 16); }
+
+/* fp32 -> bf16, round to nearest, ties to even; NaN stays a quiet NaN. */
+uint16_t oracle_bf16_rne(float f) {
+  uint32_t u = f32_to_bits(f);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+    return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t lower = u & 0xFFFFu;
+  uint32_t upper = u >> 16;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;
+  return (uint16_t)upper;
+}
+
+/* E2M1 (OCP MX v1.0): bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.
+ * Exponent field 0 is subnormal: value = mantissa * 0.5. */
+static float e2m1_value(unsigned code) {
+  unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+  float mag = (e == 0) ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, (int)e - 1);
+  return s ? -mag : mag;
+}
+
+/* E8M0: 2^(s-127); 255 is NaN (never produced by the generator). */
+static float e8m0_value(unsigned s) {
+  if (s == 255u) return NAN;
+  return ldexpf(1.0f, (int)s - 127 + (LMOE_ORACLE_PLANT == 4));
+}
+
+/* One dequantised MXFP4 element: value of code `code` under block scale `s`.
+ * Exact in fp32 for s <= 252 (the product has at most 2 significant bits). */
+float oracle_mxfp4_value(unsigned code, unsigned s) { return e2m1_value(code & 15u) * e8m0_value(s); }
+
+/* Element c of row n of a packed [N][K/2] code matrix with [N][K/32] scales. */
+static inline float mx_elem(const uint8_t* q, const uint8_t* sc, int64_t n, int64_t K, int64_t c) {
+  uint8_t byte = q[n * (K / 2) + c / 2];
+  unsigned code = ((c & 1) ^ (LMOE_ORACLE_PLANT == 1)) ? (byte >> 4) : (byte & 15u);
+  return oracle_mxfp4_value(code, sc[n * (K / 32) + c / 32]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* parallel for over an outer index: each index is computed by exactly one   */
+/* thread with the same sequential inner loops, so bits do not depend on the  */
+/* thread count                                                               */
+/* ------------------------------------------------------------------------ */
+
+static int g_threads = 1;
+void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : (n > 256 ? 256 : n); }
+int oracle_get_threads(void) { return g_threads; }
+
+typedef void (*body_fn)(void* ctx, int64_t i);
+typedef struct {
+  body_fn fn;
+  void* ctx;
+  int64_t n;
+  int tid, nth;
+} pf_job;
+
+static void* pf_run(void* arg) {
+  pf_job* j = (pf_job*)arg;
+  for (int64_t i = j->tid; i < j->n; i += j->nth) j->fn(j->ctx, i);
+  return NULL;
+}
+
+static void parallel_for(int64_t n, body_fn fn, void* ctx) {
+  int nth = g_threads;
+  if (nth > n) nth = (int)(n > 0 ? n : 1);
+  pthread_t th[256];
+  pf_job jobs[256];
+  for (int t = 0; t < nth; ++t) jobs[t] = (pf_job){fn, ctx, n, t, nth};
+  for (int t = 1; t < nth; ++t) pthread_create(&th[t], NULL, pf_run, &jobs[t]);
+  pf_run(&jobs[0]);
+  for (int t = 1; t < nth; ++t) pthread_join(th[t], NULL);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 1: router logits (fp32 router, "What was built")                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const or_dims* d;
+  const uint16_t* x;
+  const float* wr;
+  const float* bias;
+  float* logits;
+  double* absdot;
+} router_ctx;
+
+static void router_body(void* p, int64_t i) {
+  router_ctx* c = (router_ctx*)p;
+  int64_t t = i / c->d->E, e = i % c->d->E, H = c->d->H;
+  double acc = 0.0, mag = 0.0;
+  for (int64_t h = 0; h < H; ++h) {
+    double prod = (double)bf16_val(c->x[t * H + h]) * (double)c->wr[e * H + h];
+    acc += prod;
+    mag += fabs(prod);
+  }
+  float lg = (float)acc;
+  if (c->bias) lg = lg + c->bias[e];
+  c->logits[t * c->d->E + e] = lg;
+  if (c->absdot) c->absdot[t * c->d->E + e] = mag;
+}
+
+/* logits[t][e] = fp32(sum_h x[t][h] * Wr[e][h]) (+ bias[e]); absdot (optional)
+ * gets sum_h |x * Wr|, the scale of the rounding error of any fp32 sum. */
+void oracle_router_logits(const or_dims* d, const uint16_t* x, const float* router_w,
+                          const float* router_bias, float* logits, double* absdot) {
+  router_ctx c = {d, x, router_w, router_bias, logits, absdot};
+  parallel_for((int64_t)d->T * d->E, router_body, &c);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 2: top-k selection and softmax-renormalised weights                 */
+/* ------------------------------------------------------------------------ */
+
+/* For each token: the k largest logits in descending order (ties: lower
+ * index first), p = softmax over all E logits (fp64), w_j = p_j / sum_sel p. */
+void oracle_topk(const or_dims* d, const float* logits, int32_t* topk_idx, float* topk_w) {
+  int E = d->E, k = d->k;
+  char* taken = (char*)malloc((size_t)E);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  for (int t = 0; t < d->T; ++t) {
+    const float* lg = logits + (int64_t)t * E;
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+#if LMOE_ORACLE_PLANT == 6
+        if (best < 0 || lg[e] >= lg[best]) best = e;
+#else
+        if (best < 0 || lg[e] > lg[best]) best = e; /* strict '>' keeps the lower index on ties */
+#endif
+      }
+      taken[best] = 1;
+      topk_idx[t * k + j] = best;
+    }
+    double mx = lg[0];
+    for (int e = 1; e < E; ++e)
+      if (lg[e] > mx) mx = lg[e];
+    double den = 0.0;
+    for (int e = 0; e < E; ++e) {
+      p[e] = exp((double)lg[e] - mx);
+      den += p[e];
+    }
+    for (int e = 0; e < E; ++e) p[e] /= den;
+    double sel = 0.0;
+    for (int j = 0; j < k; ++j) sel += p[topk_idx[t * k + j]];
+    if (LMOE_ORACLE_PLANT == 5) sel = 1.0;
+    for (int j = 0; j < k; ++j) topk_w[t * k + j] = (float)(p[topk_idx[t * k + j]] / sel);
+  }
+  free(taken);
+  free(p);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 3: routing table: the (token, route) rows grouped by expert          */
+/* ("The latent MoE ...": each (token, route) pair is its own row)          */
+/* ------------------------------------------------------------------------ */
+
+/* Row id r = t*k + j.  offsets = exclusive scan of per-expert counts
+ * (E+1 entries); sorted_rows lists row ids by expert, ascending r within an
+ * expert; row_pos is the inverse permutation. */
+void oracle_table(const or_dims* d, const int32_t* topk_idx, int32_t* offsets,
+                  int32_t* sorted_rows, int32_t* row_pos) {
+  int E = d->E;
+  int64_t R = (int64_t)d->T * d->k;
+  int32_t* fill = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (int e = 0; e <= E; ++e) offsets[e] = 0;
+  for (int64_t r = 0; r < R; ++r) offsets[topk_idx[r] + 1] += 1;
+  for (int e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+  for (int64_t r = 0; r < R; ++r) {
+    int e = topk_idx[r];
+    int32_t pos = offsets[e] + fill[e]++;
+    sorted_rows[pos] = (int32_t)r;
+    row_pos[r] = pos;
+  }
+  free(fill);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 4: pooler, x_lat = bf16(x . P^T)  ("MoE latente")                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const or_dims* d;
+  const uint16_t* x;
+  const uint16_t* P;
+  uint16_t* x_lat;
+} pool_ctx;
+
+static void pool_body(void* p, int64_t i) {
+  pool_ctx* c = (pool_ctx*)p;
+  int64_t t = i / c->d->L, l = i % c->d->L, H = c->d->H;
+  float acc = 0.0f;
+  for (int64_t h = 0; h < H; ++h) acc += bf16_val(c->x[t * H + h]) * bf16_val(c->P[l * H + h]);
+  c->x_lat[t * c->d->L + l] = oracle_bf16_rne(acc);
+}
+
+void oracle_pool(const or_dims* d, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat) {
+  pool_ctx c = {d, x, pooler_w, x_lat};
+  parallel_for((int64_t)d->T * d->L, pool_body, &c);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 5: routed experts, W4A16 SwiGLU, one output row per (token, route)  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const or_dims* d;
+  const uint16_t* x_lat;
+  const int32_t* idx;
+  const uint8_t *w13q, *w13s, *w2q, *w2s;
+  uint16_t* h;  /* [R][I] bf16, required scratch */
+  float* gu;    /* [R][2I] optional pre-activation gate/up */
+  float* y;     /* [R][L] */
+} exp_ctx;
+
+/* phase 1 body: one (row, feature) pair -> gate, up, h */
+static void gateup_body(void* p, int64_t i) {
+  exp_ctx* c = (exp_ctx*)p;
+  int64_t I = c->d->I, L = c->d->L;
+  int64_t r = i / I, f = i % I;
+  int64_t t = r / c->d->k, e = c->idx[r];
+  const uint16_t* xr = c->x_lat + t * L;
+  int64_t gate_row = e * 2 * I + f, up_row = e * 2 * I + I + f;
+#if LMOE_ORACLE_PLANT == 2
+  { int64_t tmp = gate_row; gate_row = up_row; up_row = tmp; }
+#endif
+  float g = 0.0f, u = 0.0f;
+  for (int64_t l = 0; l < L; ++l) g += bf16_val(xr[l]) * mx_elem(c->w13q, c->w13s, gate_row, L, l);
+  for (int64_t l = 0; l < L; ++l) u += bf16_val(xr[l]) * mx_elem(c->w13q, c->w13s, up_row, L, l);
+  float silu = g / (1.0f + expf(-g));
+  c->h[r * I + f] = oracle_bf16_rne(silu * u);
+  if (c->gu) {
+    c->gu[r * 2 * I + f] = g;
+    c->gu[r * 2 * I + I + f] = u;
+  }
+}
+
+/* phase 2 body: one (row, latent column) pair -> y */
+static void down_body(void* p, int64_t i) {
+  exp_ctx* c = (exp_ctx*)p;
+  int64_t I = c->d->I, L = c->d->L;
+  int64_t r = i / L, l = i % L;
+  int64_t e = c->idx[r];
+  const uint16_t* hr = c->h + r * I;
+  float acc = 0.0f;
+#if LMOE_ORACLE_PLANT == 3
+  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * mx_elem(c->w2q, c->w2s, e * L + f, I, l);
+#else
+  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * mx_elem(c->w2q, c->w2s, e * L + l, I, f);
+#endif
+  c->y[r * L + l] = acc;
+}
+
+/* y[r][:] for every route row r = t*k + j with expert e = topk_idx[r].
+ * h_out (optional, [R][I] bf16) and gu_out (optional, [R][2I] fp32) expose
+ * the intermediate values. */
+void oracle_experts(const or_dims* d, const uint16_t* x_lat, const int32_t* topk_idx,
+                    const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
+                    const uint8_t* w2_s, uint16_t* h_out, float* gu_out, float* y) {
+  int64_t R = (int64_t)d->T * d->k;
+  uint16_t* h = h_out ? h_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(R * d->I));
+  exp_ctx c = {d, x_lat, topk_idx, w13_q, w13_s, w2_q, w2_s, h, gu_out, y};
+  parallel_for(R * d->I, gateup_body, &c);
+  parallel_for(R * d->L, down_body, &c);
+  if (!h_out) free(h);
+}
+
+/* ------------------------------------------------------------------------ */
+/* steps 6-7: post_expert_norm on each route row, then the fp32 weighted sum */
+/* ------------------------------------------------------------------------ */
+
+/* For each route row r (expert e): ms = sum_l y^2 / L, rinv = 1/sqrt(ms+eps),
+ * yhat[l] = (y[l] * rinv) * g[e][l].  z[t][l] = sum_j w[t][j] * yhat[t*k+j][l]
+ * in j order.  yhat_out (optional, [R][L]) exposes the normed rows. */
+void oracle_norm_combine(const or_dims* d, const float* y, const int32_t* topk_idx,
+                         const float* topk_w, const uint16_t* norm_g, float* yhat_out, float* z) {
+  int64_t L = d->L, k = d->k;
+  float* yh = (float*)malloc(sizeof(float) * (size_t)L);
+  for (int64_t t = 0; t < d->T; ++t) {
+    for (int64_t l = 0; l < L; ++l) z[t * L + l] = 0.0f;
+    for (int64_t j = 0; j < k; ++j) {
+      int64_t r = t * k + j, e = topk_idx[r];
+      const float* yr = y + r * L;
+      float ss = 0.0f;
+      for (int64_t l = 0; l < L; ++l) ss += yr[l] * yr[l];
+      float ms = ss / (float)L;
+      float rinv = 1.0f / sqrtf(ms + d->eps);
+#if LMOE_ORACLE_PLANT == 7
+      rinv = 1.0f;
+#endif
+#if LMOE_ORACLE_PLANT == 8
+      for (int64_t l = 0; l < L; ++l) yh[l] = yr[l] * rinv;
+#else
+      for (int64_t l = 0; l < L; ++l) yh[l] = (yr[l] * rinv) * bf16_val(norm_g[e * L + l]);
+#endif
+      if (yhat_out) memcpy(yhat_out + r * L, yh, sizeof(float) * (size_t)L);
+      float w = topk_w[r];
+      for (int64_t l = 0; l < L; ++l) z[t * L + l] += w * yh[l];
+    }
+#if LMOE_ORACLE_PLANT == 7
+    {
+      float ss = 0.0f;
+      for (int64_t l = 0; l < L; ++l) ss += z[t * L + l] * z[t * L + l];
+      float rinv = 1.0f / sqrtf(ss / (float)L + d->eps);
+      for (int64_t l = 0; l < L; ++l) z[t * L + l] *= rinv;
+    }
+#endif
+  }
+  free(yh);
+}
+
+/* ------------------------------------------------------------------------ */
+/* step 8: unpooler, out = bf16(bf16(z) . U^T)                              */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const or_dims* d;
+  const uint16_t* zb;
+  const uint16_t* U;
+  uint16_t* out;
+} unpool_ctx;
+
+static void unpool_body(void* p, int64_t i) {
+  unpool_ctx* c = (unpool_ctx*)p;
+  int64_t t = i / c->d->H, o = i % c->d->H, L = c->d->L;
+  float acc = 0.0f;
+  for (int64_t l = 0; l < L; ++l) acc += bf16_val(c->zb[t * L + l]) * bf16_val(c->U[o * L + l]);
+  c->out[t * c->d->H + o] = oracle_bf16_rne(acc);
+}
+
+void oracle_unpool(const or_dims* d, const float* z, const uint16_t* unpooler_w, uint16_t* out) {
+  int64_t n = (int64_t)d->T * d->L;
+  uint16_t* zb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n);
+  for (int64_t i = 0; i < n; ++i) zb[i] = oracle_bf16_rne(z[i]);
+  unpool_ctx c = {d, zb, unpooler_w, out};
+  parallel_for((int64_t)d->T * d->H, unpool_body, &c);
+  free(zb);
+}
+
+/* ------------------------------------------------------------------------ */
+/* whole layer                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Runs every step.  The optional outputs (any may be NULL) expose the
+ * intermediate results so each GPU call can be checked on its own. */
+void oracle_forward(const or_dims* d, const uint16_t* x, const float* router_w,
+                    const float* router_bias, const uint16_t* pooler_w, const uint8_t* w13_q,
+                    const uint8_t* w13_s, const uint8_t* w2_q, const uint8_t* w2_s,
+                    const uint16_t* norm_g, const uint16_t* unpooler_w, uint16_t* out,
+                    int32_t* topk_idx, float* topk_w, uint16_t* x_lat_out, float* y_out,
+                    float* z_out) {
+  int64_t T = d->T, R = T * d->k;
+  float* logits = (float*)malloc(sizeof(float) * (size_t)(T * d->E));
+  int32_t* idx = topk_idx ? topk_idx : (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+  float* w = topk_w ? topk_w : (float*)malloc(sizeof(float) * (size_t)R);
+  uint16_t* x_lat = x_lat_out ? x_lat_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(T * d->L));
+  float* y = y_out ? y_out : (float*)malloc(sizeof(float) * (size_t)(R * d->L));
+  float* z = z_out ? z_out : (float*)malloc(sizeof(float) * (size_t)(T * d->L));
+  oracle_router_logits(d, x, router_w, router_bias, logits, NULL);
+  oracle_topk(d, logits, idx, w);
+  oracle_pool(d, x, pooler_w, x_lat);
+  oracle_experts(d, x_lat, idx, w13_q, w13_s, w2_q, w2_s, NULL, NULL, y);
+  oracle_norm_combine(d, y, idx, w, norm_g, NULL, z);
+  oracle_unpool(d, z, unpooler_w, out);
+  free(logits);
+  if (!topk_idx) free(idx);
+  if (!topk_w) free(w);
+  if (!x_lat_out) free(x_lat);
+  if (!y_out) free(y);
+  if (!z_out) free(z);
+}

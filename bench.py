@@ -1,0 +1,370 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 latent-MoE layer (one JSON line on stdout).
+
+Workload (default): one decode step of the full layer -- T=1 token, hidden
+8192, latent 4096, 256 experts top-8, expert intermediate 4096, MXFP4 W4A16
+experts, bf16 pooler/unpooler, fp32 router -- on seeded synthetic inputs.
+A "step" is one lmoe_forward (router, top-k, table, pooler, experts,
+post_expert_norm, weighted sum, unpooler) over one batch of T tokens.
+
+  value   tokens/s of the whole job (all ranks), inputs resident in HBM,
+          device time from CUDA events, L2 flushed (512 MB write) between steps
+          outside the timed events
+  e2e     same metric with the x upload from pinned host memory and the
+          output download inside the timed region
+  roofline  the dominant kernel (expert gate/up) timed live with per-launch
+          CUDA events: algorithmic bytes per launch / mean launch duration,
+          against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle, as it stands, on a bounded sample of the same
+          workload on this host's cores
+
+--impl reference times the CPU oracle (the only reference this layer has) on
+the same workload and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs an independent replica (the layer is
+not sharded at these sizes); value = tokens of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "latent-MoE layer tokens/s and HBM GB/s (frac of roofline) at T=1..4096"
+EXPERT_BYTES = 26_738_688          # one expert: 3 matrices x (codes 8 MiB + scales 512 KiB)
+GATEUP_BYTES = 2 * EXPERT_BYTES // 3
+PROJ_BYTES = 134_217_728           # pooler + unpooler bf16
+GATEUP_LAUNCH = 5                  # launch index of the gate/up kernel inside lmoe_forward
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_name(d: synth.Dims, name: str) -> str:
+    s = " (skewed routing: +3.0 logit bias on experts 0..15)" if d.skewed else ""
+    return (f"latent-MoE layer {name}: T={d.T}, hidden {d.H}, latent {d.L}, {d.E} experts top-{d.k}, "
+            f"intermediate {d.I}, MXFP4 W4A16 experts, bf16 pooler/unpooler, fp32 router{s}")
+
+
+def traffic_from_profiles(kernel_src_hash: str):
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
+    if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "expert_gateup_decode_t1.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != kernel_src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("experts.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "latent_moe_layer_fp32_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_rate(d, hw, x, min_seconds=8.0, max_reps=30):
+    """Tokens/s of the CPU oracle on repeated whole-layer evaluations of `x`."""
+    import oracle
+    o = oracle.get()
+    reps, t0 = 0, time.perf_counter()
+    while reps < max_reps:
+        o.forward(d, x, hw)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return reps * d.T / dt, o.threads, reps, dt
+
+
+def run_reference(args, d, name, world, rank):
+    if rank != 0:
+        return
+    hw = synth.make_weights(d)
+    x = synth.make_x(d)
+    import oracle
+    o = oracle.get()
+    for _ in range(args.warmup):
+        o.forward(d, x, hw)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        o.forward(d, x, hw)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * d.T / total
+    sample = f"{name}: the whole layer for T={d.T} token(s) per step, full layer shape"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": workload_name(d, name), "T": d.T, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": o.threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode_t1", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    name = args.config
+    d = synth.CONFIGS[name]
+    world, rank, local = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        run_reference(args, d, name, world, rank)
+        return
+
+    import torch
+    import latent_moe_layer_fp32_gb300 as lm
+    lm.build()
+    lm.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    hw = synth.make_weights(d)
+    x = synth.make_x(d)
+
+    def to_dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w = {k: to_dev(v) for k, v in hw.items()}
+    wts = lm.weights_of(w)
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    x_dev = to_dev(x)
+    out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
+    x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty(d.T, d.H, dtype=torch.bfloat16).pin_memory()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+        rc = lm.lmoe_status_check(ws)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
+        launches_per_step = lm.lmoe_last_launch_count()
+        lay = lm.lmoe_workspace_layout(dims)
+        offs = ws[lay.expert_offsets:lay.expert_offsets + 4 * (d.E + 1)].view(torch.int32).cpu().numpy()
+        touched = int(np.count_nonzero(np.diff(offs)))
+
+        # ---- device-resident timed region ----
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        with Clocks(local) as clk:
+            for i in range(args.steps):
+                flush.zero_()
+                e0[i].record()
+                lm.lmoe_forward(dims, wts, x_dev, out, ws)
+                e1[i].record()
+            torch.cuda.synchronize()
+        barrier(world)
+        step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+        total_s = allreduce_max(world, sum(step_ms) / 1e3)
+        clocks = clk.summary()
+
+        # ---- end to end: host input upload and output download inside the timed region ----
+        for _ in range(2):
+            x_dev.copy_(x_host, non_blocking=True)
+            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+            out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            e0[i].record()
+            x_dev.copy_(x_host, non_blocking=True)
+            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+            out_host.copy_(out, non_blocking=True)
+            e1[i].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_s = allreduce_max(world, sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / 1e3)
+
+        # ---- dominant kernel, per-launch events ----
+        nev = launches_per_step + 1
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+        per_launch = [[] for _ in range(launches_per_step)]
+        lm.lmoe_profile_events(evs)
+        try:
+            for i in range(max(5, min(args.steps, 20))):
+                flush.zero_()
+                lm.lmoe_forward(dims, wts, x_dev, out, ws)
+                torch.cuda.synchronize()
+                for j in range(launches_per_step):
+                    per_launch[j].append(evs[j].elapsed_time(evs[j + 1]))
+        finally:
+            lm.lmoe_profile_events(None)
+        rc = lm.lmoe_status_check(ws)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
+
+    pk = peaks()
+    gate_ms = statistics.mean(per_launch[GATEUP_LAUNCH])
+    gate_bytes = touched * GATEUP_BYTES
+    achieved = gate_bytes / (gate_ms / 1e3) / 1e9
+    tokens = d.T * args.steps * world
+    value = tokens / total_s
+    layer_bytes = touched * EXPERT_BYTES + PROJ_BYTES
+    layer_gbs = layer_bytes * args.steps / (total_s if world == 1 else total_s) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random weights of the layer's shape)",
+        "config": {"workload": workload_name(d, name), "T": d.T, "touched_experts": touched,
+                   "l2": "flushed between steps (512 MB device write outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_gbs / pk["hbm_gbs"],
+        "layer_bytes_per_step": layer_bytes,
+        "roofline": {"bound": "hbm", "kernel": "expert gate/up (MXFP4 W4A16 + SwiGLU)", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": traffic_from_profiles(kernel_source_hash()),
+                     "algorithmic_bytes_per_launch": gate_bytes, "launch_ms": gate_ms,
+                     "peak_source": pk["source"]},
+        "kernels_ms": {str(j): statistics.mean(v) for j, v in enumerate(per_launch)},
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
+                "d2h_bytes_per_step": d.T * d.H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, reps, dt = cpu_oracle_rate(d, hw, x)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{reps} whole-layer evaluations of the T={d.T} workload ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * lmoe.h -- C ABI of the GB300 (sm_103a) latent mixture-of-experts layer.
+ *
+ * The layer ("Muse Spark Open on Gaudi 2", section "The latent MoE: A' with a
+ * per-expert norm"; "Soporte de dia 0 para Muse Spark Open en vLLM", section
+ * "MoE latente"):
+ *
+ *   logits = fp32(x) . Wr^T (+ bias)        fp32 router, E experts, top k
+ *   idx, w = top-k(logits), softmax over all E renormalised over the k picks
+ *   x_lat  = bf16(x . P^T)                   pooler   H -> L
+ *   per (token t, route j) row r = t*k + j, expert e = idx[t][j]:
+ *     h_r  = bf16(silu(x_lat[t] . Wg_e^T) * (x_lat[t] . Wu_e^T))   MXFP4 W4A16
+ *     y_r  = h_r . Wd_e^T                                          fp32, kept per row
+ *     yh_r = y_r * rsqrt(mean(y_r^2) + eps) * g_e                  post_expert_norm
+ *   z_t    = sum_j w[t][j] * yh_{t*k+j}      fp32, in route order j
+ *   out    = bf16(bf16(z) . U^T)             unpooler L -> H
+ *
+ * Conventions
+ *  - Every pointer argument is a DEVICE pointer owned by the caller unless a
+ *    comment says otherwise.  The library never allocates, frees or keeps a
+ *    pointer after a call returns.
+ *  - Matrices are row-major [N_out][K_in] (K contiguous).  bf16 tensors are
+ *    passed as uint16_t bit patterns.
+ *  - MXFP4 (OCP MX v1.0): codes [N][K/2] bytes, element 2m in the low nibble
+ *    of byte m, element 2m+1 in the high nibble; one E8M0 scale byte per 32
+ *    consecutive K elements, [N][K/32].  Weights are read as stored; there is
+ *    no repacking ("Muse Spark Open on Gaudi 2", "At a glance", "Why it
+ *    needed a port").
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous.  Host-detectable errors are returned
+ *    directly; errors found on the device (a wait that ran out, a routing
+ *    table entry out of range) are written to the status word inside the
+ *    workspace and read back with lmoe_status_check().
+ *  - Calls sharing one workspace must not overlap in time.
+ *  - Constraints checked on the host: hidden, latent, inter multiples of 128;
+ *    1 <= top_k <= 8; top_k <= n_experts <= 256; 1 <= T <= 65536; every
+ *    pointer 16-byte aligned; a compute-capability 10.3 device.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LMOE_API __attribute__((visibility("default")))
+#else
+#define LMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lmoe_stream_t; /* identical to cudaStream_t */
+
+enum {
+  LMOE_OK = 0,
+  LMOE_EINVAL = -1,        /* bad argument: null/misaligned pointer, bad dims */
+  LMOE_EUNSUPPORTED = -2,  /* dims or device outside what the kernels support */
+  LMOE_ECUDA = -3,         /* a CUDA runtime call failed */
+  LMOE_ETIMEOUT = -4,      /* a bounded device-side wait ran out */
+  LMOE_EDEVICE_CHECK = -5, /* a device-side input check failed (e.g. expert id) */
+  LMOE_EWORKSPACE = -6     /* workspace too small */
+};
+
+typedef struct {
+  int32_t T;         /* tokens in this call */
+  int32_t hidden;    /* H, e.g. 8192 */
+  int32_t latent;    /* L, e.g. 4096 */
+  int32_t inter;     /* I, expert intermediate width, e.g. 4096 */
+  int32_t n_experts; /* E, e.g. 256 */
+  int32_t top_k;     /* k, e.g. 8 */
+  float eps;         /* post_expert_norm epsilon, e.g. 1e-6 */
+} lmoe_dims;
+
+typedef struct {
+  const float* router_w;      /* fp32 [E][H] */
+  const float* router_bias;   /* fp32 [E], or NULL for none */
+  const uint16_t* pooler_w;   /* bf16 [L][H] */
+  const uint8_t* w13_q;       /* MXFP4 codes [E][2I][L/2]; rows 0..I-1 gate, I..2I-1 up */
+  const uint8_t* w13_s;       /* E8M0 scales [E][2I][L/32] */
+  const uint8_t* w2_q;        /* MXFP4 codes [E][L][I/2] (down projection) */
+  const uint8_t* w2_s;        /* E8M0 scales [E][L][I/32] */
+  const uint16_t* norm_g;     /* bf16 [E][L], per-expert post_expert_norm gain */
+  const uint16_t* unpooler_w; /* bf16 [H][L] */
+} lmoe_weights;
+
+/* Byte offsets of the intermediates that lmoe_forward leaves in the workspace
+ * (for inspection and tests; valid after the stream has reached the end of
+ * the call).  Offsets are from the workspace base. */
+typedef struct {
+  size_t status;         /* int32[2]: code, location */
+  size_t topk_idx;       /* int32 [T][k] */
+  size_t topk_w;         /* fp32 [T][k] */
+  size_t expert_offsets; /* int32 [E+1] */
+  size_t sorted_rows;    /* int32 [T*k] */
+  size_t row_pos;        /* int32 [T*k] */
+  size_t x_lat;          /* bf16 [T][L] */
+  size_t y;              /* fp32 [T*k][L], row t*k+j */
+  size_t z;              /* bf16 [T][L], bf16(z) as fed to the unpooler */
+  size_t total;          /* = lmoe_workspace_bytes() */
+} lmoe_ws_layout;
+
+/* Workspace size in bytes for `dims` (0 if dims are invalid).  The workspace
+ * must be 256-byte aligned device memory; its contents need no
+ * initialisation and are overwritten by every call. */
+LMOE_API size_t lmoe_workspace_bytes(const lmoe_dims* dims);
+
+/* Fills `layout` for `dims`.  Returns LMOE_OK or LMOE_EINVAL. */
+LMOE_API int lmoe_workspace_layout(const lmoe_dims* dims, lmoe_ws_layout* layout);
+
+/* Router, top-k and routing table ("Muse Spark Open on Gaudi 2", "What was
+ * built": fp32 router, 256 experts, top 8; "The latent MoE: A' with a
+ * per-expert norm": one row per (token, route)).
+ *   x              bf16 [T][H], the layer input
+ *   router_w       fp32 [E][H];  router_bias fp32 [E] or NULL
+ *   topk_idx       out int32 [T][k], descending logit, ties to the lower index
+ *   topk_w         out fp32 [T][k], softmax over all E renormalised over the k
+ *   expert_offsets out int32 [E+1], exclusive scan of per-expert row counts
+ *   sorted_rows    out int32 [T*k], row ids r = t*k+j grouped by expert,
+ *                  ascending r within an expert
+ *   row_pos        out int32 [T*k], inverse of sorted_rows
+ * Logits are fp32 sums of fp32 products (not TF32). */
+LMOE_API int lmoe_route(const lmoe_dims* dims, const uint16_t* x, const float* router_w, const float* router_bias,
+               int32_t* topk_idx, float* topk_w, int32_t* expert_offsets, int32_t* sorted_rows,
+               int32_t* row_pos, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
+/* Pooler ("Soporte de dia 0 ...", "MoE latente": 8192 -> 4096 learned
+ * projection shared by all experts).
+ *   x        bf16 [T][H];  pooler_w bf16 [L][H]
+ *   x_lat    out bf16 [T][L] = bf16_rne(sum_h x*P), fp32 accumulation. */
+LMOE_API int lmoe_pool(const lmoe_dims* dims, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
+              void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
+/* Routed experts, MXFP4 W4A16 SwiGLU, one output row per (token, route)
+ * ("Muse Spark Open on Gaudi 2", "What was built": W4A16; "The latent MoE
+ * ...": per-route rows, cost per touched expert slice).
+ *   x_lat          bf16 [T][L]
+ *   expert_offsets int32 [E+1] and sorted_rows int32 [T*k] as from lmoe_route
+ *   w13_q/w13_s, w2_q/w2_s as in lmoe_weights
+ *   y              out fp32 [T*k][L]; row r = t*k+j holds expert idx[t][j]'s
+ *                  output for token t (before the norm)
+ * Each touched expert slice is streamed from HBM once per group of up to 8
+ * of its rows.  A row id outside [0, T*k) or offsets that are not monotone
+ * are reported as LMOE_EDEVICE_CHECK in the status word. */
+LMOE_API int lmoe_experts_mxfp4(const lmoe_dims* dims, const uint16_t* x_lat, const int32_t* expert_offsets,
+                       const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s,
+                       const uint8_t* w2_q, const uint8_t* w2_s, float* y, void* ws, size_t ws_bytes,
+                       lmoe_stream_t stream);
+
+/* post_expert_norm on every route row, fp32 router-weighted sum, unpooler
+ * ("Muse Spark Open on Gaudi 2", "The latent MoE ...": norm per row, then
+ * x router weight, fp32 sum, unpool 4096 -> 8192; "Why it needed a port":
+ * the norm applies to each expert's output before the weighted sum).
+ *   y        fp32 [T*k][L];  topk_idx int32 [T][k];  topk_w fp32 [T][k]
+ *   norm_g   bf16 [E][L];    unpooler_w bf16 [H][L]
+ *   out      out bf16 [T][H] */
+LMOE_API int lmoe_norm_combine_unpool(const lmoe_dims* dims, const float* y, const int32_t* topk_idx,
+                             const float* topk_w, const uint16_t* norm_g, const uint16_t* unpooler_w,
+                             uint16_t* out, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
+/* The whole layer: route, pool, experts, norm + combine + unpool.
+ *   x   bf16 [T][H];  out bf16 [T][H]
+ * Intermediates stay in the workspace (see lmoe_workspace_layout). */
+LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x, uint16_t* out,
+                 void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
+/* Synchronises `stream`, reads the device status word of `ws` and returns it
+ * (LMOE_OK, LMOE_ETIMEOUT or LMOE_EDEVICE_CHECK), or LMOE_ECUDA if the
+ * stream itself reports an error.  `ws` is a device pointer. */
+LMOE_API int lmoe_status_check(const void* ws, lmoe_stream_t stream);
+
+/* Static description of an error code (never NULL). */
+LMOE_API const char* lmoe_error_string(int code);
+
+/* Number of kernel launches the last lmoe_* call on this thread enqueued. */
+LMOE_API int lmoe_last_launch_count(void);
+
+/* Optional per-launch timing: while set, every kernel launch i of the
+ * following lmoe_* calls on this host thread is preceded by
+ * cudaEventRecord(events[i], stream), and the end of each call records
+ * events[launches] (as far as n allows).  `events` holds cudaEvent_t handles
+ * owned by the caller; pass n = 0 to switch off.  Recording events between
+ * launches serialises the kernels, so use it only to time kernels. */
+LMOE_API int lmoe_profile_events(void* const* events, int n);
+
+/* Format self-check: converts every byte value b (two E2M1 codes, low nibble
+ * first) with the same in-register conversion the expert kernels use and
+ * writes the two values as fp32 to out[2*b], out[2*b+1] (device pointer,
+ * 512 floats).  Synchronous. */
+LMOE_API int lmoe_selftest_e2m1(float* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMOE_H */

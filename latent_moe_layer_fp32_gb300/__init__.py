@@ -1,0 +1,212 @@
+"""Python binding of the GB300 latent mixture-of-experts layer (``liblmoe.so``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions carry the C names of ``include/lmoe.h`` and take torch
+CUDA tensors (device memory and the current stream come from PyTorch).  There
+is no CPU fallback: if the library is missing or cannot load, importing the
+binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+from ._build import build, up_to_date
+
+__all__ = [
+    "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
+    "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4",
+    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_status_check", "lmoe_error_string",
+    "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
+]
+
+LMOE_OK, LMOE_EINVAL, LMOE_EUNSUPPORTED, LMOE_ECUDA, LMOE_ETIMEOUT, LMOE_EDEVICE_CHECK, LMOE_EWORKSPACE = \
+    0, -1, -2, -3, -4, -5, -6
+
+
+class LmoeDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("hidden", ctypes.c_int32), ("latent", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
+
+
+class LmoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("router_w", "router_bias", "pooler_w", "w13_q", "w13_s", "w2_q",
+                                               "w2_s", "norm_g", "unpooler_w")]
+
+
+class LmoeWsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("status", "topk_idx", "topk_w", "expert_offsets", "sorted_rows",
+                                               "row_pos", "x_lat", "y", "z", "total")]
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {lmoe_error_string(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"liblmoe.so is not built ({path}); run latent_moe_layer_fp32_gb300.build() "
+                          "or __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, dp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(LmoeDims)
+    lib.lmoe_workspace_bytes.argtypes = [dp]
+    lib.lmoe_workspace_bytes.restype = sz
+    lib.lmoe_workspace_layout.argtypes = [dp, ctypes.POINTER(LmoeWsLayout)]
+    lib.lmoe_route.argtypes = [dp] + [vp] * 8 + [vp, sz, vp]
+    lib.lmoe_pool.argtypes = [dp, vp, vp, vp, vp, sz, vp]
+    lib.lmoe_experts_mxfp4.argtypes = [dp] + [vp] * 8 + [vp, sz, vp]
+    lib.lmoe_norm_combine_unpool.argtypes = [dp] + [vp] * 6 + [vp, sz, vp]
+    lib.lmoe_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
+    lib.lmoe_status_check.argtypes = [vp, vp]
+    lib.lmoe_error_string.argtypes = [i32]
+    lib.lmoe_error_string.restype = ctypes.c_char_p
+    lib.lmoe_last_launch_count.argtypes = []
+    lib.lmoe_selftest_e2m1.argtypes = [vp]
+    lib.lmoe_profile_events.argtypes = [vp, i32]
+    for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
+              "lmoe_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
+              "lmoe_profile_events"):
+        getattr(lib, f).restype = i32
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------------
+
+def _ptr(t, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor (the library takes device pointers)")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype is not None and t.dtype not in dtype:
+        raise TypeError(f"unexpected dtype {t.dtype}, want one of {dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+_U8 = (torch.uint8,)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != LMOE_OK:
+        raise LmoeError(rc, what)
+
+
+def dims_of(T, hidden, latent, inter, n_experts, top_k, eps=1e-6) -> LmoeDims:
+    return LmoeDims(T, hidden, latent, inter, n_experts, top_k, eps)
+
+
+def weights_of(w: dict) -> LmoeWeights:
+    """LmoeWeights from a dict of device tensors (keys as in the struct)."""
+    return LmoeWeights(
+        _ptr(w["router_w"], _F32), _ptr(w.get("router_bias"), _F32), _ptr(w["pooler_w"], _BF16),
+        _ptr(w["w13_q"], _U8), _ptr(w["w13_s"], _U8), _ptr(w["w2_q"], _U8), _ptr(w["w2_s"], _U8),
+        _ptr(w["norm_g"], _BF16), _ptr(w["unpooler_w"], _BF16))
+
+
+# ---------------------------------------------------------------------------------------------
+# the C calls
+# ---------------------------------------------------------------------------------------------
+
+def lmoe_error_string(code: int) -> str:
+    return load().lmoe_error_string(int(code)).decode()
+
+
+def lmoe_workspace_bytes(dims: LmoeDims) -> int:
+    return int(load().lmoe_workspace_bytes(ctypes.byref(dims)))
+
+
+def lmoe_workspace_layout(dims: LmoeDims) -> LmoeWsLayout:
+    out = LmoeWsLayout()
+    _check(load().lmoe_workspace_layout(ctypes.byref(dims), ctypes.byref(out)), "lmoe_workspace_layout")
+    return out
+
+
+def lmoe_route(dims, x, router_w, router_bias, topk_idx, topk_w, expert_offsets, sorted_rows, row_pos, ws,
+               stream=None):
+    _check(load().lmoe_route(ctypes.byref(dims), _ptr(x, _BF16), _ptr(router_w, _F32), _ptr(router_bias, _F32),
+                             _ptr(topk_idx, _I32), _ptr(topk_w, _F32), _ptr(expert_offsets, _I32),
+                             _ptr(sorted_rows, _I32), _ptr(row_pos, _I32), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)), "lmoe_route")
+
+
+def lmoe_pool(dims, x, pooler_w, x_lat, ws=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().lmoe_pool(ctypes.byref(dims), _ptr(x, _BF16), _ptr(pooler_w, _BF16), _ptr(x_lat, _BF16),
+                            _ptr(ws), nbytes, _stream(stream)), "lmoe_pool")
+
+
+def lmoe_experts_mxfp4(dims, x_lat, expert_offsets, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, stream=None):
+    _check(load().lmoe_experts_mxfp4(ctypes.byref(dims), _ptr(x_lat, _BF16), _ptr(expert_offsets, _I32),
+                                     _ptr(sorted_rows, _I32), _ptr(w13_q, _U8), _ptr(w13_s, _U8), _ptr(w2_q, _U8),
+                                     _ptr(w2_s, _U8), _ptr(y, _F32), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "lmoe_experts_mxfp4")
+
+
+def lmoe_norm_combine_unpool(dims, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, stream=None):
+    _check(load().lmoe_norm_combine_unpool(ctypes.byref(dims), _ptr(y, _F32), _ptr(topk_idx, _I32),
+                                           _ptr(topk_w, _F32), _ptr(norm_g, _BF16), _ptr(unpooler_w, _BF16),
+                                           _ptr(out, _BF16), _ptr(ws), ws.numel() * ws.element_size(),
+                                           _stream(stream)), "lmoe_norm_combine_unpool")
+
+
+def lmoe_forward(dims, weights: LmoeWeights, x, out, ws, stream=None):
+    _check(load().lmoe_forward(ctypes.byref(dims), ctypes.byref(weights), _ptr(x, _BF16), _ptr(out, _BF16),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "lmoe_forward")
+
+
+def lmoe_status_check(ws, stream=None) -> int:
+    return int(load().lmoe_status_check(_ptr(ws), _stream(stream)))
+
+
+def lmoe_last_launch_count() -> int:
+    return int(load().lmoe_last_launch_count())
+
+
+_event_array = None
+
+
+def lmoe_profile_events(events):
+    """Record events[i] before launch i of the following calls (None to stop).
+    `events` are torch.cuda.Event(enable_timing=True) objects."""
+    global _event_array
+    if not events:
+        _event_array = None
+        _check(load().lmoe_profile_events(None, 0), "lmoe_profile_events")
+        return
+    for e in events:
+        e.record()  # make sure the underlying CUDA event exists
+    torch.cuda.synchronize()
+    _event_array = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(load().lmoe_profile_events(_event_array, len(events)), "lmoe_profile_events")
+
+
+def lmoe_selftest_e2m1(out):
+    _check(load().lmoe_selftest_e2m1(_ptr(out, _F32)), "lmoe_selftest_e2m1")

@@ -1,0 +1,374 @@
+// C ABI of the latent-MoE layer: argument checks, workspace carving and the
+// launch sequences.  See include/lmoe.h for the contract of every call.
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace lmoe;
+
+namespace {
+
+thread_local int g_launches = 0;
+thread_local void* const* g_events = nullptr;
+thread_local int g_nevents = 0;
+
+void pre_launch(cudaStream_t s) {
+  if (g_events && g_launches < g_nevents) cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
+}
+
+int post_call(cudaStream_t s, int rc) {
+  if (rc == LMOE_OK && g_events && g_launches < g_nevents)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
+  return rc;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+int dev_info(DevInfo* out) {
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ECUDA;
+  DevInfo& c = cache[dev & 63];
+  if (c.sms == 0) {
+    if (cudaDeviceGetAttribute(&c.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LMOE_ECUDA;
+  }
+  *out = c;
+  if (c.major != 10 || c.minor != 3) return LMOE_EUNSUPPORTED;
+  return LMOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const lmoe_dims* d) {
+  if (!d) return LMOE_EINVAL;
+  if (d->T < 1 || d->T > 65536 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k ||
+      d->n_experts > 256 || d->hidden < 128 || d->latent < 128 || d->inter < 128 || d->hidden % 128 ||
+      d->latent % 128 || d->inter % 128 || !(d->eps >= 0.f))
+    return LMOE_EINVAL;
+  if (d->latent > 4096 || d->inter > 4096) return LMOE_EUNSUPPORTED;  // expert stage holds K/32 <= 128 scales
+  return LMOE_OK;
+}
+
+size_t al(size_t x) { return (x + 255) & ~size_t(255); }
+
+int router_splits(const lmoe_dims* d, int sms) {
+  const int base = ((d->n_experts + 31) / 32) * ((d->T + 7) / 8);
+  int ns = 1;
+  while (base * ns < 2 * sms && ns < 16 && d->hidden % (128 * ns * 2) == 0) ns *= 2;
+  return ns;
+}
+
+struct WsLayout {
+  lmoe_ws_layout pub;
+  size_t n_groups, groups, part, x16, xexp, h, h16, hexp;
+  int nsplit;
+};
+
+int layout(const lmoe_dims* d, int sms, WsLayout* w) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  const size_t T = d->T, E = d->n_experts, k = d->top_k, R = T * k, L = d->latent, I = d->inter;
+  w->nsplit = router_splits(d, sms);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = al(o + bytes);
+    return at;
+  };
+  w->pub.status = take(64);
+  w->n_groups = w->pub.status + 16;
+  w->pub.topk_idx = take(4 * R);
+  w->pub.topk_w = take(4 * R);
+  w->pub.expert_offsets = take(4 * (E + 1));
+  w->pub.sorted_rows = take(4 * R);
+  w->pub.row_pos = take(4 * R);
+  w->groups = take(16 * (R + E + 1));
+  w->part = take(4 * (size_t)16 * T * E);
+  w->pub.x_lat = take(2 * T * L);
+  w->x16 = take(2 * T * L);
+  w->xexp = take(4 * T);
+  w->h = take(2 * R * I);
+  w->h16 = take(2 * R * I);
+  w->hexp = take(4 * R);
+  w->pub.y = take(4 * R * L);
+  w->pub.z = take(2 * T * L);
+  w->pub.total = o;
+  return LMOE_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+#define LAUNCH(grid, block, stream, kern, ...)                                   \
+  do {                                                                           \
+    cudaLaunchAttribute attr_[1];                                                \
+    cudaLaunchConfig_t cfg_ = pdl_cfg(grid, block, stream, attr_);               \
+    pre_launch(stream);                                                          \
+    if (cudaLaunchKernelEx(&cfg_, kern, __VA_ARGS__) != cudaSuccess) return LMOE_ECUDA; \
+    ++g_launches;                                                                \
+  } while (0)
+
+#define CHECK(x)                 \
+  do {                           \
+    int rc_ = (x);               \
+    if (rc_ != LMOE_OK) return rc_; \
+  } while (0)
+
+int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayout* w, cudaStream_t s,
+             bool need_ws = true) {
+  g_launches = 0;
+  CHECK(check_dims(d));
+  CHECK(dev_info(di));
+  CHECK(layout(d, di->sms, w));
+  if (need_ws) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
+    if (ws_bytes < w->pub.total) return LMOE_EWORKSPACE;
+    if (cudaMemsetAsync(at<char>(ws, w->pub.status), 0, 64, s) != cudaSuccess) return LMOE_ECUDA;
+  }
+  return LMOE_OK;
+}
+
+int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x, const float* router_w,
+              const float* router_bias, int32_t* topk_idx, float* topk_w, int32_t* offsets, int32_t* sorted_rows,
+              int32_t* row_pos, void* ws, cudaStream_t s) {
+  const int T = d->T, E = d->n_experts, k = d->top_k, H = d->hidden;
+  Status* st = at<Status>(ws, w.pub.status);
+  float* part = at<float>(ws, w.part);
+  LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T, H,
+         E, H / w.nsplit);
+  LAUNCH(dim3((T + 7) / 8), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
+         topk_w);
+  LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, expert_max_group(T), offsets,
+         sorted_rows, row_pos, at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), st);
+  return LMOE_OK;
+}
+
+int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
+             Status* st, cudaStream_t s) {
+  GemvArgs g{pooler_w, x, x_lat, d->latent, d->hidden, d->T, st};
+  pre_launch(s);
+  CHECK(launch_gemv_bf16(g, s, di.sms));
+  ++g_launches;
+  return LMOE_OK;
+}
+
+// groups must already be in the workspace
+int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
+                const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
+                const uint8_t* w2_s, float* y, void* ws, cudaStream_t s) {
+  const int T = d->T, k = d->top_k, R = T * k, L = d->latent, I = d->inter;
+  Status* st = at<Status>(ws, w.pub.status);
+  LAUNCH(dim3(T), dim3(256), s, prep_act_kernel, x_lat, L, at<uint16_t>(ws, w.x16), at<int32_t>(ws, w.xexp));
+  const int G = expert_max_group(T);
+  ExpertArgs a{};
+  a.groups = at<int4>(ws, w.groups);
+  a.n_groups = at<int32_t>(ws, w.n_groups);
+  a.sorted_rows = sorted_rows;
+  a.inter = I;
+  a.latent = L;
+  a.top_k = k;
+  a.st = st;
+  a.q = w13_q;
+  a.s = w13_s;
+  a.act16 = at<uint16_t>(ws, w.x16);
+  a.act_exp = at<int32_t>(ws, w.xexp);
+  a.K = L;
+  a.h_out = at<uint16_t>(ws, w.h);
+  pre_launch(s);
+  CHECK(launch_gateup(a, T, G, s, di.sms));
+  ++g_launches;
+  LAUNCH(dim3(R), dim3(256), s, prep_act_kernel, (const uint16_t*)at<uint16_t>(ws, w.h), I, at<uint16_t>(ws, w.h16),
+         at<int32_t>(ws, w.hexp));
+  a.q = w2_q;
+  a.s = w2_s;
+  a.act16 = at<uint16_t>(ws, w.h16);
+  a.act_exp = at<int32_t>(ws, w.hexp);
+  a.K = I;
+  a.h_out = nullptr;
+  a.y_out = y;
+  pre_launch(s);
+  CHECK(launch_down(a, T, G, s, di.sms));
+  ++g_launches;
+  return LMOE_OK;
+}
+
+int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const float* y,
+                       const int32_t* topk_idx, const float* topk_w, const uint16_t* norm_g,
+                       const uint16_t* unpooler_w, uint16_t* out, void* ws, cudaStream_t s) {
+  Status* st = at<Status>(ws, w.pub.status);
+  uint16_t* zb = at<uint16_t>(ws, w.pub.z);
+  LAUNCH(dim3(d->T), dim3(256), s, combine_kernel, y, topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts,
+         d->eps, zb, st);
+  GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st};
+  pre_launch(s);
+  CHECK(launch_gemv_bf16(g, s, di.sms));
+  ++g_launches;
+  return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lmoe_workspace_bytes(const lmoe_dims* d) {
+  DevInfo di;
+  int sms = (dev_info(&di) == LMOE_OK) ? di.sms : 148;
+  WsLayout w;
+  if (layout(d, sms, &w) != LMOE_OK) return 0;
+  return w.pub.total;
+}
+
+int lmoe_workspace_layout(const lmoe_dims* d, lmoe_ws_layout* out) {
+  if (!out) return LMOE_EINVAL;
+  DevInfo di;
+  int sms = (dev_info(&di) == LMOE_OK) ? di.sms : 148;
+  WsLayout w;
+  CHECK(layout(d, sms, &w));
+  *out = w.pub;
+  return LMOE_OK;
+}
+
+int lmoe_route(const lmoe_dims* d, const uint16_t* x, const float* router_w, const float* router_bias,
+               int32_t* topk_idx, float* topk_w, int32_t* expert_offsets, int32_t* sorted_rows, int32_t* row_pos,
+               void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  if (!aligned16(x) || !aligned16(router_w) || !topk_idx || !topk_w || !expert_offsets || !sorted_rows ||
+      !row_pos || (router_bias && !aligned16(router_bias)))
+    return LMOE_EINVAL;
+  return post_call(s, run_route(d, w, di, x, router_w, router_bias, topk_idx, topk_w, expert_offsets, sorted_rows,
+                                row_pos, ws, s));
+}
+
+int lmoe_pool(const lmoe_dims* d, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat, void* ws,
+              size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s, ws != nullptr));
+  if (!aligned16(x) || !aligned16(pooler_w) || !aligned16(x_lat) || !x || !pooler_w || !x_lat) return LMOE_EINVAL;
+  Status* st = ws ? at<Status>(ws, w.pub.status) : nullptr;
+  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, st, s));
+}
+
+int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
+                       const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
+                       const uint8_t* w2_s, float* y, void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  const void* ptrs[] = {x_lat, expert_offsets, sorted_rows, w13_q, w13_s, w2_q, w2_s, y};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  const int R = d->T * d->top_k;
+  LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
+         expert_max_group(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
+  return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s));
+}
+
+int lmoe_norm_combine_unpool(const lmoe_dims* d, const float* y, const int32_t* topk_idx, const float* topk_w,
+                             const uint16_t* norm_g, const uint16_t* unpooler_w, uint16_t* out, void* ws,
+                             size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  const void* ptrs[] = {y, topk_idx, topk_w, norm_g, unpooler_w, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  return post_call(s, run_combine_unpool(d, w, di, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, s));
+}
+
+int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, uint16_t* out, void* ws,
+                 size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  if (!wt || !x || !out || !aligned16(x) || !aligned16(out)) return LMOE_EINVAL;
+  const void* ptrs[] = {wt->router_w, wt->pooler_w, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, wt->norm_g,
+                        wt->unpooler_w};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  if (wt->router_bias && !aligned16(wt->router_bias)) return LMOE_EINVAL;
+  int32_t* idx = at<int32_t>(ws, w.pub.topk_idx);
+  float* tw = at<float>(ws, w.pub.topk_w);
+  int32_t* srows = at<int32_t>(ws, w.pub.sorted_rows);
+  uint16_t* x_lat = at<uint16_t>(ws, w.pub.x_lat);
+  float* y = at<float>(ws, w.pub.y);
+  Status* st = at<Status>(ws, w.pub.status);
+  CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets), srows,
+                  at<int32_t>(ws, w.pub.row_pos), ws, s));
+  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s));
+  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s));
+  return post_call(s, LMOE_OK);
+}
+
+int lmoe_status_check(const void* ws, lmoe_stream_t stream) {
+  if (!ws) return LMOE_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LMOE_ECUDA;
+  Status h{};
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ECUDA;
+  return h.code;
+}
+
+const char* lmoe_error_string(int code) {
+  switch (code) {
+    case LMOE_OK: return "ok";
+    case LMOE_EINVAL: return "invalid argument (null or misaligned pointer, or dims out of range)";
+    case LMOE_EUNSUPPORTED: return "unsupported dims or device (needs compute capability 10.3)";
+    case LMOE_ECUDA: return "CUDA runtime error";
+    case LMOE_ETIMEOUT: return "a bounded device-side wait ran out";
+    case LMOE_EDEVICE_CHECK: return "device-side input check failed (routing table out of range)";
+    case LMOE_EWORKSPACE: return "workspace too small";
+    default: return "unknown error";
+  }
+}
+
+int lmoe_last_launch_count(void) { return g_launches; }
+
+int lmoe_profile_events(void* const* events, int n) {
+  if (n < 0 || (n > 0 && !events)) return LMOE_EINVAL;
+  g_events = n > 0 ? events : nullptr;
+  g_nevents = n;
+  return LMOE_OK;
+}
+
+int lmoe_selftest_e2m1(float* out) {
+  if (!out || !aligned16(out)) return LMOE_EINVAL;
+  DevInfo di;
+  CHECK(dev_info(&di));
+  e2m1_selftest_kernel<<<1, 256>>>(out);
+  if (cudaGetLastError() != cudaSuccess) return LMOE_ECUDA;
+  return cudaDeviceSynchronize() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+}
+
+}  // extern "C"

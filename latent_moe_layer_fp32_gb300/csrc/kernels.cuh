@@ -1,0 +1,60 @@
+// Kernel declarations and launch-side configuration shared by the .cu files.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace lmoe {
+
+// ---- route.cu -------------------------------------------------------------
+__global__ void router_partial_kernel(const uint16_t* x, const float* wr, float* part, int T, int H, int E,
+                                      int split_len);
+__global__ void topk_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,
+                            int32_t* topk_idx, float* topk_w);
+__global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32_t* offsets, int32_t* sorted_rows,
+                             int32_t* row_pos, int4* groups, int32_t* n_groups, Status* st);
+
+// ---- experts.cu -----------------------------------------------------------
+// Group of up to G rows (sorted positions p0 .. p0+n-1) of one expert e:
+// int4 {e, p0, n, 0}.
+struct ExpertArgs {
+  const uint8_t* q;         // codes [E][rows_per_expert][K/2]
+  const uint8_t* s;         // scales [E][rows_per_expert][K/32]
+  const uint16_t* act16;    // f16 activations, row-major [*][K]
+  const int32_t* act_exp;   // per activation row: power-of-two exponent applied
+  const int4* groups;       // group list
+  const int32_t* n_groups;  // device count of groups
+  const int32_t* sorted_rows;
+  int K;                    // reduction width (L for gate/up, I for down)
+  int kc;                   // K chunk per stage
+  int inter;                // I
+  int latent;               // L
+  int top_k;
+  uint16_t* h_out;          // gate/up: bf16 [R_sorted][I]
+  float* y_out;             // down: fp32 [R][L] by original row id
+  Status* st;
+};
+
+int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms);
+int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms);
+int expert_max_group(int T);
+
+// ---- gemv.cu --------------------------------------------------------------
+struct GemvArgs {
+  const uint16_t* w;    // bf16 [N][K]
+  const uint16_t* act;  // bf16 [T][K]
+  uint16_t* out;        // bf16 [T][N]
+  int N, K, T;
+  Status* st;
+};
+int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
+
+// ---- misc.cu --------------------------------------------------------------
+__global__ void prep_act_kernel(const uint16_t* in, int K, uint16_t* out16, int32_t* exps);
+__global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
+                                           int4* groups, int32_t* n_groups, Status* st);
+__global__ void combine_kernel(const float* y, const int32_t* topk_idx, const float* topk_w, const uint16_t* norm_g,
+                               int L, int k, int E, float eps, uint16_t* zb, Status* st);
+__global__ void e2m1_selftest_kernel(float* out);
+
+}  // namespace lmoe

@@ -1,0 +1,166 @@
+// Small kernels around the streaming ones: activation preparation, the group
+// list for caller-supplied routing tables, post_expert_norm + weighted sum,
+// and the E2M1 conversion self-test.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace lmoe {
+
+__device__ __forceinline__ float block_max_256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  return m;
+}
+
+// One CTA (256 threads) per activation row: out16 = f16(x * 2^e), where the
+// power of two e puts the row's largest magnitude in [2^14, 2^15).  Values
+// with |x * 2^e| >= 2^-17 convert exactly; the expert epilogue multiplies the
+// fp32 result by 2^-e, so the products equal the bf16 ones.
+__global__ void __launch_bounds__(256) prep_act_kernel(const uint16_t* __restrict__ in, int K,
+                                                       uint16_t* __restrict__ out16, int32_t* __restrict__ exps) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[8];
+  const size_t row = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(in + row * K);
+  float m = 0.f;
+  for (int i = threadIdx.x; i < K / 8; i += 256) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = fmaxf(m, fabsf(bf16_bits_to_f32(w[j] & 0xffffu)));
+      m = fmaxf(m, fabsf(bf16_bits_to_f32(w[j] >> 16)));
+    }
+  }
+  m = block_max_256(m, red);
+  int e = 0;
+  if (m > 0.f && isfinite(m)) {
+    int E;
+    frexpf(m, &E);
+    e = min(127, max(-126, 15 - E));
+  }
+  const float scale = ldexpf(1.0f, e);
+  uint4* dst = reinterpret_cast<uint4*>(out16 + row * K);
+  for (int i = threadIdx.x; i < K / 8; i += 256) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 h = __floats2half2_rn(bf16_bits_to_f32(w[j] & 0xffffu) * scale, bf16_bits_to_f32(w[j] >> 16) * scale);
+      o[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) exps[row] = e;
+}
+
+// Group list (groups of <= G rows per expert) from a caller-supplied table,
+// with the table checked: offsets[0] == 0, monotone, offsets[E] == R, and
+// every sorted row id in [0, R).  One CTA of 256 threads.
+__global__ void __launch_bounds__(256) groups_from_offsets_kernel(const int32_t* __restrict__ offsets,
+                                                                  const int32_t* __restrict__ sorted_rows, int E,
+                                                                  int R, int G, int4* __restrict__ groups,
+                                                                  int32_t* __restrict__ n_groups, Status* st) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < R; i += 256)
+    if (sorted_rows[i] < 0 || sorted_rows[i] >= R) bad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // validate the whole table before writing any group
+    bool ok = offsets[0] == 0 && offsets[E] == R && !bad;
+    for (int e = 0; e < E && ok; ++e)
+      if (offsets[e + 1] < offsets[e] || offsets[e + 1] > R) ok = false;
+    int ng = 0;
+    if (ok) {
+      for (int e = 0; e < E; ++e) {
+        const int a = offsets[e], n = offsets[e + 1] - a;
+        for (int g0 = 0; g0 < n; g0 += G) groups[ng++] = make_int4(e, a + g0, min(G, n - g0), 0);
+      }
+    } else {
+      set_error(st, LMOE_EDEVICE_CHECK, 101);
+    }
+    *n_groups = ng;
+  }
+}
+
+// post_expert_norm on each route row, then the fp32 weighted sum in route
+// order ("Muse Spark Open on Gaudi 2", "The latent MoE: A' with a per-expert
+// norm").  One CTA (256 threads) per token t:
+//   ss_j  = sum_l y[t*k+j][l]^2            (fixed reduction tree)
+//   rinv  = 1 / sqrt(ss_j / L + eps)
+//   z[l]  = sum_j w[t][j] * ((y * rinv) * g[e_j][l]),  zb = bf16(z)
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ topk_idx,
+                                                      const float* __restrict__ topk_w,
+                                                      const uint16_t* __restrict__ norm_g, int L, int k, int E,
+                                                      float eps, uint16_t* __restrict__ zb, Status* st) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[8][8];
+  __shared__ float s_rinv[8];
+  __shared__ int s_e[8];
+  __shared__ float s_w[8];
+  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < k) {
+    int e = topk_idx[(size_t)t * k + tid];
+    if (e < 0 || e >= E) {
+      set_error(st, LMOE_EDEVICE_CHECK, 102);
+      e = 0;
+    }
+    s_e[tid] = e;
+    s_w[tid] = topk_w[(size_t)t * k + tid];
+  }
+  float ss[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ss[j] = 0.f;
+    if (j < k) {
+      const float* yr = y + ((size_t)t * k + j) * L;
+      for (int l = tid; l < L; l += 256) ss[j] = fmaf(yr[l], yr[l], ss[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float v = warp_sum(ss[j]);
+    if (lane == 0) red[j][warp] = v;
+  }
+  __syncthreads();
+  if (tid < k) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[tid][w];
+    s_rinv[tid] = 1.0f / sqrtf(s / (float)L + eps);
+  }
+  __syncthreads();
+  for (int l = tid; l < L; l += 256) {
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const float yv = y[((size_t)t * k + j) * L + l];
+      const float yh = __fmul_rn(__fmul_rn(yv, s_rinv[j]), bf16_bits_to_f32(norm_g[(size_t)s_e[j] * L + l]));
+      z = __fadd_rn(z, __fmul_rn(s_w[j], yh));
+    }
+    zb[(size_t)t * L + l] = f32_to_bf16_bits(z);
+  }
+}
+
+__global__ void e2m1_selftest_kernel(float* out) {
+  const uint32_t b = threadIdx.x;
+  uint32_t h0, h1, h2, h3;
+  e2m1x8_to_f16x8(b, h0, h1, h2, h3);
+  const __half2 v = *reinterpret_cast<const __half2*>(&h0);
+  out[2 * b] = __low2float(v);
+  out[2 * b + 1] = __high2float(v);
+}
+
+}  // namespace lmoe

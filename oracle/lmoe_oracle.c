@@ -111,11 +111,21 @@ static float e8m0_value(unsigned s) {
  * Exact in fp32 for s <= 252 (the product has at most 2 significant bits). */
 float oracle_mxfp4_value(unsigned code, unsigned s) { return e2m1_value(code & 15u) * e8m0_value(s); }
 
+/* Lookup tables filled from the two functions above (speed only: every
+ * entry is exactly the function's value). */
+static float g_e2m1_tab[16];
+static float g_e8m0_tab[256];
+static pthread_once_t g_tab_once = PTHREAD_ONCE_INIT;
+static void fill_tables(void) {
+  for (unsigned c = 0; c < 16; ++c) g_e2m1_tab[c] = e2m1_value(c);
+  for (unsigned s = 0; s < 256; ++s) g_e8m0_tab[s] = e8m0_value(s);
+}
+
 /* Element c of row n of a packed [N][K/2] code matrix with [N][K/32] scales. */
 static inline float mx_elem(const uint8_t* q, const uint8_t* sc, int64_t n, int64_t K, int64_t c) {
   uint8_t byte = q[n * (K / 2) + c / 2];
   unsigned code = ((c & 1) ^ (LMOE_ORACLE_PLANT == 1)) ? (byte >> 4) : (byte & 15u);
-  return oracle_mxfp4_value(code, sc[n * (K / 32) + c / 32]);
+  return g_e2m1_tab[code] * g_e8m0_tab[sc[n * (K / 32) + c / 32]];
 }
 
 /* ------------------------------------------------------------------------ */
@@ -341,6 +351,7 @@ void oracle_experts(const or_dims* d, const uint16_t* x_lat, const int32_t* topk
                     const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                     const uint8_t* w2_s, uint16_t* h_out, float* gu_out, float* y) {
   int64_t R = (int64_t)d->T * d->k;
+  pthread_once(&g_tab_once, fill_tables);
   uint16_t* h = h_out ? h_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(R * d->I));
   exp_ctx c = {d, x_lat, topk_idx, w13_q, w13_s, w2_q, w2_s, h, gu_out, y};
   parallel_for(R * d->I, gateup_body, &c);

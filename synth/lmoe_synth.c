@@ -72,16 +72,32 @@ typedef struct {
   uint32_t lo, count;
 } job_t;
 
+static void* run_bytes(job_t* j) {
+  uint8_t* out = (uint8_t*)j->out;
+  size_t i = j->begin;
+  for (; i < j->end && ((j->offset + i) & 7); ++i) {
+    uint64_t idx = j->offset + i;
+    out[i] = (uint8_t)(draw(j->key, idx >> 3) >> (8 * (idx & 7)));
+  }
+  for (; i + 8 <= j->end; i += 8) {
+    uint64_t d = draw(j->key, (j->offset + i) >> 3);
+    uint8_t b[8];
+    for (int k = 0; k < 8; ++k) b[k] = (uint8_t)(d >> (8 * k));
+    memcpy(out + i, b, 8);
+  }
+  for (; i < j->end; ++i) {
+    uint64_t idx = j->offset + i;
+    out[i] = (uint8_t)(draw(j->key, idx >> 3) >> (8 * (idx & 7)));
+  }
+  return NULL;
+}
+
 static void* run_job(void* arg) {
   job_t* j = (job_t*)arg;
+  if (j->kind == K_BYTES) return run_bytes(j);
   for (size_t i = j->begin; i < j->end; ++i) {
     uint64_t idx = j->offset + i;
     switch (j->kind) {
-      case K_BYTES: {
-        uint64_t d = draw(j->key, idx >> 3);
-        ((uint8_t*)j->out)[i] = (uint8_t)(d >> (8 * (idx & 7)));
-        break;
-      }
       case K_RANGE:
         ((uint8_t*)j->out)[i] = (uint8_t)(j->lo + draw(j->key, idx) % j->count);
         break;

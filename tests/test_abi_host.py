@@ -1,0 +1,78 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every function include/lmoe.h declares; argument validation and
+workspace sizing work without a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"LMOE_API\s+[\w\s\*]+?\b(lmoe_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import latent_moe_layer_fp32_gb300 as lm
+    lm.build()
+    lm.load()
+    return lm
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ("lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool", "lmoe_forward",
+              "lmoe_workspace_bytes", "lmoe_status_check", "lmoe_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lm):
+    lib = lm.load()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_error_strings(lm):
+    for code in range(-6, 1):
+        assert lm.lmoe_error_string(code)
+    assert lm.lmoe_error_string(-99) == "unknown error"
+
+
+def test_workspace_sizing_without_gpu(lm):
+    for name, d in synth.CONFIGS.items():
+        n = lm.lmoe_workspace_bytes(lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps))
+        # at least the per-route fp32 rows and the bf16 intermediates
+        assert n >= 4 * d.T * d.k * d.L + 2 * d.T * d.L, name
+        lay = lm.lmoe_workspace_layout(lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps))
+        assert lay.total == n
+        offs = [lay.status, lay.topk_idx, lay.topk_w, lay.expert_offsets, lay.sorted_rows, lay.row_pos, lay.x_lat,
+                lay.y, lay.z]
+        assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs)
+        assert lay.z + 2 * d.T * d.L <= n
+
+
+@pytest.mark.parametrize("field,value", [("T", 0), ("top_k", 9), ("top_k", 0), ("n_experts", 257),
+                                         ("hidden", 100), ("latent", 96), ("inter", 0), ("eps", -1.0)])
+def test_bad_dims_rejected(lm, field, value):
+    d = synth.CONFIGS["tiny"]
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    setattr(dims, field, value)
+    assert lm.lmoe_workspace_bytes(dims) == 0
+    lib = lm.load()
+    rc = lib.lmoe_forward(ctypes.byref(dims), None, None, None, None, 0, None)
+    assert rc == -1
+
+
+def test_unsupported_width(lm):
+    dims = lm.dims_of(1, 8192, 8192, 4096, 256, 8, 1e-6)
+    assert lm.lmoe_workspace_bytes(dims) == 0

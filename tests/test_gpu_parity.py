@@ -16,8 +16,8 @@ import torch
 
 import oracle
 import synth
-from parity_util import (bf, check_bf16_close, check_indices, check_out, check_rows_normwise, device_weights,
-                         host_weights, to_dev, to_host, ws_for, ws_view)
+from parity_util import (bf, check_bf16_close, sum_err, check_indices, check_out, check_rows_normwise, check_table_properties,
+                         device_weights, host_weights, to_dev, to_host, ws_for, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -74,16 +74,29 @@ def run_route(lm, d, x_dev, w):
     return {k_: to_host(v) for k_, v in out.items()}
 
 
+def pool_err(d, x, hw):
+    return sum_err(d.H, np.abs(bf(x)), np.abs(bf(hw["pooler_w"])))
+
+
 def check_route(orc, d, x, hw, got):
+    """Returns the oracle's (idx, w) and the tokens where the GPU chose a
+    different (valid, near-tie) set or order."""
     logits, absdot = orc.router_logits(d, x, hw["router_w"], hw["router_bias"], want_absdot=True)
     idx, tw = orc.topk(d, logits)
-    check_indices(d, got["idx"], idx, logits, absdot)
-    assert np.allclose(got["w"], tw, rtol=5e-5, atol=1e-6), np.abs(got["w"] - tw).max()
-    off, rows, pos = orc.table(d, idx)
-    assert np.array_equal(got["off"], off)
-    assert np.array_equal(got["rows"], rows)
-    assert np.array_equal(got["pos"], pos)
-    return idx, tw
+    flagged, differs = check_indices(d, got["idx"], idx, logits, absdot)
+    print(f"[route {d.T}] near-tie tokens {len(flagged)}, GPU choice differs on {len(differs)}: {differs[:8]}")
+    same = np.ones(d.T, bool)
+    same[differs] = False
+    assert np.allclose(got["w"][same], tw[same], rtol=5e-5, atol=1e-6), np.abs(got["w"][same] - tw[same]).max()
+    assert np.allclose(got["w"].sum(1), 1.0, atol=1e-5)
+    if differs.size == 0:
+        off, rows, pos = orc.table(d, idx)
+        assert np.array_equal(got["off"], off)
+        assert np.array_equal(got["rows"], rows)
+        assert np.array_equal(got["pos"], pos)
+    else:
+        check_table_properties(d, got["idx"], got["off"], got["rows"], got["pos"])
+    return idx, tw, differs
 
 
 # ------------------------------------------------------------------------------------------------
@@ -106,7 +119,7 @@ def test_stages_small(lm, orc, name, T):
     # pool
     x_lat = torch.empty(T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
-    check_bf16_close(to_host(x_lat), ref["x_lat"], "x_lat")
+    check_bf16_close(to_host(x_lat), ref["x_lat"], "x_lat", pool_err(d, x, hw))
     # experts on the oracle's x_lat and table
     off, rows, _ = orc.table(d, ref["topk_idx"])
     y = torch.empty(T * d.k, d.L, dtype=torch.float32, device="cuda")
@@ -137,7 +150,8 @@ def test_forward_small(lm, orc, name, T):
     check_out(to_host(out), ref["out"])
     lay = lm.lmoe_workspace_layout(dims)
     assert np.array_equal(to_host(ws_view(ws, lay.topk_idx, torch.int32, (T, d.k))), ref["topk_idx"])
-    check_bf16_close(to_host(ws_view(ws, lay.x_lat, torch.bfloat16, (T, d.L))), ref["x_lat"], "x_lat")
+    check_bf16_close(to_host(ws_view(ws, lay.x_lat, torch.bfloat16, (T, d.L))), ref["x_lat"], "x_lat",
+                     pool_err(d, x, hw))
 
 
 # ------------------------------------------------------------------------------------------------
@@ -155,10 +169,10 @@ def test_full_shape(lm, orc, name):
     dims = dims_c(lm, d)
     ws = ws_for(lm, dims)
     got = run_route(lm, d, x_dev, w)
-    check_route(orc, d, x, hw, got)
+    _, _, differs = check_route(orc, d, x, hw, got)
     x_lat = torch.empty(d.T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
-    check_bf16_close(to_host(x_lat), ref["x_lat"], "x_lat")
+    check_bf16_close(to_host(x_lat), ref["x_lat"], "x_lat", pool_err(d, x, hw))
     off, rows, _ = orc.table(d, ref["topk_idx"])
     y = torch.empty(d.T * d.k, d.L, dtype=torch.float32, device="cuda")
     lm.lmoe_experts_mxfp4(dims, to_dev(ref["x_lat"]), to_dev(off), to_dev(rows), w["w13_q"], w["w13_s"], w["w2_q"],
@@ -172,7 +186,9 @@ def test_full_shape(lm, orc, name):
     out2 = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_forward(dims, lm.weights_of(w), x_dev, out2, ws)
     assert lm.lmoe_status_check(ws) == 0
-    check_out(to_host(out2), ref["out"], "forward")
+    keep = np.ones(d.T, bool)
+    keep[differs] = False  # near-tie tokens routed differently (validated above)
+    check_out(to_host(out2)[keep], ref["out"][keep], "forward")
     if d.skewed:
         touched = np.count_nonzero(np.diff(got["off"]))
         assert touched < 40, touched  # routes concentrate on the biased experts
@@ -191,11 +207,11 @@ def test_prefill_sampled(lm, orc):
     xS = np.ascontiguousarray(x[S])
     # route: all tokens (indices and tables are checked in full)
     got = run_route(lm, d, x_dev, w)
-    idx, tw = check_route(orc, d, x, hw, got)
+    idx, tw, differs = check_route(orc, d, x, hw, got)
     # pool: sampled rows
     x_lat = torch.empty(d.T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
-    check_bf16_close(to_host(x_lat)[S], orc.pool(dS, xS, hw["pooler_w"]), "x_lat")
+    check_bf16_close(to_host(x_lat)[S], orc.pool(dS, xS, hw["pooler_w"]), "x_lat", pool_err(dS, xS, hw))
     # experts: generator-made x_lat for every token, the oracle's full table
     xl = synth.normal_bf16(0, TID_TEST_XLAT, (d.T, d.L), 0.0, 1.0)
     off, rows, _ = orc.table(d, idx)
@@ -218,7 +234,8 @@ def test_prefill_sampled(lm, orc):
     lm.lmoe_forward(dims, lm.weights_of(w), x_dev, out2, ws)
     assert lm.lmoe_status_check(ws) == 0
     refS = orc.forward(dS, xS, hw)
-    check_out(to_host(out2)[S], refS["out"], "forward")
+    keep = ~np.isin(S, differs)
+    check_out(to_host(out2)[S][keep], refS["out"][keep], "forward")
 
 
 # ------------------------------------------------------------------------------------------------

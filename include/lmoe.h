@@ -61,7 +61,8 @@ enum {
   LMOE_ECUDA = -3,         /* a CUDA runtime call failed */
   LMOE_ETIMEOUT = -4,      /* a bounded device-side wait ran out */
   LMOE_EDEVICE_CHECK = -5, /* a device-side input check failed (e.g. expert id) */
-  LMOE_EWORKSPACE = -6     /* workspace too small */
+  LMOE_EWORKSPACE = -6,    /* workspace too small */
+  LMOE_ENOSCRATCH = -7     /* larger than the fixed scratch of lmoe_route_noalloc */
 };
 
 typedef struct {
@@ -176,6 +177,28 @@ LMOE_API const char* lmoe_error_string(int code);
 
 /* Number of kernel launches the last lmoe_* call on this thread enqueued. */
 LMOE_API int lmoe_last_launch_count(void);
+
+/* Routing without a workspace, for callers that cannot allocate device
+ * memory where they run the layer (for example a plugin called from another
+ * runtime's enqueue path, where that runtime owns every device allocation, or
+ * an embedded runtime with a memory budget fixed at start-up).  The pages
+ * have no counterpart: this is a deployment variant of lmoe_route.
+ *   Same arguments, outputs and results as lmoe_route, minus ws/ws_bytes.
+ *   Its scratch is a fixed array inside the library (about 1.1 MB, held on
+ *   every GPU that loads the library until the process exits), so it accepts
+ *   at most T = 64 tokens and n_experts <= 256, and returns LMOE_ENOSCRATCH
+ *   beyond that.  It never allocates or frees device memory.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture on the device.
+ *   Every call shares the one array and its contents persist between calls:
+ *   calls that overlap on the GPU race and must be serialised by the caller.
+ *   Device-side check results are not reported (there is no workspace for
+ *   lmoe_status_check to read). */
+LMOE_API int lmoe_route_noalloc(const lmoe_dims* dims, const uint16_t* x, const float* router_w,
+                                const float* router_bias, int32_t* topk_idx, float* topk_w,
+                                int32_t* expert_offsets, int32_t* sorted_rows, int32_t* row_pos,
+                                lmoe_stream_t stream);
 
 /* Optional per-launch timing: while set, every kernel launch i of the
  * following lmoe_* calls on this host thread is preceded by

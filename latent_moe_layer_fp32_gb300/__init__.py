@@ -18,13 +18,14 @@ from ._build import build, up_to_date
 
 __all__ = [
     "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
-    "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4",
+    "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_route_noalloc", "lmoe_pool", "lmoe_experts_mxfp4",
     "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_status_check", "lmoe_error_string",
     "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
 ]
 
 LMOE_OK, LMOE_EINVAL, LMOE_EUNSUPPORTED, LMOE_ECUDA, LMOE_ETIMEOUT, LMOE_EDEVICE_CHECK, LMOE_EWORKSPACE = \
     0, -1, -2, -3, -4, -5, -6
+LMOE_ENOSCRATCH = -7
 
 
 class LmoeDims(ctypes.Structure):
@@ -77,9 +78,10 @@ def load(path: str | None = None):
     lib.lmoe_last_launch_count.argtypes = []
     lib.lmoe_selftest_e2m1.argtypes = [vp]
     lib.lmoe_profile_events.argtypes = [vp, i32]
+    lib.lmoe_route_noalloc.argtypes = [dp] + [vp] * 8 + [vp]
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
               "lmoe_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
-              "lmoe_profile_events"):
+              "lmoe_profile_events", "lmoe_route_noalloc"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -155,6 +157,15 @@ def lmoe_route(dims, x, router_w, router_bias, topk_idx, topk_w, expert_offsets,
                              _ptr(topk_idx, _I32), _ptr(topk_w, _F32), _ptr(expert_offsets, _I32),
                              _ptr(sorted_rows, _I32), _ptr(row_pos, _I32), _ptr(ws), ws.numel() * ws.element_size(),
                              _stream(stream)), "lmoe_route")
+
+
+def lmoe_route_noalloc(dims, x, router_w, router_bias, topk_idx, topk_w, expert_offsets, sorted_rows, row_pos,
+                       stream=None):
+    """lmoe_route without a workspace (fixed library-owned scratch, T <= 64)."""
+    _check(load().lmoe_route_noalloc(ctypes.byref(dims), _ptr(x, _BF16), _ptr(router_w, _F32),
+                                     _ptr(router_bias, _F32), _ptr(topk_idx, _I32), _ptr(topk_w, _F32),
+                                     _ptr(expert_offsets, _I32), _ptr(sorted_rows, _I32), _ptr(row_pos, _I32),
+                                     _stream(stream)), "lmoe_route_noalloc")
 
 
 def lmoe_pool(dims, x, pooler_w, x_lat, ws=None, stream=None):

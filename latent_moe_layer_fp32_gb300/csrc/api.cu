@@ -349,6 +349,7 @@ const char* lmoe_error_string(int code) {
     case LMOE_ETIMEOUT: return "a bounded device-side wait ran out";
     case LMOE_EDEVICE_CHECK: return "device-side input check failed (routing table out of range)";
     case LMOE_EWORKSPACE: return "workspace too small";
+    case LMOE_ENOSCRATCH: return "larger than the fixed scratch of lmoe_route_noalloc (T <= 64)";
     default: return "unknown error";
   }
 }

@@ -1,0 +1,102 @@
+// Routing for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain device memory at the point where they
+// run the layer: a plugin called from another runtime's enqueue path, where
+// the host framework owns every device allocation and forbids new ones, or
+// an embedded runtime with a fixed memory budget fixed at start-up.  They
+// cannot size and pass the workspace that lmoe_route needs.
+// lmoe_route_noalloc gives them the same routing with its scratch (router
+// split partials, group list, status word) in a fixed array inside the
+// library instead.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the
+// library holds it (kNoAllocScratchBytes, about 1.1 MB) until the process
+// exits.  Every call shares it: two calls that overlap on the GPU (different
+// streams, or different host threads) race on it and must be serialised by
+// the caller.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int kNoAllocMaxT = 64;
+constexpr int kNoAllocMaxE = 256;
+constexpr int kNoAllocMaxSplit = 16;
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kPartBytes = sizeof(float) * kNoAllocMaxSplit * kNoAllocMaxT * kNoAllocMaxE;
+constexpr size_t kGroupsBytes = ((sizeof(int4) * (kNoAllocMaxT * 8 + kNoAllocMaxE + 1)) + 255) / 256 * 256;
+constexpr size_t kNoAllocScratchBytes = kStatusBytes + kPartBytes + kGroupsBytes;
+
+// The scratch.  In host code this name is only a host-side stand-in for the
+// device variable; the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_addr[64] = {};
+int g_sms[64] = {};
+
+// Once per device, with that device current: look up the array's device
+// address and the SM count.
+int scratch_for_current_device(void** addr, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LMOE_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LMOE_ECUDA;
+    if (major != 10 || minor != 3) return LMOE_EUNSUPPORTED;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return LMOE_ECUDA;
+    g_sms[dev] = n;
+    g_scratch_addr[dev] = p;
+  }
+  *addr = g_scratch_addr[dev];
+  *sms = g_sms[dev];
+  return LMOE_OK;
+}
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x, const float* router_w,
+                                           const float* router_bias, int32_t* topk_idx, float* topk_w,
+                                           int32_t* expert_offsets, int32_t* sorted_rows, int32_t* row_pos,
+                                           lmoe_stream_t stream) {
+  using namespace lmoe;
+  if (!d || d->T < 1 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k || d->n_experts > 256 ||
+      d->hidden < 128 || d->hidden % 128 || d->latent < 128 || d->latent % 128 || d->inter < 128 ||
+      d->inter % 128 || !(d->eps >= 0.f))
+    return LMOE_EINVAL;
+  if (d->T > kNoAllocMaxT || d->n_experts > kNoAllocMaxE) return LMOE_ENOSCRATCH;
+  if (!al16(x) || !al16(router_w) || !topk_idx || !topk_w || !expert_offsets || !sorted_rows || !row_pos ||
+      (router_bias && !al16(router_bias)))
+    return LMOE_EINVAL;
+  void* base = nullptr;
+  int sms = 0;
+  int rc = scratch_for_current_device(&base, &sms);
+  if (rc != LMOE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = d->T, E = d->n_experts, k = d->top_k, H = d->hidden;
+  char* scratch = static_cast<char*>(base);
+  Status* st = reinterpret_cast<Status*>(scratch);
+  int32_t* n_groups = reinterpret_cast<int32_t*>(scratch + 16);
+  float* part = reinterpret_cast<float*>(scratch + kStatusBytes);
+  int4* groups = reinterpret_cast<int4*>(scratch + kStatusBytes + kPartBytes);
+  // the status word must start at zero; everything else is written before it is read
+  if (cudaMemsetAsync(st, 0, sizeof(Status), s) != cudaSuccess) return LMOE_ECUDA;
+  // same split rule as lmoe_route, capped by the scratch (at most 16 splits)
+  const int tiles = ((E + 31) / 32) * ((T + 7) / 8);
+  int ns = 1;
+  while (tiles * ns < 2 * sms && ns < kNoAllocMaxSplit && H % (128 * ns * 2) == 0) ns *= 2;
+  router_partial_kernel<<<dim3((E + 31) / 32, (T + 7) / 8, ns), 256, 0, s>>>(x, router_w, part, T, H, E, H / ns);
+  topk_kernel<<<dim3((T + 7) / 8), 256, 0, s>>>(part, ns, router_bias, T, E, k, topk_idx, topk_w);
+  table_kernel<<<1, 1024, 0, s>>>(topk_idx, T * k, E, expert_max_group(T), expert_offsets, sorted_rows, row_pos,
+                                  groups, n_groups, st);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+}

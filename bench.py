@@ -172,7 +172,7 @@ def allreduce_max(world, v: float) -> float:
     return float(t.item())
 
 
-def cpu_oracle_rate(d, hw, x, min_seconds=8.0, max_reps=30):
+def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000):
     """Tokens/s of the CPU oracle on repeated whole-layer evaluations of `x`."""
     import oracle
     o = oracle.get()
@@ -218,8 +218,8 @@ def run_reference(args, d, name, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_t1", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -275,15 +275,19 @@ def main():
         # ---- device-resident timed region ----
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        clk = Clocks(local).__enter__()
+        time.sleep(0.5)  # nvidia-smi needs a moment before its first sample
         torch.cuda.synchronize()
         barrier(world)
-        with Clocks(local) as clk:
+        try:
             for i in range(args.steps):
                 flush.zero_()
                 e0[i].record()
                 lm.lmoe_forward(dims, wts, x_dev, out, ws)
                 e1[i].record()
             torch.cuda.synchronize()
+        finally:
+            clk.__exit__(None, None, None)
         barrier(world)
         step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
         total_s = allreduce_max(world, sum(step_ms) / 1e3)

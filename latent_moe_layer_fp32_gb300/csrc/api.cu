@@ -53,7 +53,9 @@ int check_dims(const lmoe_dims* d) {
       d->n_experts > 256 || d->hidden < 128 || d->latent < 128 || d->inter < 128 || d->hidden % 128 ||
       d->latent % 128 || d->inter % 128 || !(d->eps >= 0.f))
     return LMOE_EINVAL;
-  if (d->latent > 4096 || d->inter > 4096) return LMOE_EUNSUPPORTED;  // expert stage holds K/32 <= 128 scales
+  // expert and projection kernels stream K in 128-byte planes and 1024-element chunks
+  if (d->hidden % 256 || d->latent % 256 || d->inter % 256) return LMOE_EUNSUPPORTED;
+  if ((d->latent > 1024 && d->latent % 1024) || (d->inter > 1024 && d->inter % 1024)) return LMOE_EUNSUPPORTED;
   return LMOE_OK;
 }
 
@@ -68,7 +70,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, groups, part, x16, xexp, h, h16, hexp;
+  size_t n_groups, groups, part, x16, xexp, h, h16, hexp, ssq;
   int nsplit;
 };
 
@@ -99,6 +101,7 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->h16 = take(2 * R * I);
   w->hexp = take(4 * R);
   w->pub.y = take(4 * R * L);
+  w->ssq = take(4 * R * (L / 32));
   w->pub.z = take(2 * T * L);
   w->pub.total = o;
   return LMOE_OK;
@@ -159,7 +162,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   float* part = at<float>(ws, w.part);
   LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T, H,
          E, H / w.nsplit);
-  LAUNCH(dim3((T + 7) / 8), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
+  LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
          topk_w);
   LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, expert_max_group(T), offsets,
          sorted_rows, row_pos, at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), st);
@@ -190,6 +193,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.inter = I;
   a.latent = L;
   a.top_k = k;
+  a.n_experts = d->n_experts;
   a.st = st;
   a.q = w13_q;
   a.s = w13_s;
@@ -209,6 +213,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.K = I;
   a.h_out = nullptr;
   a.y_out = y;
+  a.ssq_out = at<float>(ws, w.ssq);
   pre_launch(s);
   CHECK(launch_down(a, T, G, s, di.sms));
   ++g_launches;
@@ -217,11 +222,16 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
 
 int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const float* y,
                        const int32_t* topk_idx, const float* topk_w, const uint16_t* norm_g,
-                       const uint16_t* unpooler_w, uint16_t* out, void* ws, cudaStream_t s) {
+                       const uint16_t* unpooler_w, uint16_t* out, void* ws, cudaStream_t s, bool ssq_ready) {
   Status* st = at<Status>(ws, w.pub.status);
   uint16_t* zb = at<uint16_t>(ws, w.pub.z);
-  LAUNCH(dim3(d->T), dim3(256), s, combine_kernel, y, topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts,
-         d->eps, zb, st);
+  if (!ssq_ready) {
+    const long long n = (long long)d->T * d->top_k * (d->latent / 32);
+    LAUNCH(dim3((unsigned)((n + 7) / 8)), dim3(256), s, ssq_kernel, y, d->T * d->top_k, d->latent,
+           at<float>(ws, w.ssq));
+  }
+  LAUNCH(dim3(d->T, (d->latent + 511) / 512), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
+         topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts, d->eps, zb, st);
   GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st};
   pre_launch(s);
   CHECK(launch_gemv_bf16(g, s, di.sms));
@@ -302,7 +312,7 @@ int lmoe_norm_combine_unpool(const lmoe_dims* d, const float* y, const int32_t* 
   const void* ptrs[] = {y, topk_idx, topk_w, norm_g, unpooler_w, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return LMOE_EINVAL;
-  return post_call(s, run_combine_unpool(d, w, di, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, s));
+  return post_call(s, run_combine_unpool(d, w, di, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, s, false));
 }
 
 int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, uint16_t* out, void* ws,
@@ -327,7 +337,7 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
                   at<int32_t>(ws, w.pub.row_pos), ws, s));
   CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
   CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s));
-  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s));
+  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);
 }
 

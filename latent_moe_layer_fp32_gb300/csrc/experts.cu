@@ -7,55 +7,100 @@
 // page's stock op unpacked every touched slice to bf16 in memory ("What it
 // taught about Gaudi"); here nothing is unpacked in memory.
 //
-// Work item = (group of <= G rows of one expert, tile of 16 weight rows).
-// gate/up tile: 8 gate rows + the 8 matching up rows (so SwiGLU is local to a
-// lane); down tile: 16 consecutive output rows.  Each item streams its 16
-// weight rows once (all of K) for every row of the group.
+// Work item = (group of <= G rows of one expert, tile of 32 weight rows =
+// two m16 tiles).  gate/up: 16 gate rows + the matching 16 up rows (an m16
+// tile pairs 8 gate rows with their 8 up rows, so SwiGLU is local to a lane);
+// down: 32 consecutive output rows.  Each item streams its rows once (all of
+// K) for every row of its group.
 //
-// CTA = W consumer warps + 1 producer warp.  The producer issues TMA bulk
-// copies (codes, scales and the group's f16 activation rows for one K chunk)
-// into per-warp rings of D slots guarded by mbarriers; consumer warp w
-// handles items w, w+W, ... of the CTA's contiguous item range.
+// CTA = W consumer warps + 1 producer warp.  Per K chunk the producer issues
+// two TMA tensor copies of the codes (16 rows x kc/2 bytes each, a 3-D view
+// {128 B, rows, K/256} with 128-byte swizzle, so each copy is one 8 KB
+// request and ldmatrix reads it without bank conflicts), two of the E8M0
+// scales and one bulk copy per activation row, into per-warp mbarrier rings
+// of D slots; consumer warp w takes items w, w+W, ... of the CTA's range.
 //
-// Consumer inner loop per 32-element scale block: ldmatrix.x4 hands every
-// lane 4 code bytes of a gate row and of an up row; cvt.rn.f16x2.e2m1x2 turns
-// each byte into two exact f16 values; two mma.sync m16n8k16 (f16 in, fp32
-// accumulate) take the K positions of one block in a fixed permutation that
-// the activation fragment follows; the fresh block result is scaled by the
-// block's E8M0 value and added to the fp32 accumulator.  Activations arrive
-// as f16 scaled by a per-row power of two (exact; undone in the epilogue).
+// Consumer per 32-element scale block: ldmatrix.x4 hands each lane 4 code
+// bytes of two rows; cvt.rn.f16x2.e2m1x2 turns each byte into two exact f16
+// values; two mma.sync m16n8k16 (f16 in, fp32 accumulate) cover the block's
+// 32 K positions in a fixed permutation that the activation fragment follows;
+// the fresh block result is scaled by the block's E8M0 value (expanded once
+// per chunk into a per-warp fp32 table) and added to the fp32 accumulator.
+// Activations arrive as f16 scaled by a per-row power of two (exact; undone
+// in the epilogue).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tmap.cuh"
 
 namespace lmoe {
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
-constexpr int kMaxKs = 128;  // scale bytes per row (K <= 4096)
+constexpr int kRows = 32;  // weight rows per item: two m16 tiles
+constexpr int kKC = 1024;  // K elements per chunk when K > 1024 (else the whole K)
 
-template <int G, int KCMAX>
+template <int G>
 struct Layout {
-  static constexpr int kCodeRow = KCMAX / 2 + 16;  // padded: 8 rows hit distinct banks for ldmatrix
-  static constexpr int kCodes = 16 * kCodeRow;
-  static constexpr int kScales = 16 * kMaxKs;
-  static constexpr int kActRow = KCMAX * 2 + 64;   // padded: conflict-free 16-byte loads
+  static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (8 KB)
+  static constexpr int kCodes = 2 * kBox;      // box A (rows 0-15 of the item), box B (rows 16-31)
+  static constexpr int kScales = kRows * (kKC / 32);
+  static constexpr int kActRow = kKC * 2 + 64;  // padded: conflict-free 16-byte loads
   static constexpr int kActs = G * kActRow;
-  static constexpr int kSlot = ((kCodes + kScales + kActs) + 127) / 128 * 128;
+  static constexpr int kSlot = (kCodes + kScales + kActs + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
+  // per consumer warp: the chunk's block scales as fp32, [block][mtile][g][lo,hi]
+  static constexpr int kTable = (kKC / 32) * 2 * 8 * 2 * 4;
 };
 
-template <int MODE, int G, int KCMAX, int W, int D>
-__global__ void __launch_bounds__(32 * (W + 1), 1) expert_kernel(const ExpertArgs a) {
-  using Lay = Layout<G, KCMAX>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + W * D * Lay::kSlot);
+// Expand the chunk's E8M0 bytes (scale region [32 rows][nb]) into fp32
+// 2^(s-127) in the warp's table.  Fast path s << 23 is exact for
+// 1 <= s <= 254; a chunk holding 0 or 255 takes the exact per-value path.
+template <int MODE>
+__device__ __forceinline__ void expand_scales(const uint8_t* sc, int nb, float* table, int lane) {
+  const int r = lane;  // region row: rows 0-15 from box A, 16-31 from box B
+  const int box = r >> 4, rb = r & 15;
+  // gate/up: box A = gate (lo), box B = up (hi); m-tile = rb / 8.
+  // down: box = m-tile; lo/hi = rb / 8.
+  const int mt = (MODE == MODE_GATEUP) ? (rb >> 3) : box;
+  const int hi = (MODE == MODE_GATEUP) ? box : (rb >> 3);
+  const int g = r & 7;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(sc + r * nb);
+  bool special = false;
+  for (int j = 0; j < nb / 4; ++j) {
+    const uint32_t w = src[j];
+    special |= (__vcmpeq4(w, 0u) | __vcmpeq4(w, 0xffffffffu)) != 0u;
+  }
+  special = __any_sync(0xffffffffu, special);
+  float* dst = table + (mt * 8 + g) * 2 + hi;
+  if (!special) {
+    for (int j = 0; j < nb / 4; ++j) {
+      const uint32_t w = src[j];
+      dst[(4 * j + 0) * 32] = __uint_as_float((w << 23) & 0x7f800000u);
+      dst[(4 * j + 1) * 32] = __uint_as_float((w << 15) & 0x7f800000u);
+      dst[(4 * j + 2) * 32] = __uint_as_float((w << 7) & 0x7f800000u);
+      dst[(4 * j + 3) * 32] = __uint_as_float((w >> 1) & 0x7f800000u);
+    }
+  } else {
+    for (int j = 0; j < nb; ++j) dst[j * 32] = e8m0_to_f32(sc[r * nb + j]);
+  }
+}
+
+template <int MODE, int G, int W, int D>
+__global__ void __launch_bounds__(32 * (W + 1), 1)
+    expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s) {
+  using Lay = Layout<G>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1 KB alignment for the swizzled boxes
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* tables = reinterpret_cast<float*>(smem + W * D * Lay::kSlot);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + W * D * Lay::kSlot + W * Lay::kTable);
   uint64_t* empty = full + W * D;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K, kc = a.kc, Ks = K / 32, nch = K / kc;
-  const int kcode_row = kc / 2 + 16;  // runtime row stride when kc < KCMAX keeps the padding rule
-  const int kact_row = kc * 2 + 64;
-  const int tiles = (MODE == MODE_GATEUP) ? a.inter / 8 : a.latent / 16;
+  const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
+  const int Ks = K / 32;
+  const int tiles = (MODE == MODE_GATEUP) ? a.inter / 16 : a.latent / kRows;
   const int rows_per_expert = (MODE == MODE_GATEUP) ? 2 * a.inter : a.latent;
+  const int kact_row = kc * 2 + 64;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * D; ++i) {
@@ -75,8 +120,11 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) expert_kernel(const ExpertArg
 
   if (warp == W) {
     // ------------------------------ producer ------------------------------
-    if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
+    }
     int seq[W];
 #pragma unroll
     for (int w = 0; w < W; ++w) seq[w] = 0;
@@ -84,7 +132,6 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) expert_kernel(const ExpertArg
     for (int base = 0; base < nloc && ok; base += W) {
       const int nw = min(W, nloc - base);
       for (int c = 0; c < nch && ok; ++c) {
-        const int k0 = c * kc;
         for (int w = 0; w < nw; ++w) {
           const int it = it0 + base + w;
           const int grp = it / tiles, tile = it % tiles;
@@ -93,131 +140,180 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) expert_kernel(const ExpertArg
           const int d = seq[w] % D;
           const uint32_t par = ((seq[w] / D) & 1) ^ 1;
           ++seq[w];
-          if (!mbar_wait(&empty[w * D + d], par, a.st, 1)) {
+          int got = 1;
+          if (lane == 0) got = mbar_wait(&empty[w * D + d], par, a.st, 1);
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
             ok = false;
             break;
           }
           uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
           uint64_t* bar = &full[w * D + d];
-          const uint32_t bytes = 16u * (kc / 2) + 16u * Ks + (uint32_t)ntok * kc * 2;
-          mbar_arrive_expect_tx(bar, bytes);
-          // codes: 16 rows of kc/2 bytes
-#pragma unroll 4
-          for (int i = 0; i < 16; ++i) {
-            int row;
-            if (MODE == MODE_GATEUP)
-              row = e * rows_per_expert + (i < 8 ? tile * 8 + i : a.inter + tile * 8 + i - 8);
-            else
-              row = e * rows_per_expert + tile * 16 + i;
-            bulk_g2s_stream(slot + i * kcode_row, a.q + (size_t)row * (K / 2) + k0 / 2, kc / 2, bar, pol);
-          }
-          // scales: whole rows (16 x Ks bytes)
-          uint8_t* sdst = slot + Lay::kCodes;
+          // first rows of box A and box B
+          int rowA, rowB;
           if (MODE == MODE_GATEUP) {
-            const size_t g_row = (size_t)e * rows_per_expert + tile * 8;
-            bulk_g2s(sdst, a.s + g_row * Ks, 8 * Ks, bar);
-            bulk_g2s(sdst + 8 * Ks, a.s + (g_row + a.inter) * Ks, 8 * Ks, bar);
+            rowA = e * rows_per_expert + tile * 16;
+            rowB = rowA + a.inter;
           } else {
-            bulk_g2s(sdst, a.s + ((size_t)e * rows_per_expert + tile * 16) * Ks, 16 * Ks, bar);
+            rowA = e * rows_per_expert + tile * kRows;
+            rowB = rowA + 16;
           }
-          // activations: ntok rows of kc f16
-          uint8_t* adst = slot + Lay::kCodes + Lay::kScales;
-          for (int j = 0; j < ntok; ++j) {
-            int arow;
-            if (MODE == MODE_GATEUP)
-              arow = a.sorted_rows[p0 + j] / a.top_k;
-            else
-              arow = p0 + j;
-            bulk_g2s(adst + j * kact_row, a.act16 + (size_t)arow * K + k0, kc * 2, bar);
+          if (lane == 0) mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb + (uint32_t)ntok * kc * 2);
+          __syncwarp();
+          if (lane == 0) {
+            tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
+            tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
+          } else if (lane == 1 || lane == 2) {
+            uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
+            const int srow = lane == 1 ? rowA : rowB;
+            if (nch > 1)
+              tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
+            else  // one chunk: the 16 rows' scales are contiguous
+              bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
+          } else if (lane >= 8 && lane < 8 + ntok) {
+            const int j = lane - 8;
+            const int arow = (MODE == MODE_GATEUP) ? a.sorted_rows[p0 + j] / a.top_k : p0 + j;
+            bulk_g2s(slot + Lay::kCodes + Lay::kScales + j * kact_row, a.act16 + (size_t)arow * K + c * kc, kc * 2,
+                     bar);
           }
+          __syncwarp();
         }
       }
     }
-    // drain: make sure no copy is still in flight when this thread leaves
+    // drain: no copy may still be in flight when this warp leaves
+    if (lane == 0) {
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      for (int s = max(0, seq[w] - D); s < seq[w]; ++s) {
-        mbar_wait(&full[w * D + (s % D)], (s / D) & 1, a.st, 2);
-      }
+      for (int w = 0; w < W; ++w)
+        for (int s = max(0, seq[w] - D); s < seq[w]; ++s)
+          mbar_wait(&full[w * D + (s % D)], (s / D) & 1, a.st, 2);
     }
     return;
   }
 
   // -------------------------------- consumer --------------------------------
   const int g = lane >> 2, q = lane & 3;
-  // ldmatrix.x4 source row/column for this lane: matrix m = lane/8
-  const int lm_m = lane >> 3, lm_r = lane & 7;
-  const int lm_row = lm_r + 8 * (lm_m & 1);
-  const int lm_blk = lm_m >> 1;
+  // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
+  const int lm = lane >> 3, rr = lane & 7;
+  float* table = tables + warp * (Lay::kTable / 4);
+  constexpr int NV = (G == 1) ? 1 : 2;  // token columns per lane that can hold a valid token
+  // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
+  uint32_t box_off[2];
+  int row_in_box[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    int box, row;
+    if (MODE == MODE_GATEUP) {
+      box = lm & 1;  // gate box (lo) / up box (hi)
+      row = m * 8 + rr;
+    } else {
+      box = m;
+      row = (lm & 1) * 8 + rr;
+    }
+    box_off[m] = box * 16 * (kc / 2);
+    row_in_box[m] = row;
+  }
   int seq = 0;
   for (int j = warp; j < nloc; j += W) {
     const int it = it0 + j;
     const int grp = it / tiles, tile = it % tiles;
     const int4 gi = a.groups[grp];
     const int p0 = gi.y, ntok = gi.z;
-    float acc_lo[2] = {0.f, 0.f}, acc_hi[2] = {0.f, 0.f};
+    float acc[2][2][NV];  // [mtile][lo/hi row][token column]
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[m][h][v] = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int d = seq % D;
       const uint32_t par = (seq / D) & 1;
       ++seq;
       if (!mbar_wait(&full[warp * D + d], par, a.st, 3)) return;
       const uint8_t* slot = smem + (warp * D + d) * Lay::kSlot;
-      const uint32_t codes = smem_u32(slot);
-      const uint8_t* sc = slot + Lay::kCodes;
-      const uint32_t acts = smem_u32(slot + Lay::kCodes + Lay::kScales);
-      const int kb0 = c * (kc / 32);
-      const uint32_t lm_addr = codes + lm_row * kcode_row + lm_blk * 16;
-      // lanes whose token column is beyond the group's capacity read row 0 (in
-      // bounds); their mma columns are never stored
-      const uint32_t act_addr = acts + (g < G ? g : 0) * kact_row + q * 16;
+      expand_scales<MODE>(slot + Lay::kCodes, nb, table, lane);
+      __syncwarp();
+      const uint32_t sbase = smem_u32(slot);
+      const uint32_t act_addr = smem_u32(slot + Lay::kCodes + Lay::kScales) + (g < G ? g : 0) * kact_row + q * 16;
+      const float2* tab2 = reinterpret_cast<const float2*>(table) + g;
 #pragma unroll 2
-      for (int bb = 0; bb < kc / 32; bb += 2) {
-        uint32_t w0, w1, w2, w3;
-        ldmatrix_x4(w0, w1, w2, w3, lm_addr + bb * 16);
+      for (int bb = 0; bb < nb; bb += 2) {
+        // this lane's ldmatrix block: bb + (lm >> 1); plane = blk / 8, chunk = blk % 8
+        const int blk_l = bb + (lm >> 1);
+        uint32_t w[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+          ldmatrix_x4(w[m][0], w[m][1], w[m][2], w[m][3],
+                      sbase + box_off[m] + swz128(blk_l >> 3, 16, row_in_box[m], blk_l & 7));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int blk = bb + half;
-          const uint32_t wl = half ? w2 : w0, wh = half ? w3 : w1;
-          uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-          e2m1x8_to_f16x8(wl, l0, l1, l2, l3);
-          e2m1x8_to_f16x8(wh, h0, h1, h2, h3);
           uint32_t b0, b1, b2, b3;
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
                        : "r"(act_addr + blk * 64));
-          float dacc[4];
-          mma_f16_zero(dacc, l0, h0, l1, h1, b0, b1);
-          mma_f16(dacc, l2, h2, l3, h3, b2, b3);
-          const float s_lo = e8m0_to_f32(sc[g * Ks + kb0 + blk]);
-          const float s_hi = e8m0_to_f32(sc[(8 + g) * Ks + kb0 + blk]);
-          acc_lo[0] = fmaf(dacc[0], s_lo, acc_lo[0]);
-          acc_lo[1] = fmaf(dacc[1], s_lo, acc_lo[1]);
-          acc_hi[0] = fmaf(dacc[2], s_hi, acc_hi[0]);
-          acc_hi[1] = fmaf(dacc[3], s_hi, acc_hi[1]);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+            e2m1x8_to_f16x8(w[m][2 * half], l0, l1, l2, l3);
+            e2m1x8_to_f16x8(w[m][2 * half + 1], h0, h1, h2, h3);
+            float dacc[4];
+            mma_f16_zero(dacc, l0, h0, l1, h1, b0, b1);
+            mma_f16(dacc, l2, h2, l3, h3, b2, b3);
+            const float2 s = tab2[(blk * 2 + m) * 8];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+              acc[m][0][v] = fmaf(dacc[v], s.x, acc[m][0][v]);
+              acc[m][1][v] = fmaf(dacc[2 + v], s.y, acc[m][1][v]);
+            }
+          }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[warp * D + d]);
     }
     // ------------------------------ epilogue ------------------------------
+    // gate/up m-tile m holds features tile*16 + m*8 + g; down m-tile m holds
+    // output rows tile*32 + m*16 + g (+8 for the hi half)
+    float ssq[NV];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int tok = 2 * q + i;
+    for (int v = 0; v < NV; ++v) {
+      const int tok = 2 * q + v;
+      ssq[v] = 0.f;
       if (tok < ntok) {
         const int p = p0 + tok;
         if (MODE == MODE_GATEUP) {
           const int t = a.sorted_rows[p] / a.top_k;
           const float inv = ldexpf(1.0f, -a.act_exp[t]);
-          const float gv = acc_lo[i] * inv, uv = acc_hi[i] * inv;
-          const float hv = gv / (1.0f + expf(-gv)) * uv;
-          a.h_out[(size_t)p * a.inter + tile * 8 + g] = f32_to_bf16_bits(hv);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const float gv = acc[m][0][v] * inv, uv = acc[m][1][v] * inv;
+            const float hv = gv / (1.0f + expf(-gv)) * uv;
+            a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = f32_to_bf16_bits(hv);
+          }
         } else {
           const int r = a.sorted_rows[p];
           const float inv = ldexpf(1.0f, -a.act_exp[p]);
-          float* yr = a.y_out + (size_t)r * a.latent + tile * 16;
-          yr[g] = acc_lo[i] * inv;
-          yr[g + 8] = acc_hi[i] * inv;
+          float* yr = a.y_out + (size_t)r * a.latent + tile * kRows;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const float y0 = acc[m][0][v] * inv, y1 = acc[m][1][v] * inv;
+            yr[m * 16 + g] = y0;
+            yr[m * 16 + g + 8] = y1;
+            ssq[v] = fmaf(y0, y0, fmaf(y1, y1, ssq[v]));
+          }
         }
+      }
+    }
+    if (MODE == MODE_DOWN && a.ssq_out) {
+      // sum of squares of the tile's 32 rows per token (fixed tree over g)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float sv = ssq[v];
+        sv += __shfl_xor_sync(0xffffffffu, sv, 4);
+        sv += __shfl_xor_sync(0xffffffffu, sv, 8);
+        sv += __shfl_xor_sync(0xffffffffu, sv, 16);
+        const int tok = 2 * q + v;
+        if (g == 0 && tok < ntok) a.ssq_out[(size_t)a.sorted_rows[p0 + tok] * (a.latent / kRows) + tile] = sv;
       }
     }
   }
@@ -228,20 +324,12 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) expert_kernel(const ExpertArg
 // ---------------------------------------------------------------------------
 int expert_max_group(int T) { return T <= 1 ? 1 : 8; }
 
-static int pick_kc(int K, int kcmax) {
-  int kc = kcmax;
-  while (kc > 128 && (K % kc) != 0) kc >>= 1;
-  if (kc > K) kc = K;
-  while (K % kc) kc >>= 1;
-  return kc;
-}
-
-template <int MODE, int G, int KCMAX, int W, int D>
+template <int MODE, int G, int W, int D>
 static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
-  using Lay = Layout<G, KCMAX>;
-  auto kern = expert_kernel<MODE, G, KCMAX, W, D>;
-  const int smem = W * D * Lay::kSlot + 2 * W * D * 8;
-  static_assert(W * D * Lay::kSlot + 2 * W * D * 8 <= 232448, "shared memory budget");
+  using Lay = Layout<G>;
+  auto kern = expert_kernel<MODE, G, W, D>;
+  constexpr int smem = W * D * Lay::kSlot + W * Lay::kTable + 2 * W * D * 8 + 1024;  // +1 KB alignment slack
+  static_assert(smem <= 232448, "shared memory budget");
   static unsigned long long attr_done = 0;  // one bit per device, per template instance
   int dev = 0;
   cudaGetDevice(&dev);
@@ -250,7 +338,28 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
       return LMOE_ECUDA;
     attr_done |= 1ull << (dev & 63);
   }
-  a.kc = pick_kc(a.K, KCMAX);
+  // K chunk: the whole K when K <= 1024, else 1024 (K is a multiple of 1024 then)
+  a.kc = a.K <= kKC ? a.K : kKC;
+  const int rows_per_expert = (MODE == MODE_GATEUP) ? 2 * a.inter : a.latent;
+  const uint64_t rows_total = (uint64_t)a.n_experts * rows_per_expert;
+  CUtensorMap tq, ts;
+  {
+    // codes as {128 B, rows, K/256 planes}: plane stride 128 B, row stride K/2 B
+    const uint64_t dims[3] = {128, rows_total, (uint64_t)a.K / 256};
+    const uint64_t strides[2] = {(uint64_t)a.K / 2, 128};
+    const uint32_t box[3] = {128, 16, (uint32_t)(a.kc / 256)};
+    if (get_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LMOE_ECUDA;
+  }
+  if (a.K > kKC) {
+    const uint64_t dims[2] = {(uint64_t)a.K / 32, rows_total};
+    const uint64_t strides[1] = {(uint64_t)a.K / 32};
+    const uint32_t box[2] = {(uint32_t)(a.kc / 32), 16};
+    if (get_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return LMOE_ECUDA;
+  } else {
+    ts = tq;  // unused: one chunk copies the scales with a bulk copy
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(32 * (W + 1));
@@ -261,17 +370,17 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+  return cudaLaunchKernelEx(&cfg, kern, a, tq, ts) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 2048, 5, 2>(a, s, num_sms);
-  return launch_one<MODE_GATEUP, 8, 1024, 4, 2>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 5, 2>(a, s, num_sms);
+  return launch_one<MODE_GATEUP, 8, 5, 1>(a, s, num_sms);
 }
 
 int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_DOWN, 1, 2048, 5, 2>(a, s, num_sms);
-  return launch_one<MODE_DOWN, 8, 1024, 4, 2>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_DOWN, 1, 5, 2>(a, s, num_sms);
+  return launch_one<MODE_DOWN, 8, 5, 1>(a, s, num_sms);
 }
 
 }  // namespace lmoe

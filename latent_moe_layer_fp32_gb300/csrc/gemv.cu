@@ -7,34 +7,44 @@
 // "Correctness": bf16 values with fp32 accumulation.
 //
 // out[t][n] = bf16_rne(sum_k act[t][k] * W[n][k]).  At small T this is a
-// weight stream: each item is 16 weight rows x all of K for a group of up to
-// 8*NT tokens; weights and the matching activation chunk arrive by TMA bulk
-// copies in per-warp mbarrier rings, and mma.sync m16n8k16 (bf16 in, fp32
-// accumulate) does the products with both operands fed by ldmatrix.
+// weight stream.  Item = 16 weight rows x all of K for a group of up to 8*NT
+// tokens; the W consumer warps of a CTA share an item (chunk c of 256 K
+// elements goes to warp c % W) and add their fp32 partials in warp order at
+// the end.  Per chunk the producer issues one TMA tensor copy of the weights
+// (a 3-D view {64 elements, rows, K/64} with 128-byte swizzle: 16 rows x 256
+// elements, 8 KB) and one of the token rows (tokens beyond T read as zero);
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) takes both operands by
+// ldmatrix from the swizzled boxes.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tmap.cuh"
 
 namespace lmoe {
 
-template <int NT, int KC>
+constexpr int kGemvKC = 256;  // K elements per chunk (4 planes of 64)
+
+template <int NT>
 struct GemvLayout {
-  static constexpr int kRow = KC * 2 + 16;  // padded row: ldmatrix phases hit distinct banks
-  static constexpr int kW = 16 * kRow;
-  static constexpr int kA = 8 * NT * kRow;
-  static constexpr int kSlot = (kW + kA + 127) / 128 * 128;
+  static constexpr int kW = 16 * kGemvKC * 2;       // 8 KB
+  static constexpr int kA = 8 * NT * kGemvKC * 2;   // 4 KB per n-tile
+  static constexpr int kSlot = (kW + kA + 1023) / 1024 * 1024;
 };
 
-template <int NT, int KC, int W, int D>
-__global__ void __launch_bounds__(32 * (W + 1), 1) gemv_bf16_kernel(const GemvArgs a) {
-  using Lay = GemvLayout<NT, KC>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + W * D * Lay::kSlot);
+template <int NT, int W, int D>
+__global__ void __launch_bounds__(32 * (W + 1), 1)
+    gemv_bf16_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x) {
+  using Lay = GemvLayout<NT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* red = reinterpret_cast<float*>(smem + W * D * Lay::kSlot);  // [W][NT][4][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + W * NT * 4 * 32);
   uint64_t* empty = full + W * D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K, nch = K / KC;
+  const int K = a.K, nch = K / kGemvKC;
   constexpr int GT = 8 * NT;
   const int ngroups = (a.T + GT - 1) / GT;
-  const int n_items = (a.N / 16) * ngroups;
+  const int mtiles = a.N / 16;
+  const int n_items = mtiles * ngroups;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * D; ++i) {
@@ -49,40 +59,34 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) gemv_bf16_kernel(const GemvAr
 
   const int it0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
-  const int nloc = it1 - it0;
 
   if (warp == W) {
     if (lane != 0) return;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
     const uint64_t pol = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
     int seq[W];
 #pragma unroll
     for (int w = 0; w < W; ++w) seq[w] = 0;
     bool ok = true;
-    for (int base = 0; base < nloc && ok; base += W) {
-      const int nw = min(W, nloc - base);
-      for (int c = 0; c < nch && ok; ++c) {
-        const int k0 = c * KC;
-        for (int w = 0; w < nw; ++w) {
-          const int it = it0 + base + w;
-          // token group outer, row tile inner: consecutive items share tokens
-          const int tg = it / (a.N / 16), mt = it % (a.N / 16);
-          const int t0 = tg * GT, ntok = min(GT, a.T - t0);
-          const int d = seq[w] % D;
-          const uint32_t par = ((seq[w] / D) & 1) ^ 1;
-          ++seq[w];
-          if (!mbar_wait(&empty[w * D + d], par, a.st, 11)) {
-            ok = false;
-            break;
-          }
-          uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
-          uint64_t* bar = &full[w * D + d];
-          mbar_arrive_expect_tx(bar, 16u * KC * 2 + (uint32_t)ntok * KC * 2);
-#pragma unroll 4
-          for (int i = 0; i < 16; ++i)
-            bulk_g2s_stream(slot + i * Lay::kRow, a.w + (size_t)(mt * 16 + i) * K + k0, KC * 2, bar, pol);
-          for (int j = 0; j < ntok; ++j)
-            bulk_g2s(slot + Lay::kW + j * Lay::kRow, a.act + (size_t)(t0 + j) * K + k0, KC * 2, bar);
+    for (int it = it0; it < it1 && ok; ++it) {
+      // token group outer, row tile inner: consecutive items share tokens
+      const int tg = it / mtiles, mt = it % mtiles;
+      for (int c = 0; c < nch; ++c) {
+        const int w = c % W;
+        const int d = seq[w] % D;
+        const uint32_t par = ((seq[w] / D) & 1) ^ 1;
+        ++seq[w];
+        if (!mbar_wait(&empty[w * D + d], par, a.st, 11)) {
+          ok = false;
+          break;
         }
+        uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
+        uint64_t* bar = &full[w * D + d];
+        mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // out-of-range token rows are zero-filled, bytes still count
+        tma_load_3d(slot, &tm_w, 0, mt * 16, c * 4, bar, pol);
+        tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * 4, bar, pol_x);
       }
     }
 #pragma unroll
@@ -92,36 +96,44 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) gemv_bf16_kernel(const GemvAr
   }
 
   const int g = lane >> 2, q = lane & 3;
-  const int lm_m = lane >> 3, lm_r = lane & 7;
-  // A (weights, 16 rows x 16 k): matrices (rows 0-7,k0-7) (rows 8-15,k0-7) (rows 0-7,k8-15) (rows 8-15,k8-15)
-  const int a_row = lm_r + 8 * (lm_m & 1), a_col = 16 * (lm_m >> 1);
-  // B (tokens, 8 x 16 k) via x4: matrices (tok 0-7,k0-7) (tok 0-7,k8-15) for k-step s and s+1
-  const int b_col = 16 * (lm_m & 1) + 32 * (lm_m >> 1);
+  const int lm = lane >> 3, rr = lane & 7;
+  // A (weights, 16 rows x 16 k) x4: (rows 0-7,k0-7) (rows 8-15,k0-7) (rows 0-7,k8-15) (rows 8-15,k8-15)
+  const int a_row = rr + 8 * (lm & 1), a_k8 = lm >> 1;
+  // B (tokens, 8 x 16 k) x4 over k-steps s, s+1: (k0-7) (k8-15) (k16-23) (k24-31)
+  const int b_k8 = lm;
   int seq = 0;
-  for (int j = warp; j < nloc; j += W) {
-    const int it = it0 + j;
-    const int tg = it / (a.N / 16), mt = it % (a.N / 16);
+  bool alive = true;
+  for (int it = it0; it < it1; ++it) {
+    const int tg = it / mtiles, mt = it % mtiles;
     const int t0 = tg * GT, ntok = min(GT, a.T - t0);
     float acc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    for (int c = 0; c < nch; ++c) {
+    for (int c = warp; c < nch && alive; c += W) {
       const int d = seq % D;
       const uint32_t par = (seq / D) & 1;
       ++seq;
-      if (!mbar_wait(&full[warp * D + d], par, a.st, 13)) return;
+      if (!mbar_wait(&full[warp * D + d], par, a.st, 13)) {
+        alive = false;
+        break;
+      }
       const uint32_t base = smem_u32(smem + (warp * D + d) * Lay::kSlot);
-      const uint32_t a_addr = base + a_row * Lay::kRow + a_col;
-      const uint32_t b_addr = base + Lay::kW + lm_r * Lay::kRow + b_col;
+      const uint32_t xbase = base + Lay::kW;
 #pragma unroll 4
-      for (int ks = 0; ks < KC / 16; ks += 2) {
+      for (int ks = 0; ks < kGemvKC / 16; ks += 2) {
+        // element k of the chunk: plane k/64, 16-byte chunk (k%64)/8
         uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-        ldmatrix_x4(a0, a1, a2, a3, a_addr + ks * 32);
-        ldmatrix_x4(a4, a5, a6, a7, a_addr + ks * 32 + 32);
+        {
+          const int k8 = ks * 2 + a_k8;  // 8-element column index for k-step ks
+          ldmatrix_x4(a0, a1, a2, a3, base + swz128(k8 >> 3, 16, a_row, k8 & 7));
+          const int k8b = k8 + 2;        // k-step ks + 1
+          ldmatrix_x4(a4, a5, a6, a7, base + swz128(k8b >> 3, 16, a_row, k8b & 7));
+        }
+        const int bk8 = ks * 2 + b_k8;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(b0, b1, b2, b3, b_addr + n * 8 * Lay::kRow + ks * 32);
+          ldmatrix_x4(b0, b1, b2, b3, xbase + swz128(bk8 >> 3, GT, n * 8 + rr, bk8 & 7));
           mma_bf16(acc[n], a0, a1, a2, a3, b0, b1);
           mma_bf16(acc[n], a4, a5, a6, a7, b2, b3);
         }
@@ -129,26 +141,41 @@ __global__ void __launch_bounds__(32 * (W + 1), 1) gemv_bf16_kernel(const GemvAr
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[warp * D + d]);
     }
+    // cross-warp reduction in warp order (named barrier over the consumers only)
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int tok = n * 8 + 2 * q + i;
-        if (tok < ntok) {
-          uint16_t* o = a.out + (size_t)(t0 + tok) * a.N + mt * 16;
-          o[g] = f32_to_bf16_bits(acc[n][i]);
-          o[g + 8] = f32_to_bf16_bits(acc[n][2 + i]);
+      for (int i = 0; i < 4; ++i) red[((warp * NT + n) * 4 + i) * 32 + lane] = acc[n][i];
+    asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+    if (warp == 0) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[i] = red[((0 * NT + n) * 4 + i) * 32 + lane];
+          for (int w = 1; w < W; ++w) v[i] += red[((w * NT + n) * 4 + i) * 32 + lane];
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = n * 8 + 2 * q + i;
+          if (tok < ntok) {
+            uint16_t* o = a.out + (size_t)(t0 + tok) * a.N + mt * 16;
+            o[g] = f32_to_bf16_bits(v[i]);
+            o[g + 8] = f32_to_bf16_bits(v[2 + i]);
+          }
         }
       }
     }
+    asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
   }
 }
 
-template <int NT, int KC, int W, int D>
+template <int NT, int W, int D>
 static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
-  using Lay = GemvLayout<NT, KC>;
-  auto kern = gemv_bf16_kernel<NT, KC, W, D>;
-  constexpr int smem = W * D * Lay::kSlot + 2 * W * D * 8;
+  using Lay = GemvLayout<NT>;
+  auto kern = gemv_bf16_kernel<NT, W, D>;
+  constexpr int smem = W * D * Lay::kSlot + W * NT * 4 * 32 * 4 + 2 * W * D * 8 + 1024;
   static_assert(smem <= 232448, "shared memory budget");
   static unsigned long long attr_done = 0;
   int dev = 0;
@@ -157,6 +184,22 @@ static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return LMOE_ECUDA;
     attr_done |= 1ull << (dev & 63);
+  }
+  CUtensorMap tw, tx;
+  {
+    // {64 elements (128 B), rows, K/64 planes}: plane stride 128 B, row stride 2K B
+    const uint64_t dims[3] = {64, (uint64_t)a.N, (uint64_t)a.K / 64};
+    const uint64_t strides[2] = {(uint64_t)a.K * 2, 128};
+    const uint32_t box[3] = {64, 16, kGemvKC / 64};
+    if (get_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LMOE_ECUDA;
+  }
+  {
+    const uint64_t dims[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
+    const uint64_t strides[2] = {(uint64_t)a.K * 2, 128};
+    const uint32_t box[3] = {64, (uint32_t)(8 * NT), kGemvKC / 64};
+    if (get_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.act, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LMOE_ECUDA;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
@@ -168,18 +211,13 @@ static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+  return cudaLaunchKernelEx(&cfg, kern, a, tw, tx) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
 int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms) {
-  if (a.K % 512 != 0) {
-    // small K (tiny shapes): one chunk of 128
-    if (a.T <= 8) return launch_gemv<1, 128, 4, 2>(a, s, num_sms);
-    return launch_gemv<4, 128, 4, 2>(a, s, num_sms);
-  }
-  if (a.T <= 8) return launch_gemv<1, 512, 4, 2>(a, s, num_sms);
-  if (a.T <= 16) return launch_gemv<2, 512, 3, 2>(a, s, num_sms);
-  return launch_gemv<4, 512, 4, 1>(a, s, num_sms);
+  if (a.T <= 8) return launch_gemv<1, 4, 4>(a, s, num_sms);
+  if (a.T <= 16) return launch_gemv<2, 4, 3>(a, s, num_sms);
+  return launch_gemv<4, 4, 2>(a, s, num_sms);
 }
 
 }  // namespace lmoe

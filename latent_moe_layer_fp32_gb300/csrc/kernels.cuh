@@ -30,8 +30,10 @@ struct ExpertArgs {
   int inter;                // I
   int latent;               // L
   int top_k;
+  int n_experts;
   uint16_t* h_out;          // gate/up: bf16 [R_sorted][I]
   float* y_out;             // down: fp32 [R][L] by original row id
+  float* ssq_out;           // down: fp32 [R][L/32] sum of y^2 per 32-row tile (may be null)
   Status* st;
 };
 
@@ -53,8 +55,9 @@ int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 __global__ void prep_act_kernel(const uint16_t* in, int K, uint16_t* out16, int32_t* exps);
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
                                            int4* groups, int32_t* n_groups, Status* st);
-__global__ void combine_kernel(const float* y, const int32_t* topk_idx, const float* topk_w, const uint16_t* norm_g,
-                               int L, int k, int E, float eps, uint16_t* zb, Status* st);
+__global__ void ssq_kernel(const float* y, int R, int L, float* ssq);
+__global__ void combine_kernel(const float* y, const float* ssq, const int32_t* topk_idx, const float* topk_w,
+                               const uint16_t* norm_g, int L, int k, int E, float eps, uint16_t* zb, Status* st);
 __global__ void e2m1_selftest_kernel(float* out);
 
 }  // namespace lmoe

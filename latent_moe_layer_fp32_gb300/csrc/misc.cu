@@ -95,55 +95,61 @@ __global__ void __launch_bounds__(256) groups_from_offsets_kernel(const int32_t*
   }
 }
 
+// Sum of squares of each route row per 32-column tile: ssq[r][tile] (used when
+// y comes from the caller; the down kernel writes the same partials itself).
+// One warp per (row, tile), 8 per CTA.
+__global__ void __launch_bounds__(256) ssq_kernel(const float* __restrict__ y, int R, int L,
+                                                  float* __restrict__ ssq) {
+  pdl_wait();
+  pdl_trigger();
+  const int tiles = L / 32;
+  const long long i = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (i >= (long long)R * tiles) return;
+  const int r = (int)(i / tiles), tile = (int)(i % tiles), lane = threadIdx.x & 31;
+  const float v = y[(size_t)r * L + tile * 32 + lane];
+  const float s = warp_sum(v * v);
+  if (lane == 0) ssq[i] = s;
+}
+
 // post_expert_norm on each route row, then the fp32 weighted sum in route
 // order ("Muse Spark Open on Gaudi 2", "The latent MoE: A' with a per-expert
-// norm").  One CTA (256 threads) per token t:
-//   ss_j  = sum_l y[t*k+j][l]^2            (fixed reduction tree)
+// norm").  Grid (T, ceil(L/512)), 256 threads, 2 columns per thread:
+//   ss_j  = sum over the row's 32-column tiles of ssq (fixed order)
 //   rinv  = 1 / sqrt(ss_j / L + eps)
 //   z[l]  = sum_j w[t][j] * ((y * rinv) * g[e_j][l]),  zb = bf16(z)
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ topk_idx,
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ssq,
+                                                      const int32_t* __restrict__ topk_idx,
                                                       const float* __restrict__ topk_w,
                                                       const uint16_t* __restrict__ norm_g, int L, int k, int E,
                                                       float eps, uint16_t* __restrict__ zb, Status* st) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[8][8];
   __shared__ float s_rinv[8];
   __shared__ int s_e[8];
   __shared__ float s_w[8];
   const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid < k) {
-    int e = topk_idx[(size_t)t * k + tid];
-    if (e < 0 || e >= E) {
-      set_error(st, LMOE_EDEVICE_CHECK, 102);
-      e = 0;
-    }
-    s_e[tid] = e;
-    s_w[tid] = topk_w[(size_t)t * k + tid];
-  }
-  float ss[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    ss[j] = 0.f;
-    if (j < k) {
-      const float* yr = y + ((size_t)t * k + j) * L;
-      for (int l = tid; l < L; l += 256) ss[j] = fmaf(yr[l], yr[l], ss[j]);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float v = warp_sum(ss[j]);
-    if (lane == 0) red[j][warp] = v;
-  }
-  __syncthreads();
-  if (tid < k) {
+  const int tiles = L / 32;
+  if (warp < k) {
+    const int r = t * k + warp;
     float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) s += red[tid][w];
-    s_rinv[tid] = 1.0f / sqrtf(s / (float)L + eps);
+    for (int i = lane; i < tiles; i += 32) s += ssq[(size_t)r * tiles + i];
+    s = warp_sum(s);
+    if (lane == 0) {
+      int e = topk_idx[r];
+      if (e < 0 || e >= E) {
+        set_error(st, LMOE_EDEVICE_CHECK, 102);
+        e = 0;
+      }
+      s_e[warp] = e;
+      s_w[warp] = topk_w[r];
+      s_rinv[warp] = 1.0f / sqrtf(s / (float)L + eps);
+    }
   }
   __syncthreads();
-  for (int l = tid; l < L; l += 256) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int l = blockIdx.y * 512 + h * 256 + tid;
+    if (l >= L) break;
     float z = 0.f;
     for (int j = 0; j < k; ++j) {
       const float yv = y[((size_t)t * k + j) * L + l];

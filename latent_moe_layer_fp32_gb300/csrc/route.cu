@@ -85,21 +85,29 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
                                                    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   pdl_wait();
   pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
+  // one CTA per token: thread e sums its nsplit partials (independent loads,
+  // summed in split order), then warp 0 selects the top k
+  __shared__ float s_lg[256];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  if (tid < E) {
+    float v[16];
+#pragma unroll
+    for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? part[((size_t)sp * T + t) * E + tid] : 0.f;
+    float acc = v[0];
+#pragma unroll
+    for (int sp = 1; sp < 16; ++sp)
+      if (sp < nsplit) acc += v[sp];
+    if (bias) acc = acc + bias[tid];
+    s_lg[tid] = acc;
+  }
+  __syncthreads();
+  if (tid >= 32) return;
   float lg[8];
   bool taken[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    float v = -INFINITY;
-    if (e < E) {
-      v = 0.f;
-      for (int s = 0; s < nsplit; ++s) v += part[((size_t)s * T + t) * E + e];
-      if (bias) v = v + bias[e];
-    }
-    lg[i] = v;
+    lg[i] = e < E ? s_lg[e] : -INFINITY;
     taken[i] = (e >= E);
   }
   float mx = -INFINITY;
@@ -107,7 +115,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   for (int i = 0; i < 8; ++i) mx = fmaxf(mx, lg[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-
   float sel_p[8];
   int sel_e[8];
   float den = 0.f;
@@ -175,6 +182,7 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
   __shared__ int s_count[256];
   __shared__ int s_fill[256];
   __shared__ int s_off[257];
+  __shared__ int s_goff[256];
   __shared__ int s_wcnt[32][256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < 256; e += kTableThreads) s_count[e] = 0;
@@ -188,16 +196,48 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
     atomicAdd(&s_count[e], 1);
   }
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0, ng = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = acc;
-      const int n = s_count[e];
-      for (int g0 = 0; g0 < n; g0 += G) groups[ng++] = make_int4(e, acc + g0, min(G, n - g0), 0);
-      acc += n;
+  // exclusive scans (warp 0, 8 experts per lane, lane order = expert order):
+  // row offsets and group offsets
+  if (warp == 0) {
+    int cnt[8], gcnt[8], rs = 0, gs = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      cnt[i] = e < E ? s_count[e] : 0;
+      gcnt[i] = (cnt[i] + G - 1) / G;
+      rs += cnt[i];
+      gs += gcnt[i];
     }
-    s_off[E] = acc;
-    *n_groups = ng;
+    int rx = rs, gx = gs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ry = __shfl_up_sync(0xffffffffu, rx, o), gy = __shfl_up_sync(0xffffffffu, gx, o);
+      if (lane >= o) {
+        rx += ry;
+        gx += gy;
+      }
+    }
+    int racc = rx - rs, gacc = gx - gs;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) {
+        s_off[e] = racc;
+        s_goff[e] = gacc;
+      }
+      racc += cnt[i];
+      gacc += gcnt[i];
+    }
+    if (lane == 31) {
+      s_off[E] = racc;
+      *n_groups = gacc;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kTableThreads) {
+    const int n = s_count[e], a0 = s_off[e];
+    int gi = s_goff[e];
+    for (int g0 = 0; g0 < n; g0 += G) groups[gi++] = make_int4(e, a0 + g0, min(G, n - g0), 0);
   }
   for (int e = tid; e < 256; e += kTableThreads) s_fill[e] = 0;
   __syncthreads();

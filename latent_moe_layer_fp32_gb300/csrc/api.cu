@@ -53,9 +53,10 @@ int check_dims(const lmoe_dims* d) {
       d->n_experts > 256 || d->hidden < 128 || d->latent < 128 || d->inter < 128 || d->hidden % 128 ||
       d->latent % 128 || d->inter % 128 || !(d->eps >= 0.f))
     return LMOE_EINVAL;
-  // expert and projection kernels stream K in 128-byte planes and 1024-element chunks
+  // expert kernels stream K in 128-byte planes and 2048-element chunks, the
+  // projections in 256- or 512-element chunks
   if (d->hidden % 256 || d->latent % 256 || d->inter % 256) return LMOE_EUNSUPPORTED;
-  if ((d->latent > 1024 && d->latent % 1024) || (d->inter > 1024 && d->inter % 1024)) return LMOE_EUNSUPPORTED;
+  if ((d->latent > 2048 && d->latent % 2048) || (d->inter > 2048 && d->inter % 2048)) return LMOE_EUNSUPPORTED;
   return LMOE_OK;
 }
 

@@ -15,7 +15,7 @@
 //
 // CTA = W consumer warps + 1 producer warp.  Per K chunk the producer issues
 // two TMA tensor copies of the codes (16 rows x kc/2 bytes each, a 3-D view
-// {128 B, rows, K/256} with 128-byte swizzle, so each copy is one 8 KB
+// {128 B, rows, K/256} with 128-byte swizzle, so each copy is one 16 KB
 // request and ldmatrix reads it without bank conflicts), two of the E8M0
 // scales and one bulk copy per activation row, into per-warp mbarrier rings
 // of D slots; consumer warp w takes items w, w+W, ... of the CTA's range.
@@ -37,25 +37,24 @@ namespace lmoe {
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
 constexpr int kRows = 32;  // weight rows per item: two m16 tiles
-constexpr int kKC = 1024;  // K elements per chunk when K > 1024 (else the whole K)
+constexpr int kKC = 2048;  // K elements per chunk when K > 2048 (else the whole K): 16 KB code boxes
 
 template <int G>
 struct Layout {
-  static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (8 KB)
+  static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (16 KB)
   static constexpr int kCodes = 2 * kBox;      // box A (rows 0-15 of the item), box B (rows 16-31)
   static constexpr int kScales = kRows * (kKC / 32);
   static constexpr int kActRow = kKC * 2 + 64;  // padded: conflict-free 16-byte loads
   static constexpr int kActs = G * kActRow;
   static constexpr int kSlot = (kCodes + kScales + kActs + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
-  // per consumer warp: the chunk's block scales as fp32, [block][mtile][g][lo,hi]
-  static constexpr int kTable = (kKC / 32) * 2 * 8 * 2 * 4;
 };
 
-// Expand the chunk's E8M0 bytes (scale region [32 rows][nb]) into fp32
-// 2^(s-127) in the warp's table.  Fast path s << 23 is exact for
-// 1 <= s <= 254; a chunk holding 0 or 255 takes the exact per-value path.
+// Expand the E8M0 bytes of one 128-byte plane (8 blocks; scale region
+// [32 rows][nb], blocks p*8 .. p*8+7) into fp32 2^(s-127) in the warp's table
+// [block][mtile][g][lo,hi].  Fast path s << 23 is exact for 1 <= s <= 254; a
+// plane holding 0 or 255 takes the exact per-value path.
 template <int MODE>
-__device__ __forceinline__ void expand_scales(const uint8_t* sc, int nb, float* table, int lane) {
+__device__ __forceinline__ void expand_plane_scales(const uint8_t* sc, int nb, int p, float* table, int lane) {
   const int r = lane;  // region row: rows 0-15 from box A, 16-31 from box B
   const int box = r >> 4, rb = r & 15;
   // gate/up: box A = gate (lo), box B = up (hi); m-tile = rb / 8.
@@ -63,37 +62,89 @@ __device__ __forceinline__ void expand_scales(const uint8_t* sc, int nb, float* 
   const int mt = (MODE == MODE_GATEUP) ? (rb >> 3) : box;
   const int hi = (MODE == MODE_GATEUP) ? box : (rb >> 3);
   const int g = r & 7;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(sc + r * nb);
-  bool special = false;
-  for (int j = 0; j < nb / 4; ++j) {
-    const uint32_t w = src[j];
-    special |= (__vcmpeq4(w, 0u) | __vcmpeq4(w, 0xffffffffu)) != 0u;
-  }
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(sc + r * nb + p * 8);
+  const uint32_t w0 = src[0], w1 = src[1];
+  bool special = ((__vcmpeq4(w0, 0u) | __vcmpeq4(w0, 0xffffffffu) | __vcmpeq4(w1, 0u) |
+                   __vcmpeq4(w1, 0xffffffffu)) != 0u);
   special = __any_sync(0xffffffffu, special);
   float* dst = table + (mt * 8 + g) * 2 + hi;
   if (!special) {
-    for (int j = 0; j < nb / 4; ++j) {
-      const uint32_t w = src[j];
-      dst[(4 * j + 0) * 32] = __uint_as_float((w << 23) & 0x7f800000u);
-      dst[(4 * j + 1) * 32] = __uint_as_float((w << 15) & 0x7f800000u);
-      dst[(4 * j + 2) * 32] = __uint_as_float((w << 7) & 0x7f800000u);
-      dst[(4 * j + 3) * 32] = __uint_as_float((w >> 1) & 0x7f800000u);
-    }
+    dst[0 * 32] = __uint_as_float((w0 << 23) & 0x7f800000u);
+    dst[1 * 32] = __uint_as_float((w0 << 15) & 0x7f800000u);
+    dst[2 * 32] = __uint_as_float((w0 << 7) & 0x7f800000u);
+    dst[3 * 32] = __uint_as_float((w0 >> 1) & 0x7f800000u);
+    dst[4 * 32] = __uint_as_float((w1 << 23) & 0x7f800000u);
+    dst[5 * 32] = __uint_as_float((w1 << 15) & 0x7f800000u);
+    dst[6 * 32] = __uint_as_float((w1 << 7) & 0x7f800000u);
+    dst[7 * 32] = __uint_as_float((w1 >> 1) & 0x7f800000u);
   } else {
-    for (int j = 0; j < nb; ++j) dst[j * 32] = e8m0_to_f32(sc[r * nb + j]);
+    for (int j = 0; j < 8; ++j) dst[j * 32] = e8m0_to_f32(sc[r * nb + p * 8 + j]);
   }
 }
 
-template <int MODE, int G, int W, int D>
-__global__ void __launch_bounds__(32 * (W + 1), 1)
+// The 8 blocks of one 128-byte plane p of a chunk.  The four 16-byte chunk
+// offsets a lane reads are fixed by the swizzle (chunk ^ (row & 7)), so every
+// address is a per-lane base plus an immediate.  `table` holds this plane's
+// scales only.
+template <int NV>
+__device__ __forceinline__ void plane_blocks(uint32_t sbase, uint32_t act_addr, const float* table,
+                                             const uint32_t (&box_off)[2], const int (&row_in_box)[2], int lm, int g,
+                                             float (&acc)[2][2][NV], int p) {
+  const float2* tab2 = reinterpret_cast<const float2*>(table) + g;
+  const int rr = row_in_box[0] & 7;  // both m-tiles' rows share row & 7
+  const uint32_t pb0 = sbase + box_off[0] + row_in_box[0] * 128 + p * 2048;  // plane stride: 16 rows x 128 B
+  const uint32_t pb1 = sbase + box_off[1] + row_in_box[1] * 128 + p * 2048;
+  const uint32_t pact = act_addr + p * 512;  // 8 blocks x 64 B
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t coff = static_cast<uint32_t>(((2 * i + (lm >> 1)) ^ rr) << 4);
+    uint32_t w[2][4];
+    ldmatrix_x4(w[0][0], w[0][1], w[0][2], w[0][3], pb0 + coff);
+    ldmatrix_x4(w[1][0], w[1][1], w[1][2], w[1][3], pb1 + coff);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int blk = 2 * i + half;  // block within the plane
+      uint32_t b0, b1, b2, b3;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                   : "r"(pact + blk * 64));
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+        e2m1x8_to_f16x8(w[m][2 * half], l0, l1, l2, l3);
+        e2m1x8_to_f16x8(w[m][2 * half + 1], h0, h1, h2, h3);
+        float dacc[4];
+        mma_f16_zero(dacc, l0, h0, l1, h1, b0, b1);
+        mma_f16(dacc, l2, h2, l3, h3, b2, b3);
+        const float2 sc = tab2[(blk * 2 + m) * 8];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          acc[m][0][v] = fmaf(dacc[v], sc.x, acc[m][0][v]);
+          acc[m][1][v] = fmaf(dacc[2 + v], sc.y, acc[m][1][v]);
+        }
+      }
+    }
+  }
+}
+
+template <int MODE, int G, int NGRP, int Q, int D>
+__global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
     expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s) {
+  // NGRP groups of Q consumer warps; group gi owns a ring of D slots and the
+  // CTA items gi, gi+NGRP, ...; its Q warps share every slot, member j taking
+  // the chunk's 128-byte planes j, j+Q, ...; the members' fp32 partials are
+  // added in member order at the end of each item.
   using Lay = Layout<G>;
+  constexpr int NW = NGRP * Q;
+  constexpr int NV = (G == 1) ? 1 : 2;  // token columns per lane that can hold a valid token
+  constexpr int kRed = 2 * 2 * NV * 32;  // floats per member partial
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1 KB alignment for the swizzled boxes
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* tables = reinterpret_cast<float*>(smem + W * D * Lay::kSlot);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + W * D * Lay::kSlot + W * Lay::kTable);
-  uint64_t* empty = full + W * D;
+  float* tables = reinterpret_cast<float*>(smem + NGRP * D * Lay::kSlot);      // [NW][8*2*8*2]
+  float* red = tables + NW * 256;                                              // [NW][kRed]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + NW * kRed);
+  uint64_t* empty = full + NGRP * D;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
@@ -103,9 +154,9 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
   const int kact_row = kc * 2 + 64;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < W * D; ++i) {
+    for (int i = 0; i < NGRP * D; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], Q);
     }
     fence_barrier_init();
   }
@@ -118,36 +169,36 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
   const int nloc = it1 - it0;
 
-  if (warp == W) {
+  if (warp == NW) {
     // ------------------------------ producer ------------------------------
     const uint64_t pol = policy_evict_first();
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
     }
-    int seq[W];
+    int seq[NGRP];
 #pragma unroll
-    for (int w = 0; w < W; ++w) seq[w] = 0;
+    for (int gi = 0; gi < NGRP; ++gi) seq[gi] = 0;
     bool ok = true;
-    for (int base = 0; base < nloc && ok; base += W) {
-      const int nw = min(W, nloc - base);
+    for (int base = 0; base < nloc && ok; base += NGRP) {
+      const int ng = min(NGRP, nloc - base);
       for (int c = 0; c < nch && ok; ++c) {
-        for (int w = 0; w < nw; ++w) {
-          const int it = it0 + base + w;
+        for (int gi = 0; gi < ng; ++gi) {
+          const int it = it0 + base + gi;
           const int grp = it / tiles, tile = it % tiles;
-          const int4 gi = a.groups[grp];
-          const int e = gi.x, p0 = gi.y, ntok = gi.z;
-          const int d = seq[w] % D;
-          const uint32_t par = ((seq[w] / D) & 1) ^ 1;
-          ++seq[w];
+          const int4 gq = a.groups[grp];
+          const int e = gq.x, p0 = gq.y, ntok = gq.z;
+          const int d = seq[gi] % D;
+          const uint32_t par = ((seq[gi] / D) & 1) ^ 1;
+          ++seq[gi];
           int got = 1;
-          if (lane == 0) got = mbar_wait(&empty[w * D + d], par, a.st, 1);
+          if (lane == 0) got = mbar_wait(&empty[gi * D + d], par, a.st, 1);
           if (!__shfl_sync(0xffffffffu, got, 0)) {
             ok = false;
             break;
           }
-          uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
-          uint64_t* bar = &full[w * D + d];
+          uint8_t* slot = smem + (gi * D + d) * Lay::kSlot;
+          uint64_t* bar = &full[gi * D + d];
           // first rows of box A and box B
           int rowA, rowB;
           if (MODE == MODE_GATEUP) {
@@ -182,19 +233,20 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
     // drain: no copy may still be in flight when this warp leaves
     if (lane == 0) {
 #pragma unroll
-      for (int w = 0; w < W; ++w)
-        for (int s = max(0, seq[w] - D); s < seq[w]; ++s)
-          mbar_wait(&full[w * D + (s % D)], (s / D) & 1, a.st, 2);
+      for (int gi = 0; gi < NGRP; ++gi)
+        for (int s = max(0, seq[gi] - D); s < seq[gi]; ++s)
+          mbar_wait(&full[gi * D + (s % D)], (s / D) & 1, a.st, 2);
     }
     return;
   }
 
   // -------------------------------- consumer --------------------------------
+  const int gi = warp / Q, mem = warp % Q;
   const int g = lane >> 2, q = lane & 3;
   // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
   const int lm = lane >> 3, rr = lane & 7;
-  float* table = tables + warp * (Lay::kTable / 4);
-  constexpr int NV = (G == 1) ? 1 : 2;  // token columns per lane that can hold a valid token
+  float* table = tables + warp * 256;
+  float* my_red = red + warp * kRed;
   // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
   uint32_t box_off[2];
   int row_in_box[2];
@@ -211,12 +263,14 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
     box_off[m] = box * 16 * (kc / 2);
     row_in_box[m] = row;
   }
+  const int nplanes = nb / 8;
   int seq = 0;
-  for (int j = warp; j < nloc; j += W) {
+  bool alive = true;
+  for (int j = gi; j < nloc; j += NGRP) {
     const int it = it0 + j;
     const int grp = it / tiles, tile = it % tiles;
-    const int4 gi = a.groups[grp];
-    const int p0 = gi.y, ntok = gi.z;
+    const int4 gq = a.groups[grp];
+    const int p0 = gq.y, ntok = gq.z;
     float acc[2][2][NV];  // [mtile][lo/hi row][token column]
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -224,98 +278,91 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int v = 0; v < NV; ++v) acc[m][h][v] = 0.f;
-    for (int c = 0; c < nch; ++c) {
+    for (int c = 0; c < nch && alive; ++c) {
       const int d = seq % D;
       const uint32_t par = (seq / D) & 1;
       ++seq;
-      if (!mbar_wait(&full[warp * D + d], par, a.st, 3)) return;
-      const uint8_t* slot = smem + (warp * D + d) * Lay::kSlot;
-      expand_scales<MODE>(slot + Lay::kCodes, nb, table, lane);
-      __syncwarp();
+      if (!mbar_wait(&full[gi * D + d], par, a.st, 3)) {
+        alive = false;
+        break;
+      }
+      const uint8_t* slot = smem + (gi * D + d) * Lay::kSlot;
       const uint32_t sbase = smem_u32(slot);
       const uint32_t act_addr = smem_u32(slot + Lay::kCodes + Lay::kScales) + (g < G ? g : 0) * kact_row + q * 16;
-      const float2* tab2 = reinterpret_cast<const float2*>(table) + g;
-#pragma unroll 2
-      for (int bb = 0; bb < nb; bb += 2) {
-        // this lane's ldmatrix block: bb + (lm >> 1); plane = blk / 8, chunk = blk % 8
-        const int blk_l = bb + (lm >> 1);
-        uint32_t w[2][4];
+      for (int pl = mem; pl < nplanes; pl += Q) {
+        expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
+        __syncwarp();
+        plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&empty[gi * D + d]);
+    }
+    // ------------------- member partials, added in member order -------------------
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
-          ldmatrix_x4(w[m][0], w[m][1], w[m][2], w[m][3],
-                      sbase + box_off[m] + swz128(blk_l >> 3, 16, row_in_box[m], blk_l & 7));
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int blk = bb + half;
-          uint32_t b0, b1, b2, b3;
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                       : "r"(act_addr + blk * 64));
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-            e2m1x8_to_f16x8(w[m][2 * half], l0, l1, l2, l3);
-            e2m1x8_to_f16x8(w[m][2 * half + 1], h0, h1, h2, h3);
-            float dacc[4];
-            mma_f16_zero(dacc, l0, h0, l1, h1, b0, b1);
-            mma_f16(dacc, l2, h2, l3, h3, b2, b3);
-            const float2 s = tab2[(blk * 2 + m) * 8];
+        for (int v = 0; v < NV; ++v) my_red[((m * 2 + h) * NV + v) * 32 + lane] = acc[m][h][v];
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(Q * 32) : "memory");
+    if (mem == 0) {
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-              acc[m][0][v] = fmaf(dacc[v], s.x, acc[m][0][v]);
-              acc[m][1][v] = fmaf(dacc[2 + v], s.y, acc[m][1][v]);
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            float t = my_red[((m * 2 + h) * NV + v) * 32 + lane];
+            for (int o = 1; o < Q; ++o) t += red[(gi * Q + o) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
+            acc[m][h][v] = t;
+          }
+      // ------------------------------ epilogue ------------------------------
+      // gate/up m-tile m holds features tile*16 + m*8 + g; down m-tile m holds
+      // output rows tile*32 + m*16 + g (+8 for the hi half)
+      float ssq[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int tok = 2 * q + v;
+        ssq[v] = 0.f;
+        if (tok < ntok) {
+          const int p = p0 + tok;
+          if (MODE == MODE_GATEUP) {
+            const int t = a.sorted_rows[p] / a.top_k;
+            const float inv = ldexpf(1.0f, -a.act_exp[t]);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const float gv = acc[m][0][v] * inv, uv = acc[m][1][v] * inv;
+              const float hv = gv / (1.0f + expf(-gv)) * uv;
+              a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = f32_to_bf16_bits(hv);
+            }
+          } else {
+            const int r = a.sorted_rows[p];
+            const float inv = ldexpf(1.0f, -a.act_exp[p]);
+            float* yr = a.y_out + (size_t)r * a.latent + tile * kRows;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const float y0 = acc[m][0][v] * inv, y1 = acc[m][1][v] * inv;
+              yr[m * 16 + g] = y0;
+              yr[m * 16 + g + 8] = y1;
+              ssq[v] = fmaf(y0, y0, fmaf(y1, y1, ssq[v]));
             }
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[warp * D + d]);
-    }
-    // ------------------------------ epilogue ------------------------------
-    // gate/up m-tile m holds features tile*16 + m*8 + g; down m-tile m holds
-    // output rows tile*32 + m*16 + g (+8 for the hi half)
-    float ssq[NV];
+      if (MODE == MODE_DOWN && a.ssq_out) {
+        // sum of squares of the tile's 32 rows per token (fixed tree over g)
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int tok = 2 * q + v;
-      ssq[v] = 0.f;
-      if (tok < ntok) {
-        const int p = p0 + tok;
-        if (MODE == MODE_GATEUP) {
-          const int t = a.sorted_rows[p] / a.top_k;
-          const float inv = ldexpf(1.0f, -a.act_exp[t]);
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const float gv = acc[m][0][v] * inv, uv = acc[m][1][v] * inv;
-            const float hv = gv / (1.0f + expf(-gv)) * uv;
-            a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = f32_to_bf16_bits(hv);
-          }
-        } else {
-          const int r = a.sorted_rows[p];
-          const float inv = ldexpf(1.0f, -a.act_exp[p]);
-          float* yr = a.y_out + (size_t)r * a.latent + tile * kRows;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const float y0 = acc[m][0][v] * inv, y1 = acc[m][1][v] * inv;
-            yr[m * 16 + g] = y0;
-            yr[m * 16 + g + 8] = y1;
-            ssq[v] = fmaf(y0, y0, fmaf(y1, y1, ssq[v]));
-          }
+        for (int v = 0; v < NV; ++v) {
+          float sv = ssq[v];
+          sv += __shfl_xor_sync(0xffffffffu, sv, 4);
+          sv += __shfl_xor_sync(0xffffffffu, sv, 8);
+          sv += __shfl_xor_sync(0xffffffffu, sv, 16);
+          const int tok = 2 * q + v;
+          if (g == 0 && tok < ntok) a.ssq_out[(size_t)a.sorted_rows[p0 + tok] * (a.latent / kRows) + tile] = sv;
         }
       }
     }
-    if (MODE == MODE_DOWN && a.ssq_out) {
-      // sum of squares of the tile's 32 rows per token (fixed tree over g)
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        float sv = ssq[v];
-        sv += __shfl_xor_sync(0xffffffffu, sv, 4);
-        sv += __shfl_xor_sync(0xffffffffu, sv, 8);
-        sv += __shfl_xor_sync(0xffffffffu, sv, 16);
-        const int tok = 2 * q + v;
-        if (g == 0 && tok < ntok) a.ssq_out[(size_t)a.sorted_rows[p0 + tok] * (a.latent / kRows) + tile] = sv;
-      }
-    }
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(Q * 32) : "memory");
   }
 }
 
@@ -324,11 +371,13 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
 // ---------------------------------------------------------------------------
 int expert_max_group(int T) { return T <= 1 ? 1 : 8; }
 
-template <int MODE, int G, int W, int D>
+template <int MODE, int G, int NGRP, int Q, int D>
 static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   using Lay = Layout<G>;
-  auto kern = expert_kernel<MODE, G, W, D>;
-  constexpr int smem = W * D * Lay::kSlot + W * Lay::kTable + 2 * W * D * 8 + 1024;  // +1 KB alignment slack
+  auto kern = expert_kernel<MODE, G, NGRP, Q, D>;
+  constexpr int NV = (G == 1) ? 1 : 2;
+  constexpr int smem = NGRP * D * Lay::kSlot + NGRP * Q * (256 + 2 * 2 * NV * 32) * 4 + 2 * NGRP * D * 8 +
+                       1024;  // +1 KB alignment slack
   static_assert(smem <= 232448, "shared memory budget");
   static unsigned long long attr_done = 0;  // one bit per device, per template instance
   int dev = 0;
@@ -338,7 +387,7 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
       return LMOE_ECUDA;
     attr_done |= 1ull << (dev & 63);
   }
-  // K chunk: the whole K when K <= 1024, else 1024 (K is a multiple of 1024 then)
+  // K chunk: the whole K when K <= kKC, else kKC (K is a multiple of kKC then)
   a.kc = a.K <= kKC ? a.K : kKC;
   const int rows_per_expert = (MODE == MODE_GATEUP) ? 2 * a.inter : a.latent;
   const uint64_t rows_total = (uint64_t)a.n_experts * rows_per_expert;
@@ -362,7 +411,7 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(32 * (W + 1));
+  cfg.blockDim = dim3(32 * (NGRP * Q + 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -374,13 +423,13 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
 }
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 5, 2>(a, s, num_sms);
-  return launch_one<MODE_GATEUP, 8, 5, 1>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 1, 8, 5>(a, s, num_sms);
+  return launch_one<MODE_GATEUP, 8, 1, 8, 3>(a, s, num_sms);
 }
 
 int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_DOWN, 1, 5, 2>(a, s, num_sms);
-  return launch_one<MODE_DOWN, 8, 5, 1>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_DOWN, 1, 1, 8, 5>(a, s, num_sms);
+  return launch_one<MODE_DOWN, 8, 1, 8, 3>(a, s, num_sms);
 }
 
 }  // namespace lmoe

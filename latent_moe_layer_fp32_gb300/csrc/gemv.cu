@@ -8,11 +8,11 @@
 //
 // out[t][n] = bf16_rne(sum_k act[t][k] * W[n][k]).  At small T this is a
 // weight stream.  Item = 16 weight rows x all of K for a group of up to 8*NT
-// tokens; the W consumer warps of a CTA share an item (chunk c of 256 K
+// tokens; the W consumer warps of a CTA share an item (chunk c of 512 K
 // elements goes to warp c % W) and add their fp32 partials in warp order at
 // the end.  Per chunk the producer issues one TMA tensor copy of the weights
-// (a 3-D view {64 elements, rows, K/64} with 128-byte swizzle: 16 rows x 256
-// elements, 8 KB) and one of the token rows (tokens beyond T read as zero);
+// (a 3-D view {64 elements, rows, K/64} with 128-byte swizzle: 16 rows x 512
+// elements, 16 KB) and one of the token rows (tokens beyond T read as zero);
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) takes both operands by
 // ldmatrix from the swizzled boxes.
 #include "common.cuh"
@@ -21,19 +21,20 @@
 
 namespace lmoe {
 
-constexpr int kGemvKC = 256;  // K elements per chunk (4 planes of 64)
 
-template <int NT>
+// KC: K elements per chunk (KC/64 planes of 64); 512 gives 16 KB weight boxes
+template <int NT, int KC>
 struct GemvLayout {
-  static constexpr int kW = 16 * kGemvKC * 2;       // 8 KB
-  static constexpr int kA = 8 * NT * kGemvKC * 2;   // 4 KB per n-tile
+  static constexpr int kW = 16 * KC * 2;       // 16 KB at KC = 512
+  static constexpr int kA = 8 * NT * KC * 2;   // 8 KB per n-tile at KC = 512
   static constexpr int kSlot = (kW + kA + 1023) / 1024 * 1024;
 };
 
-template <int NT, int W, int D>
+template <int NT, int KC, int W, int D>
 __global__ void __launch_bounds__(32 * (W + 1), 1)
     gemv_bf16_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x) {
-  using Lay = GemvLayout<NT>;
+  using Lay = GemvLayout<NT, KC>;
+  constexpr int kGemvKC = KC;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + W * D * Lay::kSlot);  // [W][NT][4][32]
@@ -54,11 +55,20 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-
   const int it0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
+  // The weights depend on nothing earlier in the stream: start pulling this
+  // CTA's rows into L2 before waiting on the preceding kernel.
+  if (warp == W && lane == 0) {
+    int last_mt = -1;
+    for (int it = it0; it < it1; ++it) {
+      const int mt = it % mtiles;
+      if (mt != last_mt) prefetch_l2_range(a.w + (size_t)mt * 16 * K, (size_t)16 * K * 2);
+      last_mt = mt;
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == W) {
     if (lane != 0) return;
@@ -85,8 +95,8 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
         uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
         uint64_t* bar = &full[w * D + d];
         mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // out-of-range token rows are zero-filled, bytes still count
-        tma_load_3d(slot, &tm_w, 0, mt * 16, c * 4, bar, pol);
-        tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * 4, bar, pol_x);
+        tma_load_3d(slot, &tm_w, 0, mt * 16, c * (kGemvKC / 64), bar, pol);
+        tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * (kGemvKC / 64), bar, pol_x);
       }
     }
 #pragma unroll
@@ -171,10 +181,11 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
   }
 }
 
-template <int NT, int W, int D>
+template <int NT, int KC, int W, int D>
 static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
-  using Lay = GemvLayout<NT>;
-  auto kern = gemv_bf16_kernel<NT, W, D>;
+  using Lay = GemvLayout<NT, KC>;
+  constexpr int kGemvKC = KC;
+  auto kern = gemv_bf16_kernel<NT, KC, W, D>;
   constexpr int smem = W * D * Lay::kSlot + W * NT * 4 * 32 * 4 + 2 * W * D * 8 + 1024;
   static_assert(smem <= 232448, "shared memory budget");
   static unsigned long long attr_done = 0;
@@ -215,9 +226,14 @@ static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
 }
 
 int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms) {
-  if (a.T <= 8) return launch_gemv<1, 4, 4>(a, s, num_sms);
-  if (a.T <= 16) return launch_gemv<2, 4, 3>(a, s, num_sms);
-  return launch_gemv<4, 4, 2>(a, s, num_sms);
+  if (a.K % 512 == 0) {
+    if (a.T <= 8) return launch_gemv<1, 512, 4, 2>(a, s, num_sms);
+    if (a.T <= 16) return launch_gemv<2, 512, 3, 2>(a, s, num_sms);
+    return launch_gemv<4, 512, 2, 2>(a, s, num_sms);
+  }
+  if (a.T <= 8) return launch_gemv<1, 256, 4, 4>(a, s, num_sms);
+  if (a.T <= 16) return launch_gemv<2, 256, 4, 3>(a, s, num_sms);
+  return launch_gemv<4, 256, 4, 2>(a, s, num_sms);
 }
 
 }  // namespace lmoe

@@ -74,6 +74,6 @@ def test_bad_dims_rejected(lm, field, value):
 
 
 def test_unsupported_width(lm):
-    # K is streamed in 1024-element chunks above 1024, and in 128-byte planes
-    for h, l, i in [(8192, 1280, 4096), (8192, 4096, 3072 + 128), (8192 + 128, 4096, 4096)]:
+    # K is streamed in 2048-element chunks above 2048, and in 128-byte planes
+    for h, l, i in [(8192, 2560, 4096), (8192, 4096, 3328), (8192 + 128, 4096, 4096)]:
         assert lm.lmoe_workspace_bytes(lm.dims_of(1, h, l, i, 256, 8, 1e-6)) == 0

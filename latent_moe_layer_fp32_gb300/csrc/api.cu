@@ -71,7 +71,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, groups, part, x16, xexp, h, h16, hexp, ssq;
+  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq;
   int nsplit;
 };
 
@@ -86,8 +86,14 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
     o = al(o + bytes);
     return at;
   };
-  w->pub.status = take(64);
-  w->n_groups = w->pub.status + 16;
+  // zeroed at the start of every call: status word, counters, row max words
+  w->pub.status = 0;
+  w->n_groups = 16;
+  w->route_count = 24;
+  w->xmax = 64;
+  w->hmax = 64 + 4 * T;
+  w->zero_bytes = 64 + 4 * T + 4 * R;
+  take(w->zero_bytes);
   w->pub.topk_idx = take(4 * R);
   w->pub.topk_w = take(4 * R);
   w->pub.expert_offsets = take(4 * (E + 1));
@@ -96,11 +102,7 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->groups = take(16 * (R + E + 1));
   w->part = take(4 * (size_t)16 * T * E);
   w->pub.x_lat = take(2 * T * L);
-  w->x16 = take(2 * T * L);
-  w->xexp = take(4 * T);
   w->h = take(2 * R * I);
-  w->h16 = take(2 * R * I);
-  w->hexp = take(4 * R);
   w->pub.y = take(4 * R * L);
   w->ssq = take(4 * R * (L / 32));
   w->pub.z = take(2 * T * L);
@@ -150,7 +152,7 @@ int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayou
   if (need_ws) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
     if (ws_bytes < w->pub.total) return LMOE_EWORKSPACE;
-    if (cudaMemsetAsync(at<char>(ws, w->pub.status), 0, 64, s) != cudaSuccess) return LMOE_ECUDA;
+    if (cudaMemsetAsync(ws, 0, w->zero_bytes, s) != cudaSuccess) return LMOE_ECUDA;
   }
   return LMOE_OK;
 }
@@ -161,6 +163,13 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   const int T = d->T, E = d->n_experts, k = d->top_k, H = d->hidden;
   Status* st = at<Status>(ws, w.pub.status);
   float* part = at<float>(ws, w.part);
+  if (T <= 16) {
+    // one launch: router partials, then the last CTA finishes the routing
+    LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, route_small_kernel, x, router_w, router_bias,
+           part, T, H, E, k, H / w.nsplit, expert_max_group(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
+           at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st);
+    return LMOE_OK;
+  }
   LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T, H,
          E, H / w.nsplit);
   LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
@@ -171,21 +180,20 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
 }
 
 int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
-             Status* st, cudaStream_t s) {
-  GemvArgs g{pooler_w, x, x_lat, d->latent, d->hidden, d->T, st};
+             uint32_t* xmax, Status* st, cudaStream_t s) {
+  GemvArgs g{pooler_w, x, x_lat, xmax, d->latent, d->hidden, d->T, st};
   pre_launch(s);
   CHECK(launch_gemv_bf16(g, s, di.sms));
   ++g_launches;
   return LMOE_OK;
 }
 
-// groups must already be in the workspace
+// groups must already be in the workspace; xmax must hold each token's max |x_lat|
 int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
                 const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                 const uint8_t* w2_s, float* y, void* ws, cudaStream_t s) {
-  const int T = d->T, k = d->top_k, R = T * k, L = d->latent, I = d->inter;
+  const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
-  LAUNCH(dim3(T), dim3(256), s, prep_act_kernel, x_lat, L, at<uint16_t>(ws, w.x16), at<int32_t>(ws, w.xexp));
   const int G = expert_max_group(T);
   ExpertArgs a{};
   a.groups = at<int4>(ws, w.groups);
@@ -198,21 +206,21 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.st = st;
   a.q = w13_q;
   a.s = w13_s;
-  a.act16 = at<uint16_t>(ws, w.x16);
-  a.act_exp = at<int32_t>(ws, w.xexp);
+  a.act = x_lat;
+  a.act_max = at<uint32_t>(ws, w.xmax);
   a.K = L;
   a.h_out = at<uint16_t>(ws, w.h);
+  a.h_max = at<uint32_t>(ws, w.hmax);
   pre_launch(s);
   CHECK(launch_gateup(a, T, G, s, di.sms));
   ++g_launches;
-  LAUNCH(dim3(R), dim3(256), s, prep_act_kernel, (const uint16_t*)at<uint16_t>(ws, w.h), I, at<uint16_t>(ws, w.h16),
-         at<int32_t>(ws, w.hexp));
   a.q = w2_q;
   a.s = w2_s;
-  a.act16 = at<uint16_t>(ws, w.h16);
-  a.act_exp = at<int32_t>(ws, w.hexp);
+  a.act = at<uint16_t>(ws, w.h);
+  a.act_max = at<uint32_t>(ws, w.hmax);
   a.K = I;
   a.h_out = nullptr;
+  a.h_max = nullptr;
   a.y_out = y;
   a.ssq_out = at<float>(ws, w.ssq);
   pre_launch(s);
@@ -231,9 +239,9 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
     LAUNCH(dim3((unsigned)((n + 7) / 8)), dim3(256), s, ssq_kernel, y, d->T * d->top_k, d->latent,
            at<float>(ws, w.ssq));
   }
-  LAUNCH(dim3(d->T, (d->latent + 511) / 512), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
+  LAUNCH(dim3(d->T, (d->latent + 255) / 256), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
          topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts, d->eps, zb, st);
-  GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st};
+  GemvArgs g{unpooler_w, zb, out, nullptr, d->hidden, d->latent, d->T, st};
   pre_launch(s);
   CHECK(launch_gemv_bf16(g, s, di.sms));
   ++g_launches;
@@ -284,7 +292,7 @@ int lmoe_pool(const lmoe_dims* d, const uint16_t* x, const uint16_t* pooler_w, u
   CHECK(prologue(d, ws, ws_bytes, &di, &w, s, ws != nullptr));
   if (!aligned16(x) || !aligned16(pooler_w) || !aligned16(x_lat) || !x || !pooler_w || !x_lat) return LMOE_EINVAL;
   Status* st = ws ? at<Status>(ws, w.pub.status) : nullptr;
-  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, st, s));
+  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, nullptr, st, s));
 }
 
 int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
@@ -300,6 +308,7 @@ int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t*
   const int R = d->T * d->top_k;
   LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
          expert_max_group(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
+  LAUNCH(dim3(d->T), dim3(256), s, row_max_kernel, x_lat, d->latent, at<uint32_t>(ws, w.xmax));
   return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s));
 }
 
@@ -336,7 +345,7 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   Status* st = at<Status>(ws, w.pub.status);
   CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets), srows,
                   at<int32_t>(ws, w.pub.row_pos), ws, s));
-  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
+  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, at<uint32_t>(ws, w.xmax), st, s));
   CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);

@@ -208,6 +208,16 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// Power of two e that puts a row's largest magnitude m in [2^14, 2^15): f16(x * 2^e)
+// then holds every bf16 value x of the row with |x * 2^e| >= 2^-17 exactly.
+__device__ __forceinline__ int act_exponent(uint32_t max_bits) {
+  const float m = __uint_as_float(max_bits);
+  if (!(m > 0.f) || !isfinite(m)) return 0;
+  int E;
+  frexpf(m, &E);
+  return min(127, max(-126, 15 - E));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -26,8 +26,9 @@
 // 32 K positions in a fixed permutation that the activation fragment follows;
 // the fresh block result is scaled by the block's E8M0 value (expanded once
 // per chunk into a per-warp fp32 table) and added to the fp32 accumulator.
-// Activations arrive as f16 scaled by a per-row power of two (exact; undone
-// in the epilogue).
+// Activations arrive as bf16 rows; each warp converts its plane's columns to
+// f16 times a per-row power of two (exact; undone in the epilogue), the power
+// coming from the row's max |value| that the producing kernel recorded.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.cuh"
@@ -39,6 +40,14 @@ enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 constexpr int kRows = 32;  // weight rows per item: two m16 tiles
 constexpr int kKC = 2048;  // K elements per chunk when K > 2048 (else the whole K): 16 KB code boxes
 
+// Header the producer writes into the first slot of every item.
+struct ItemMeta {
+  int p0, ntok, pad0, pad1;
+  int aexp[8];  // per token of the group: power of two mapping its activation row into f16 range
+  int rows[8];  // per token: sorted_rows[p0 + j] (the original route row id)
+};
+static_assert(sizeof(ItemMeta) <= 128, "item header");
+
 template <int G>
 struct Layout {
   static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (16 KB)
@@ -46,7 +55,8 @@ struct Layout {
   static constexpr int kScales = kRows * (kKC / 32);
   static constexpr int kActRow = kKC * 2 + 64;  // padded: conflict-free 16-byte loads
   static constexpr int kActs = G * kActRow;
-  static constexpr int kSlot = (kCodes + kScales + kActs + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
+  static constexpr int kMeta = 128;  // item header: p0, ntok, per-token exponent and row id
+  static constexpr int kSlot = (kCodes + kScales + kActs + kMeta + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
 };
 
 // Expand the E8M0 bytes of one 128-byte plane (8 blocks; scale region
@@ -137,13 +147,13 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
   using Lay = Layout<G>;
   constexpr int NW = NGRP * Q;
   constexpr int NV = (G == 1) ? 1 : 2;  // token columns per lane that can hold a valid token
-  constexpr int kRed = 2 * 2 * NV * 32;  // floats per member partial
+  constexpr int kRed = 2 * 2 * NV * 32;  // floats per member partial (two buffers, by item parity)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1 KB alignment for the swizzled boxes
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* tables = reinterpret_cast<float*>(smem + NGRP * D * Lay::kSlot);      // [NW][8*2*8*2]
-  float* red = tables + NW * 256;                                              // [NW][kRed]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + NW * kRed);
+  float* red = tables + NW * 256;                                              // [2][NW][kRed]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * NW * kRed);
   uint64_t* empty = full + NGRP * D;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -180,14 +190,49 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
 #pragma unroll
     for (int gi = 0; gi < NGRP; ++gi) seq[gi] = 0;
     bool ok = true;
+    // metadata of 32 items at a time, item (batch + lane) in lane `lane`
+    int m_e = 0, m_p0 = 0, m_ntok = 0, m_rows[G], m_exp[G];
+    int batch = -1;
     for (int base = 0; base < nloc && ok; base += NGRP) {
       const int ng = min(NGRP, nloc - base);
+      if (base / 32 != batch) {
+        batch = base / 32;
+        const int itl = batch * 32 + lane;
+        m_ntok = 0;
+        if (itl < nloc) {
+          const int4 gq = a.groups[(it0 + itl) / tiles];
+          m_e = gq.x;
+          m_p0 = gq.y;
+          m_ntok = gq.z;
+        }
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) {
+          m_rows[jj] = 0;
+          m_exp[jj] = 0;
+          if (jj < m_ntok) m_rows[jj] = a.sorted_rows[m_p0 + jj];
+        }
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+          if (jj < m_ntok) m_exp[jj] = act_exponent(a.act_max[(MODE == MODE_GATEUP) ? m_rows[jj] / a.top_k : m_p0 + jj]);
+      }
       for (int c = 0; c < nch && ok; ++c) {
         for (int gi = 0; gi < ng; ++gi) {
           const int it = it0 + base + gi;
-          const int grp = it / tiles, tile = it % tiles;
-          const int4 gq = a.groups[grp];
-          const int e = gq.x, p0 = gq.y, ntok = gq.z;
+          const int tile = it % tiles;
+          const int src = (base + gi) & 31;
+          const int e = __shfl_sync(0xffffffffu, m_e, src);
+          const int p0 = __shfl_sync(0xffffffffu, m_p0, src);
+          const int ntok = __shfl_sync(0xffffffffu, m_ntok, src);
+          int my_row = 0, my_exp = 0;  // token `lane` of this item
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) {
+            const int rv = __shfl_sync(0xffffffffu, m_rows[jj], src);
+            const int ev = __shfl_sync(0xffffffffu, m_exp[jj], src);
+            if (lane == jj) {
+              my_row = rv;
+              my_exp = ev;
+            }
+          }
           const int d = seq[gi] % D;
           const uint32_t par = ((seq[gi] / D) & 1) ^ 1;
           ++seq[gi];
@@ -208,6 +253,18 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
             rowA = e * rows_per_expert + tile * kRows;
             rowB = rowA + 16;
           }
+          if (c == 0) {
+            ItemMeta* meta = reinterpret_cast<ItemMeta*>(slot + Lay::kCodes + Lay::kScales + Lay::kActs);
+            if (lane == 0) {
+              meta->p0 = p0;
+              meta->ntok = ntok;
+            }
+            if (lane < G) {
+              meta->aexp[lane] = my_exp;
+              meta->rows[lane] = my_row;
+            }
+          }
+          __syncwarp();
           if (lane == 0) mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb + (uint32_t)ntok * kc * 2);
           __syncwarp();
           if (lane == 0) {
@@ -220,10 +277,12 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
               tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
             else  // one chunk: the 16 rows' scales are contiguous
               bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
-          } else if (lane >= 8 && lane < 8 + ntok) {
-            const int j = lane - 8;
-            const int arow = (MODE == MODE_GATEUP) ? a.sorted_rows[p0 + j] / a.top_k : p0 + j;
-            bulk_g2s(slot + Lay::kCodes + Lay::kScales + j * kact_row, a.act16 + (size_t)arow * K + c * kc, kc * 2,
+          }
+          // activation rows: token j's copy from lane j (its row id is in my_row)
+          if (lane < ntok) {
+            const int j = lane;
+            const int arow = (MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + j;
+            bulk_g2s(slot + Lay::kCodes + Lay::kScales + j * kact_row, a.act + (size_t)arow * K + c * kc, kc * 2,
                      bar);
           }
           __syncwarp();
@@ -246,7 +305,7 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
   // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
   const int lm = lane >> 3, rr = lane & 7;
   float* table = tables + warp * 256;
-  float* my_red = red + warp * kRed;
+  int item_count = 0;
   // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
   uint32_t box_off[2];
   int row_in_box[2];
@@ -268,9 +327,9 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
   bool alive = true;
   for (int j = gi; j < nloc; j += NGRP) {
     const int it = it0 + j;
-    const int grp = it / tiles, tile = it % tiles;
-    const int4 gq = a.groups[grp];
-    const int p0 = gq.y, ntok = gq.z;
+    const int tile = it % tiles;
+    int p0 = 0, ntok = 0;
+    int aexp[G], arow_id[G];  // from the item header (first chunk's slot)
     float acc[2][2][NV];  // [mtile][lo/hi row][token column]
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -287,10 +346,38 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
         break;
       }
       const uint8_t* slot = smem + (gi * D + d) * Lay::kSlot;
+      if (c == 0) {
+        const ItemMeta* meta = reinterpret_cast<const ItemMeta*>(slot + Lay::kCodes + Lay::kScales + Lay::kActs);
+        p0 = meta->p0;
+        ntok = meta->ntok;
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) {
+          aexp[jj] = meta->aexp[jj];
+          arow_id[jj] = meta->rows[jj];
+        }
+      }
       const uint32_t sbase = smem_u32(slot);
       const uint32_t act_addr = smem_u32(slot + Lay::kCodes + Lay::kScales) + (g < G ? g : 0) * kact_row + q * 16;
       for (int pl = mem; pl < nplanes; pl += Q) {
         expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
+        // this plane's activation columns (256 per token): bf16 -> f16 * 2^e in place
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) {
+          if (jj < ntok) {
+            uint4* pa = reinterpret_cast<uint4*>(const_cast<uint8_t*>(slot) + Lay::kCodes + Lay::kScales +
+                                                 jj * kact_row + pl * 512) + lane;
+            const uint4 v = *pa;
+            const float sc = ldexpf(1.0f, aexp[jj]);
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(in[u] & 0xffffu) * sc, bf16_bits_to_f32(in[u] >> 16) * sc);
+              o[u] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *pa = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
         __syncwarp();
         plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
         __syncwarp();
@@ -298,12 +385,18 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
       if (lane == 0) mbar_arrive(&empty[gi * D + d]);
     }
     // ------------------- member partials, added in member order -------------------
+    // Two buffers by item parity: a member may write item i+1's partials while
+    // member 0 still reads item i's, so one barrier per item suffices (a member
+    // reaches item i+2's write only after the barrier of item i+1, which member
+    // 0 passes after finishing item i).
+    float* rbuf = red + (item_count & 1) * NW * kRed;
+    ++item_count;
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int v = 0; v < NV; ++v) my_red[((m * 2 + h) * NV + v) * 32 + lane] = acc[m][h][v];
+        for (int v = 0; v < NV; ++v) rbuf[warp * kRed + ((m * 2 + h) * NV + v) * 32 + lane] = acc[m][h][v];
     asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(Q * 32) : "memory");
     if (mem == 0) {
 #pragma unroll
@@ -312,8 +405,8 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            float t = my_red[((m * 2 + h) * NV + v) * 32 + lane];
-            for (int o = 1; o < Q; ++o) t += red[(gi * Q + o) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
+            float t = rbuf[(gi * Q) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
+            for (int o = 1; o < Q; ++o) t += rbuf[(gi * Q + o) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
             acc[m][h][v] = t;
           }
       // ------------------------------ epilogue ------------------------------
@@ -324,20 +417,26 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
       for (int v = 0; v < NV; ++v) {
         const int tok = 2 * q + v;
         ssq[v] = 0.f;
+        int e_tok = 0, r_tok = 0;
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+          if (jj == tok) {
+            e_tok = aexp[jj];
+            r_tok = arow_id[jj];
+          }
         if (tok < ntok) {
           const int p = p0 + tok;
+          const float inv = ldexpf(1.0f, -e_tok);
           if (MODE == MODE_GATEUP) {
-            const int t = a.sorted_rows[p] / a.top_k;
-            const float inv = ldexpf(1.0f, -a.act_exp[t]);
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               const float gv = acc[m][0][v] * inv, uv = acc[m][1][v] * inv;
-              const float hv = gv / (1.0f + expf(-gv)) * uv;
-              a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = f32_to_bf16_bits(hv);
+              const uint16_t hb = f32_to_bf16_bits(gv / (1.0f + expf(-gv)) * uv);
+              a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = hb;
+              ssq[v] = fmaxf(ssq[v], fabsf(bf16_bits_to_f32(hb)));  // gate/up: running max |h|
             }
           } else {
-            const int r = a.sorted_rows[p];
-            const float inv = ldexpf(1.0f, -a.act_exp[p]);
+            const int r = r_tok;
             float* yr = a.y_out + (size_t)r * a.latent + tile * kRows;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
@@ -349,6 +448,18 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
           }
         }
       }
+      if (MODE == MODE_GATEUP) {
+        // row max of |h| over this tile's 16 features, folded into the row's max word
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          float mv = ssq[v];
+          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 4));
+          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 8));
+          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 16));
+          const int tok = 2 * q + v;
+          if (g == 0 && tok < ntok) atomicMax(&a.h_max[p0 + tok], __float_as_uint(mv));
+        }
+      }
       if (MODE == MODE_DOWN && a.ssq_out) {
         // sum of squares of the tile's 32 rows per token (fixed tree over g)
 #pragma unroll
@@ -358,11 +469,14 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
           sv += __shfl_xor_sync(0xffffffffu, sv, 8);
           sv += __shfl_xor_sync(0xffffffffu, sv, 16);
           const int tok = 2 * q + v;
-          if (g == 0 && tok < ntok) a.ssq_out[(size_t)a.sorted_rows[p0 + tok] * (a.latent / kRows) + tile] = sv;
+          int r_tok = 0;
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj)
+            if (jj == tok) r_tok = arow_id[jj];
+          if (g == 0 && tok < ntok) a.ssq_out[(size_t)r_tok * (a.latent / kRows) + tile] = sv;
         }
       }
     }
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(Q * 32) : "memory");
   }
 }
 
@@ -376,7 +490,7 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   using Lay = Layout<G>;
   auto kern = expert_kernel<MODE, G, NGRP, Q, D>;
   constexpr int NV = (G == 1) ? 1 : 2;
-  constexpr int smem = NGRP * D * Lay::kSlot + NGRP * Q * (256 + 2 * 2 * NV * 32) * 4 + 2 * NGRP * D * 8 +
+  constexpr int smem = NGRP * D * Lay::kSlot + NGRP * Q * (256 + 2 * 2 * 2 * NV * 32) * 4 + 2 * NGRP * D * 8 +
                        1024;  // +1 KB alignment slack
   static_assert(smem <= 232448, "shared memory budget");
   static unsigned long long attr_done = 0;  // one bit per device, per template instance

@@ -169,10 +169,19 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int tok = n * 8 + 2 * q + i;
+          const uint16_t b_lo = f32_to_bf16_bits(v[i]), b_hi = f32_to_bf16_bits(v[2 + i]);
           if (tok < ntok) {
             uint16_t* o = a.out + (size_t)(t0 + tok) * a.N + mt * 16;
-            o[g] = f32_to_bf16_bits(v[i]);
-            o[g + 8] = f32_to_bf16_bits(v[2 + i]);
+            o[g] = b_lo;
+            o[g + 8] = b_hi;
+          }
+          if (a.col_max) {
+            // max |out| of this token over the tile's 16 rows, folded into the token's max word
+            float mv = fmaxf(fabsf(bf16_bits_to_f32(b_lo)), fabsf(bf16_bits_to_f32(b_hi)));
+            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 4));
+            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 8));
+            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 16));
+            if (g == 0 && tok < ntok) atomicMax(&a.col_max[t0 + tok], __float_as_uint(mv));
           }
         }
       }

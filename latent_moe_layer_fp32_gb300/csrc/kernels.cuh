@@ -11,6 +11,10 @@ __global__ void router_partial_kernel(const uint16_t* x, const float* wr, float*
                                       int split_len);
 __global__ void topk_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,
                             int32_t* topk_idx, float* topk_w);
+__global__ void route_small_kernel(const uint16_t* x, const float* wr, const float* bias, float* part, int T, int H,
+                                   int E, int k, int split_len, int G, int32_t* topk_idx, float* topk_w,
+                                   int32_t* offsets, int32_t* sorted_rows, int32_t* row_pos, int4* groups,
+                                   int32_t* n_groups, int32_t* ticket, Status* st);
 __global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32_t* offsets, int32_t* sorted_rows,
                              int32_t* row_pos, int4* groups, int32_t* n_groups, Status* st);
 
@@ -20,8 +24,8 @@ __global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32
 struct ExpertArgs {
   const uint8_t* q;         // codes [E][rows_per_expert][K/2]
   const uint8_t* s;         // scales [E][rows_per_expert][K/32]
-  const uint16_t* act16;    // f16 activations, row-major [*][K]
-  const int32_t* act_exp;   // per activation row: power-of-two exponent applied
+  const uint16_t* act;      // bf16 activations, row-major [*][K] (x_lat by token, or h by sorted position)
+  const uint32_t* act_max;  // per activation row: max |value| as fp32 bits
   const int4* groups;       // group list
   const int32_t* n_groups;  // device count of groups
   const int32_t* sorted_rows;
@@ -32,6 +36,7 @@ struct ExpertArgs {
   int top_k;
   int n_experts;
   uint16_t* h_out;          // gate/up: bf16 [R_sorted][I]
+  uint32_t* h_max;          // gate/up: per sorted row, atomic max of |h| as fp32 bits (zeroed by the caller)
   float* y_out;             // down: fp32 [R][L] by original row id
   float* ssq_out;           // down: fp32 [R][L/32] sum of y^2 per 32-row tile (may be null)
   Status* st;
@@ -46,13 +51,14 @@ struct GemvArgs {
   const uint16_t* w;    // bf16 [N][K]
   const uint16_t* act;  // bf16 [T][K]
   uint16_t* out;        // bf16 [T][N]
+  uint32_t* col_max;    // optional: per token, atomic max of |out| as fp32 bits (zeroed by the caller)
   int N, K, T;
   Status* st;
 };
 int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 
 // ---- misc.cu --------------------------------------------------------------
-__global__ void prep_act_kernel(const uint16_t* in, int K, uint16_t* out16, int32_t* exps);
+__global__ void row_max_kernel(const uint16_t* in, int K, uint32_t* row_max);
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
                                            int4* groups, int32_t* n_groups, Status* st);
 __global__ void ssq_kernel(const float* y, int R, int L, float* ssq);

@@ -18,12 +18,10 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
   return m;
 }
 
-// One CTA (256 threads) per activation row: out16 = f16(x * 2^e), where the
-// power of two e puts the row's largest magnitude in [2^14, 2^15).  Values
-// with |x * 2^e| >= 2^-17 convert exactly; the expert epilogue multiplies the
-// fp32 result by 2^-e, so the products equal the bf16 ones.
-__global__ void __launch_bounds__(256) prep_act_kernel(const uint16_t* __restrict__ in, int K,
-                                                       uint16_t* __restrict__ out16, int32_t* __restrict__ exps) {
+// One CTA (256 threads) per row: row_max[row] = max |x| over the bf16 row, as
+// fp32 bits (the expert kernels derive each row's f16 scaling from it).
+__global__ void __launch_bounds__(256) row_max_kernel(const uint16_t* __restrict__ in, int K,
+                                                      uint32_t* __restrict__ row_max) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[8];
@@ -40,26 +38,7 @@ __global__ void __launch_bounds__(256) prep_act_kernel(const uint16_t* __restric
     }
   }
   m = block_max_256(m, red);
-  int e = 0;
-  if (m > 0.f && isfinite(m)) {
-    int E;
-    frexpf(m, &E);
-    e = min(127, max(-126, 15 - E));
-  }
-  const float scale = ldexpf(1.0f, e);
-  uint4* dst = reinterpret_cast<uint4*>(out16 + row * K);
-  for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __half2 h = __floats2half2_rn(bf16_bits_to_f32(w[j] & 0xffffu) * scale, bf16_bits_to_f32(w[j] >> 16) * scale);
-      o[j] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (threadIdx.x == 0) exps[row] = e;
+  if (threadIdx.x == 0) row_max[row] = __float_as_uint(m);
 }
 
 // Group list (groups of <= G rows per expert) from a caller-supplied table,
@@ -113,10 +92,11 @@ __global__ void __launch_bounds__(256) ssq_kernel(const float* __restrict__ y, i
 
 // post_expert_norm on each route row, then the fp32 weighted sum in route
 // order ("Muse Spark Open on Gaudi 2", "The latent MoE: A' with a per-expert
-// norm").  Grid (T, ceil(L/512)), 256 threads, 2 columns per thread:
+// norm").  Grid (T, ceil(L/256)), 256 threads, 1 column per thread:
 //   ss_j  = sum over the row's 32-column tiles of ssq (fixed order)
 //   rinv  = 1 / sqrt(ss_j / L + eps)
 //   z[l]  = sum_j w[t][j] * ((y * rinv) * g[e_j][l]),  zb = bf16(z)
+// (each CTA recomputes the k factors rinv for its token: k x L/32 partials)
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ssq,
                                                       const int32_t* __restrict__ topk_idx,
                                                       const float* __restrict__ topk_w,
@@ -146,10 +126,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
   }
   __syncthreads();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int l = blockIdx.y * 512 + h * 256 + tid;
-    if (l >= L) break;
+  {
+    const int l = blockIdx.y * 256 + tid;
+    if (l >= L) return;
     float z = 0.f;
     for (int j = 0; j < k; ++j) {
       const float yv = y[((size_t)t * k + j) * L + l];

@@ -17,10 +17,8 @@ namespace lmoe {
 // ---------------------------------------------------------------------------
 constexpr int kRouterTok = 8;
 
-__global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __restrict__ x,
-                                                             const float* __restrict__ wr,
-                                                             float* __restrict__ part, int T, int H, int E,
-                                                             int split_len) {
+__device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                    float* __restrict__ part, int T, int H, int E, int split_len) {
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -71,6 +69,13 @@ __global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __r
   }
 }
 
+__global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __restrict__ x,
+                                                             const float* __restrict__ wr,
+                                                             float* __restrict__ part, int T, int H, int E,
+                                                             int split_len) {
+  router_partial_body(x, wr, part, T, H, E, split_len);
+}
+
 // ---------------------------------------------------------------------------
 // top-k + softmax-renormalised weights, one warp per token.
 // logit[e] = sum over splits in order (+ bias); candidates e = lane + 32*i.
@@ -80,34 +85,17 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int nsplit,
-                                                   const float* __restrict__ bias, int T, int E, int k,
-                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  pdl_wait();
-  pdl_trigger();
-  // one CTA per token: thread e sums its nsplit partials (independent loads,
-  // summed in split order), then warp 0 selects the top k
-  __shared__ float s_lg[256];
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  if (tid < E) {
-    float v[16];
-#pragma unroll
-    for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? part[((size_t)sp * T + t) * E + tid] : 0.f;
-    float acc = v[0];
-#pragma unroll
-    for (int sp = 1; sp < 16; ++sp)
-      if (sp < nsplit) acc += v[sp];
-    if (bias) acc = acc + bias[tid];
-    s_lg[tid] = acc;
-  }
-  __syncthreads();
-  if (tid >= 32) return;
+// Top-k of one token by one warp, logits lg_s[0..E) in shared memory.
+// Writes topk_idx[k], topk_w[k] for the token (softmax over all E,
+// renormalised over the k picks; ties to the lower expert index).
+__device__ __forceinline__ void topk_one_token(const float* lg_s, int E, int k, int32_t* topk_idx, float* topk_w,
+                                               int lane) {
   float lg[8];
   bool taken[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    lg[i] = e < E ? s_lg[e] : -INFINITY;
+    lg[i] = e < E ? lg_s[e] : -INFINITY;
     taken[i] = (e >= E);
   }
   float mx = -INFINITY;
@@ -159,9 +147,36 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
       e = sel_e[j];
     }
   if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = e;
-    topk_w[(size_t)t * k + lane] = p / den;
+    topk_idx[lane] = e;
+    topk_w[lane] = p / den;
   }
+}
+
+// logit[e] of token t = sum over splits in split order (+ bias)
+__device__ __forceinline__ float token_logit(const float* part, int nsplit, const float* bias, int T, int E, int t,
+                                             int e) {
+  float v[16];
+#pragma unroll
+  for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? __ldcg(part + ((size_t)sp * T + t) * E + e) : 0.f;
+  float acc = v[0];
+#pragma unroll
+  for (int sp = 1; sp < 16; ++sp)
+    if (sp < nsplit) acc += v[sp];
+  if (bias) acc = acc + bias[e];
+  return acc;
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int nsplit,
+                                                   const float* __restrict__ bias, int T, int E, int k,
+                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_wait();
+  pdl_trigger();
+  // one CTA per token: thread e sums its partials, warp 0 selects the top k
+  __shared__ float s_lg[256];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  if (tid < E) s_lg[tid] = token_logit(part, nsplit, bias, T, E, t, tid);
+  __syncthreads();
+  if (tid < 32) topk_one_token(s_lg, E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, tid);
 }
 
 // ---------------------------------------------------------------------------
@@ -171,29 +186,31 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 // ---------------------------------------------------------------------------
 constexpr int kTableThreads = 1024;
 
-__global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __restrict__ topk_idx, int R, int E,
-                                                              int G, int32_t* __restrict__ offsets,
-                                                              int32_t* __restrict__ sorted_rows,
-                                                              int32_t* __restrict__ row_pos,
-                                                              int4* __restrict__ groups,
-                                                              int32_t* __restrict__ n_groups, Status* st) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ int s_count[256];
-  __shared__ int s_fill[256];
-  __shared__ int s_off[257];
-  __shared__ int s_goff[256];
-  __shared__ int s_wcnt[32][256];
+// Shared state of the table build for a CTA of NT threads.
+template <int NT>
+struct TableSmem {
+  int count[256], fill[256], off[257], goff[256];
+  int wcnt[NT / 32][256];
+};
+
+// Stable counting sort of the R row ids by expert (ascending row id within an
+// expert) plus the group list, by one CTA of NT threads; idx may be global
+// memory written by this CTA before a __syncthreads.
+template <int NT>
+__device__ void build_table(const int32_t* idx, int R, int E, int G, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ sorted_rows, int32_t* __restrict__ row_pos, int4* __restrict__ groups,
+                            int32_t* __restrict__ n_groups, Status* st, TableSmem<NT>& sm) {
+  constexpr int NW = NT / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int e = tid; e < 256; e += kTableThreads) s_count[e] = 0;
+  for (int e = tid; e < 256; e += NT) sm.count[e] = 0;
   __syncthreads();
-  for (int r = tid; r < R; r += kTableThreads) {
-    int e = topk_idx[r];
+  for (int r = tid; r < R; r += NT) {
+    int e = idx[r];
     if (e < 0 || e >= E) {
       set_error(st, LMOE_EDEVICE_CHECK, 100);
       e = 0;
     }
-    atomicAdd(&s_count[e], 1);
+    atomicAdd(&sm.count[e], 1);
   }
   __syncthreads();
   // exclusive scans (warp 0, 8 experts per lane, lane order = expert order):
@@ -203,7 +220,7 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      cnt[i] = e < E ? s_count[e] : 0;
+      cnt[i] = e < E ? sm.count[e] : 0;
       gcnt[i] = (cnt[i] + G - 1) / G;
       rs += cnt[i];
       gs += gcnt[i];
@@ -222,63 +239,117 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
       if (e < E) {
-        s_off[e] = racc;
-        s_goff[e] = gacc;
+        sm.off[e] = racc;
+        sm.goff[e] = gacc;
       }
       racc += cnt[i];
       gacc += gcnt[i];
     }
     if (lane == 31) {
-      s_off[E] = racc;
+      sm.off[E] = racc;
       *n_groups = gacc;
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kTableThreads) {
-    const int n = s_count[e], a0 = s_off[e];
-    int gi = s_goff[e];
+  for (int e = tid; e < E; e += NT) {
+    const int n = sm.count[e], a0 = sm.off[e];
+    int gi = sm.goff[e];
     for (int g0 = 0; g0 < n; g0 += G) groups[gi++] = make_int4(e, a0 + g0, min(G, n - g0), 0);
   }
-  for (int e = tid; e < 256; e += kTableThreads) s_fill[e] = 0;
+  for (int e = tid; e < 256; e += NT) sm.fill[e] = 0;
   __syncthreads();
-  for (int e = tid; e <= E; e += kTableThreads) offsets[e] = s_off[e];
+  for (int e = tid; e <= E; e += NT) offsets[e] = sm.off[e];
 
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < R; base += kTableThreads) {
-    for (int i = tid; i < 32 * 256; i += kTableThreads) (&s_wcnt[0][0])[i] = 0;
+  for (int base = 0; base < R; base += NT) {
+    for (int i = tid; i < NW * 256; i += NT) (&sm.wcnt[0][0])[i] = 0;
     __syncthreads();
     const int r = base + tid;
     int e = -1, rank = 0;
     if (r < R) {
-      e = topk_idx[r];
+      e = idx[r];
       if (e < 0 || e >= E) e = 0;
     }
     const unsigned same = __match_any_sync(0xffffffffu, e);
     if (r < R) {
       rank = __popc(same & lt_mask);
-      if (rank == 0) s_wcnt[warp][e] = __popc(same);
+      if (rank == 0) sm.wcnt[warp][e] = __popc(same);
     }
     __syncthreads();
     // exclusive prefix over warps, per expert (fixed order)
     if (tid < E) {
       int acc = 0;
-      for (int w = 0; w < 32; ++w) {
-        const int c = s_wcnt[w][tid];
-        s_wcnt[w][tid] = acc;
+      for (int w = 0; w < NW; ++w) {
+        const int c = sm.wcnt[w][tid];
+        sm.wcnt[w][tid] = acc;
         acc += c;
       }
-      s_count[tid] = acc;  // rows of expert tid in this chunk
+      sm.count[tid] = acc;  // rows of expert tid in this chunk
     }
     __syncthreads();
     if (r < R) {
-      const int pos = s_off[e] + s_fill[e] + s_wcnt[warp][e] + rank;
+      const int pos = sm.off[e] + sm.fill[e] + sm.wcnt[warp][e] + rank;
       sorted_rows[pos] = r;
       row_pos[r] = pos;
     }
     __syncthreads();
-    if (tid < E) s_fill[tid] += s_count[tid];
+    if (tid < E) sm.fill[tid] += sm.count[tid];
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __restrict__ topk_idx, int R, int E,
+                                                              int G, int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ sorted_rows,
+                                                              int32_t* __restrict__ row_pos,
+                                                              int4* __restrict__ groups,
+                                                              int32_t* __restrict__ n_groups, Status* st) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ TableSmem<kTableThreads> sm;
+  build_table<kTableThreads>(topk_idx, R, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm);
+}
+
+// ---------------------------------------------------------------------------
+// Small-T routing in one launch: the router partials of router_partial_kernel
+// (same grid), and the last CTA to finish -- it sees every partial -- sums
+// them in split order, selects the top k of every token and builds the
+// table.  Requires T <= 64 (the last CTA's warps take the tokens in turn).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                          const float* __restrict__ bias, float* __restrict__ part,
+                                                          int T, int H, int E, int k, int split_len, int G,
+                                                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ sorted_rows,
+                                                          int32_t* __restrict__ row_pos, int4* __restrict__ groups,
+                                                          int32_t* __restrict__ n_groups, int32_t* ticket,
+                                                          Status* st) {
+  router_partial_body(x, wr, part, T, H, E, split_len);
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's partials before its ticket
+    const int total = gridDim.x * gridDim.y * gridDim.z;
+    s_last = (atomicAdd(ticket, 1) == total - 1);
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __shared__ float s_lg[8][256];
+  __shared__ TableSmem<256> sm;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t0 = 0; t0 < T; t0 += 8) {
+    // every thread sums one expert's split partials for up to 8 tokens (independent loads)
+    if (threadIdx.x < E)
+      for (int u = 0; u < 8 && t0 + u < T; ++u)
+        s_lg[u][threadIdx.x] = token_logit(part, gridDim.z, bias, T, E, t0 + u, threadIdx.x);
+    __syncthreads();
+    if (t0 + warp < T)
+      topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)(t0 + warp) * k, topk_w + (size_t)(t0 + warp) * k, lane);
+    __syncthreads();
+  }
+  build_table<256>(topk_idx, T * k, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm);
 }
 
 }  // namespace lmoe

@@ -265,7 +265,7 @@ def test_forward_deterministic(lm):
         lm.lmoe_forward(dims, lm.weights_of(w), x_dev, o, ws)
         outs.append(to_host(o))
     assert np.array_equal(outs[0], outs[1])
-    assert lm.lmoe_last_launch_count() >= 9
+    assert lm.lmoe_last_launch_count() >= 5  # kernels of the fused chain ran
 
 
 def test_host_errors(lm):

@@ -12,7 +12,7 @@ post_expert_norm, weighted sum, unpooler) over one batch of T tokens.
           outside the timed events
   e2e     same metric with the x upload from pinned host memory and the
           output download inside the timed region
-  roofline  the dominant kernel (expert gate/up) timed live with per-launch
+  roofline  the dominant kernel (largest device time) timed live with per-launch
           CUDA events: algorithmic bytes per launch / mean launch duration,
           against the measured HBM copy bandwidth
   cpu_baseline  the CPU oracle, as it stands, on a bounded sample of the same
@@ -45,7 +45,15 @@ METRIC = "latent-MoE layer tokens/s and HBM GB/s (frac of roofline) at T=1..4096
 EXPERT_BYTES = 26_738_688          # one expert: 3 matrices x (codes 8 MiB + scales 512 KiB)
 GATEUP_BYTES = 2 * EXPERT_BYTES // 3
 PROJ_BYTES = 134_217_728           # pooler + unpooler bf16
-GATEUP_LAUNCH = 5                  # launch index of the gate/up kernel inside lmoe_forward
+# source files each measured kernel is built from (the ncu summary's source_sha256 covers these)
+KERNEL_SOURCES = {
+    "expert_gateup": ("experts.cu", "common.cuh"),
+    "expert_down": ("experts.cu", "common.cuh"),
+    "pool_tc_gemm": ("tc_gemm.cu", "tc.cuh", "common.cuh"),
+    "unpool_tc_gemm": ("tc_gemm.cu", "tc.cuh", "common.cuh"),
+    "pool_gemv": ("gemv.cu", "common.cuh"),
+    "unpool_gemv": ("gemv.cu", "common.cuh"),
+}
 
 
 def peaks():
@@ -64,18 +72,38 @@ def workload_name(d: synth.Dims, name: str) -> str:
             f"intermediate {d.I}, MXFP4 W4A16 experts, bf16 pooler/unpooler, fp32 router{s}")
 
 
-def traffic_from_profiles(kernel_src_hash: str):
-    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
-    if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "expert_gateup_decode_t1.txt")
+def kernel_work(kernel: str, d: synth.Dims, touched: int):
+    """Algorithmic (bytes, flops) of one launch of `kernel` on workload d:
+    every operand read once, every result written once, 2 flops per MAC."""
+    T, H, L, I, k = d.T, d.H, d.L, d.I, d.k
+    R = T * k
+    if kernel == "expert_gateup":
+        return touched * GATEUP_BYTES + 2 * T * L + 2 * R * I, 2 * R * 2 * I * L
+    if kernel == "expert_down":
+        return touched * (EXPERT_BYTES - GATEUP_BYTES) + 2 * R * I + 4 * R * L, 2 * R * L * I
+    if kernel.startswith("pool_"):
+        return 2 * L * H + 2 * T * H + 2 * T * L, 2 * T * L * H
+    if kernel.startswith("unpool_"):
+        return 2 * H * L + 2 * T * L + 2 * T * H, 2 * T * H * L
+    return None
+
+
+def profile_name(kernel: str, config: str) -> str:
+    return os.path.join(ROOT, "profiles", f"{kernel}_{config}.txt")
+
+
+def traffic_from_profiles(kernel: str, config: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary for
+    this workload, if it was taken on the current kernel source."""
+    p = profile_name(kernel, config)
     if not os.path.exists(p):
         return None
     vals = {}
     for line in open(p):
         if ":" in line and not line.startswith("#"):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha256") != kernel_src_hash:
+            key, v = line.split(":", 1)
+            vals[key.strip()] = v.strip()
+    if vals.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -83,9 +111,9 @@ def traffic_from_profiles(kernel_src_hash: str):
         return None
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in ("experts.cu", "common.cuh"):
+    for f in KERNEL_SOURCES.get(kernel, ()):
         h.update(open(os.path.join(ROOT, "latent_moe_layer_fp32_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -215,6 +243,71 @@ def run_reference(args, d, name, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(args, d, name, lm, dev):
+    """One dense projection call per step on its own (inputs resident, L2
+    flushed between steps): the pooler (lmoe_pool) or the post-expert path
+    ending in the unpooler (lmoe_norm_combine_unpool: ssq, combine, unpool)."""
+    import torch
+
+    def bf_dev(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    T, H, L, k, E = d.T, d.H, d.L, d.k, d.E
+    dims = lm.dims_of(T, H, L, d.I, E, k, d.eps)
+    ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    if args.stage == "pool":
+        x = bf_dev(synth.make_x(d))
+        pw = bf_dev(synth.normal_bf16(0, synth.TID_POOLER, (L, H), 0.0, (1.0 / H) ** 0.5))
+        x_lat = torch.empty(T, L, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            lm.lmoe_pool(dims, x, pw, x_lat, ws)
+    else:
+        y = torch.from_numpy(synth.normal_f32(0, 21, (T * k, L), 0.0, 1.0)).to(dev)
+        # routing: token t takes experts (t + j * E / k) mod E, equal weights (a valid top-k table)
+        t_ = np.arange(T)[:, None]
+        j_ = np.arange(k)[None, :]
+        idx = torch.from_numpy(((t_ + j_ * (E // k)) % E).astype(np.int32)).to(dev)
+        tw = torch.full((T, k), 1.0 / k, dtype=torch.float32, device=dev)
+        g = bf_dev(synth.normal_bf16(0, synth.TID_GAIN, (E, L), 1.0, 0.1 ** 0.5))
+        uw = bf_dev(synth.normal_bf16(0, synth.TID_UNPOOLER, (H, L), 0.0, (1.0 / L) ** 0.5))
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            lm.lmoe_norm_combine_unpool(dims, y, idx, tw, g, uw, out, ws)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            call()
+        n = lm.lmoe_last_launch_count()
+        names = [lm.lmoe_last_launch_name(j) for j in range(n)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        per = [[] for _ in range(n)]
+        lm.lmoe_profile_events(evs)
+        try:
+            for _ in range(args.steps):
+                flush.zero_()
+                call()
+                torch.cuda.synchronize()
+                for j in range(n):
+                    per[j].append(evs[j].elapsed_time(evs[j + 1]))
+        finally:
+            lm.lmoe_profile_events(None)
+        rc = lm.lmoe_status_check(ws)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
+    pk = peaks()
+    kern = names[-1]
+    ms = statistics.mean(per[-1])
+    nbytes, flops = kernel_work(kern, d, 0)
+    print(json.dumps({"stage": args.stage, "config": name, "kernel": kern, "launch_ms": ms,
+                      "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / pk[
+                          "bf16_tflops"], "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "peak_source": pk["source"],
+                      "kernels_ms": {names[j]: statistics.mean(per[j]) for j in range(n)}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +316,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_t1", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", choices=["pool", "unpool"], default=None,
+                    help="time one dense projection call alone (for profiling); prints a stage line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     name = args.config
@@ -239,6 +334,9 @@ def main():
     lm.load()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.stage:
+        run_stage(args, d, name, lm, dev)
+        return
 
     hw = synth.make_weights(d)
     x = synth.make_x(d)
@@ -268,6 +366,7 @@ def main():
         if rc != 0:
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
         launches_per_step = lm.lmoe_last_launch_count()
+        names = [lm.lmoe_last_launch_name(j) for j in range(launches_per_step)]
         lay = lm.lmoe_workspace_layout(dims)
         offs = ws[lay.expert_offsets:lay.expert_offsets + 4 * (d.E + 1)].view(torch.int32).cpu().numpy()
         touched = int(np.count_nonzero(np.diff(offs)))
@@ -330,13 +429,32 @@ def main():
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
 
     pk = peaks()
-    gate_ms = statistics.mean(per_launch[GATEUP_LAUNCH])
-    gate_bytes = touched * GATEUP_BYTES
-    achieved = gate_bytes / (gate_ms / 1e3) / 1e9
     tokens = d.T * args.steps * world
     value = tokens / total_s
     layer_bytes = touched * EXPERT_BYTES + PROJ_BYTES
-    layer_gbs = layer_bytes * args.steps / (total_s if world == 1 else total_s) / 1e9
+    layer_gbs = layer_bytes * args.steps / total_s / 1e9
+
+    # dominant kernel: the modelled launch with the largest mean device time
+    kern_ms = {names[j]: statistics.mean(v) for j, v in enumerate(per_launch)}
+    cand = [(ms, n) for n, ms in kern_ms.items() if kernel_work(n, d, touched) is not None]
+    dom_ms, dom = max(cand)
+    dom_bytes, dom_flops = kernel_work(dom, d, touched)
+    step_ms_mean = 1e3 * total_s / args.steps
+    tc_peak = pk["bf16_tflops"] if step_ms_mean < 50 or not pk.get("bf16_tflops_sustained") \
+        else pk["bf16_tflops_sustained"]
+    balance = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)  # flops per byte where the two roofs meet
+    if dom_flops / dom_bytes > balance:
+        roof = {"bound": "tensor", "achieved": dom_flops / (dom_ms / 1e3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "algorithmic_flops_per_launch": dom_flops}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    traffic = traffic_from_profiles(dom, name)
+    roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes_per_launch": dom_bytes,
+                 "launch_ms": dom_ms, "peak_source": pk["source"] + (
+                     "" if roof["bound"] == "hbm" else
+                     (" burst" if tc_peak == pk["bf16_tflops"] else " sustained"))})
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -348,12 +466,8 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_gbs / pk["hbm_gbs"],
         "layer_bytes_per_step": layer_bytes,
-        "roofline": {"bound": "hbm", "kernel": "expert gate/up (MXFP4 W4A16 + SwiGLU)", "achieved": achieved,
-                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "traffic": traffic_from_profiles(kernel_source_hash()),
-                     "algorithmic_bytes_per_launch": gate_bytes, "launch_ms": gate_ms,
-                     "peak_source": pk["source"]},
-        "kernels_ms": {str(j): statistics.mean(v) for j, v in enumerate(per_launch)},
+        "roofline": roof,
+        "kernels_ms": kern_ms,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
                 "d2h_bytes_per_step": d.T * d.H * 2},
         "gpu_launches": launches_per_step * args.steps,

@@ -178,6 +178,11 @@ LMOE_API const char* lmoe_error_string(int code);
 /* Number of kernel launches the last lmoe_* call on this thread enqueued. */
 LMOE_API int lmoe_last_launch_count(void);
 
+/* Name of kernel launch i (0-based) of the last lmoe_* call on this host
+ * thread, e.g. "expert_gateup" or "pool_tc_gemm": a static string owned by
+ * the library, or NULL when i is out of range. */
+LMOE_API const char* lmoe_last_launch_name(int i);
+
 /* Routing without a workspace, for callers that cannot allocate device
  * memory where they run the layer (for example a plugin called from another
  * runtime's enqueue path, where that runtime owns every device allocation, or
@@ -207,6 +212,25 @@ LMOE_API int lmoe_route_noalloc(const lmoe_dims* dims, const uint16_t* x, const 
  * owned by the caller; pass n = 0 to switch off.  Recording events between
  * launches serialises the kernels, so use it only to time kernels. */
 LMOE_API int lmoe_profile_events(void* const* events, int n);
+
+/* Regime switches (process-wide; they apply to calls issued after the
+ * setter returns).  No counterpart in the pages: they exist so that both
+ * implementations of a stage can be run and tested on the same input.
+ *
+ *  LMOE_OPT_DENSE_MIN_TOKENS: from this many tokens on, the pooler (H -> L)
+ *    and the unpooler (L -> H) run as tensor-core GEMMs (tcgen05, 128 x 256
+ *    output tiles accumulated in tensor memory); below it, as a
+ *    weight-streaming kernel tuned for a few tokens.  Default 64.
+ *  LMOE_OPT_EXPERT_TC_MIN_TOKENS: from this many tokens on, the experts run
+ *    as grouped tensor-core GEMMs (weights dequantised to bf16 in shared
+ *    memory, up to 256 rows of one expert per tile); below it, as the
+ *    weight-streaming kernels.  Default 512.
+ *
+ * Both implementations of a stage give bf16 (or fp32) of an fp32 sum per
+ * output and differ only in the order of that sum.  value <= 0 restores the
+ * default.  Returns the previous value, or LMOE_EINVAL for an unknown key. */
+enum { LMOE_OPT_DENSE_MIN_TOKENS = 1, LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2 };
+LMOE_API int lmoe_set_option(int key, int value);
 
 /* Format self-check: converts every byte value b (two E2M1 codes, low nibble
  * first) with the same in-register conversion the expert kernels use and

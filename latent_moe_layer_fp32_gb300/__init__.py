@@ -79,9 +79,12 @@ def load(path: str | None = None):
     lib.lmoe_selftest_e2m1.argtypes = [vp]
     lib.lmoe_profile_events.argtypes = [vp, i32]
     lib.lmoe_route_noalloc.argtypes = [dp] + [vp] * 8 + [vp]
+    lib.lmoe_set_option.argtypes = [i32, i32]
+    lib.lmoe_last_launch_name.argtypes = [i32]
+    lib.lmoe_last_launch_name.restype = ctypes.c_char_p
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
               "lmoe_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
-              "lmoe_profile_events", "lmoe_route_noalloc"):
+              "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -199,6 +202,23 @@ def lmoe_status_check(ws, stream=None) -> int:
 
 def lmoe_last_launch_count() -> int:
     return int(load().lmoe_last_launch_count())
+
+
+def lmoe_last_launch_name(i: int) -> str | None:
+    n = load().lmoe_last_launch_name(int(i))
+    return None if n is None else n.decode()
+
+
+LMOE_OPT_DENSE_MIN_TOKENS = 1
+LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2
+
+
+def lmoe_set_option(key: int, value: int) -> int:
+    """Set a regime switch (LMOE_OPT_*); returns the previous value."""
+    rc = int(load().lmoe_set_option(int(key), int(value)))
+    if rc < 0:
+        raise LmoeError(rc, "lmoe_set_option")
+    return rc
 
 
 _event_array = None

@@ -1,5 +1,6 @@
 // C ABI of the latent-MoE layer: argument checks, workspace carving and the
 // launch sequences.  See include/lmoe.h for the contract of every call.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -10,11 +11,19 @@ using namespace lmoe;
 
 namespace {
 
+constexpr int kDenseMinTokensDefault = 64;
+constexpr int kExpertTcMinTokensDefault = 512;
+std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
+std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
+
 thread_local int g_launches = 0;
+constexpr int kMaxNamed = 32;
+thread_local const char* g_names[kMaxNamed];
 thread_local void* const* g_events = nullptr;
 thread_local int g_nevents = 0;
 
-void pre_launch(cudaStream_t s) {
+void pre_launch(cudaStream_t s, const char* name) {
+  if (g_launches < kMaxNamed) g_names[g_launches] = name;
   if (g_events && g_launches < g_nevents) cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
 }
 
@@ -132,7 +141,7 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttr
   do {                                                                           \
     cudaLaunchAttribute attr_[1];                                                \
     cudaLaunchConfig_t cfg_ = pdl_cfg(grid, block, stream, attr_);               \
-    pre_launch(stream);                                                          \
+    pre_launch(stream, #kern);                                                   \
     if (cudaLaunchKernelEx(&cfg_, kern, __VA_ARGS__) != cudaSuccess) return LMOE_ECUDA; \
     ++g_launches;                                                                \
   } while (0)
@@ -181,9 +190,15 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
 
 int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
              uint32_t* xmax, Status* st, cudaStream_t s) {
-  GemvArgs g{pooler_w, x, x_lat, xmax, d->latent, d->hidden, d->T, st};
-  pre_launch(s);
-  CHECK(launch_gemv_bf16(g, s, di.sms));
+  const bool dense = d->T >= g_dense_min_t.load(std::memory_order_relaxed);
+  pre_launch(s, dense ? "pool_tc_gemm" : "pool_gemv");
+  if (dense) {
+    TcGemmArgs g{x_lat, xmax, d->T, d->latent, d->hidden, st};
+    CHECK(launch_tc_gemm_bf16(g, x, pooler_w, s, di.sms));
+  } else {
+    GemvArgs g{pooler_w, x, x_lat, xmax, d->latent, d->hidden, d->T, st};
+    CHECK(launch_gemv_bf16(g, s, di.sms));
+  }
   ++g_launches;
   return LMOE_OK;
 }
@@ -211,7 +226,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.K = L;
   a.h_out = at<uint16_t>(ws, w.h);
   a.h_max = at<uint32_t>(ws, w.hmax);
-  pre_launch(s);
+  pre_launch(s, "expert_gateup");
   CHECK(launch_gateup(a, T, G, s, di.sms));
   ++g_launches;
   a.q = w2_q;
@@ -223,7 +238,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.h_max = nullptr;
   a.y_out = y;
   a.ssq_out = at<float>(ws, w.ssq);
-  pre_launch(s);
+  pre_launch(s, "expert_down");
   CHECK(launch_down(a, T, G, s, di.sms));
   ++g_launches;
   return LMOE_OK;
@@ -241,9 +256,15 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
   }
   LAUNCH(dim3(d->T, (d->latent + 255) / 256), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
          topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts, d->eps, zb, st);
-  GemvArgs g{unpooler_w, zb, out, nullptr, d->hidden, d->latent, d->T, st};
-  pre_launch(s);
-  CHECK(launch_gemv_bf16(g, s, di.sms));
+  const bool dense = d->T >= g_dense_min_t.load(std::memory_order_relaxed);
+  pre_launch(s, dense ? "unpool_tc_gemm" : "unpool_gemv");
+  if (dense) {
+    TcGemmArgs g{out, nullptr, d->T, d->hidden, d->latent, st};
+    CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
+  } else {
+    GemvArgs g{unpooler_w, zb, out, nullptr, d->hidden, d->latent, d->T, st};
+    CHECK(launch_gemv_bf16(g, s, di.sms));
+  }
   ++g_launches;
   return LMOE_OK;
 }
@@ -375,6 +396,21 @@ const char* lmoe_error_string(int code) {
 }
 
 int lmoe_last_launch_count(void) { return g_launches; }
+
+const char* lmoe_last_launch_name(int i) {
+  return (i >= 0 && i < g_launches && i < kMaxNamed) ? g_names[i] : nullptr;
+}
+
+int lmoe_set_option(int key, int value) {
+  switch (key) {
+    case LMOE_OPT_DENSE_MIN_TOKENS:
+      return g_dense_min_t.exchange(value > 0 ? value : kDenseMinTokensDefault);
+    case LMOE_OPT_EXPERT_TC_MIN_TOKENS:
+      return g_expert_tc_min_t.exchange(value > 0 ? value : kExpertTcMinTokensDefault);
+    default:
+      return LMOE_EINVAL;
+  }
+}
 
 int lmoe_profile_events(void* const* events, int n) {
   if (n < 0 || (n > 0 && !events)) return LMOE_EINVAL;

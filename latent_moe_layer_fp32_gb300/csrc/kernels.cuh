@@ -57,6 +57,18 @@ struct GemvArgs {
 };
 int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 
+// ---- tc_gemm.cu -----------------------------------------------------------
+// out[M][N] = bf16_rne(A[M][K] . B[N][K]^T) on tcgen05; N % 256 == 0, K % 64 == 0,
+// A, B, out 16-byte aligned.
+struct TcGemmArgs {
+  uint16_t* out;        // bf16 [M][N]
+  uint32_t* row_max;    // optional: per row, atomic max of |out| as fp32 bits (zeroed by the caller)
+  int M, N, K;
+  Status* st;
+};
+int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* B, cudaStream_t s, int num_sms);
+constexpr int kTcGemmN = 256, kTcGemmK = 64;
+
 // ---- misc.cu --------------------------------------------------------------
 __global__ void row_max_kernel(const uint16_t* in, int K, uint32_t* row_max);
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,

@@ -77,3 +77,18 @@ def test_unsupported_width(lm):
     # K is streamed in 2048-element chunks above 2048, and in 128-byte planes
     for h, l, i in [(8192, 2560, 4096), (8192, 4096, 3328), (8192 + 128, 4096, 4096)]:
         assert lm.lmoe_workspace_bytes(lm.dims_of(1, h, l, i, 256, 8, 1e-6)) == 0
+
+
+def test_regime_options_round_trip(lm):
+    for key, default in ((lm.LMOE_OPT_DENSE_MIN_TOKENS, 64), (lm.LMOE_OPT_EXPERT_TC_MIN_TOKENS, 512)):
+        prev = lm.lmoe_set_option(key, 7)
+        assert prev == default
+        assert lm.lmoe_set_option(key, 0) == 7  # 0 restores the default
+        assert lm.lmoe_set_option(key, prev) == default
+    with pytest.raises(lm.LmoeError):
+        lm.lmoe_set_option(99, 1)
+
+
+def test_launch_names_out_of_range(lm):
+    assert lm.lmoe_last_launch_name(-1) is None
+    assert lm.lmoe_last_launch_name(1 << 20) is None

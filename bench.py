@@ -51,6 +51,8 @@ KERNEL_SOURCES = {
     "expert_down": ("experts.cu", "common.cuh"),
     "pool_tc_gemm": ("tc_gemm.cu", "tc.cuh", "common.cuh"),
     "unpool_tc_gemm": ("tc_gemm.cu", "tc.cuh", "common.cuh"),
+    "expert_gateup_tc": ("tc_experts.cu", "tc.cuh", "common.cuh"),
+    "expert_down_tc": ("tc_experts.cu", "tc.cuh", "common.cuh"),
     "pool_gemv": ("gemv.cu", "common.cuh"),
     "unpool_gemv": ("gemv.cu", "common.cuh"),
 }
@@ -77,9 +79,9 @@ def kernel_work(kernel: str, d: synth.Dims, touched: int):
     every operand read once, every result written once, 2 flops per MAC."""
     T, H, L, I, k = d.T, d.H, d.L, d.I, d.k
     R = T * k
-    if kernel == "expert_gateup":
+    if kernel.startswith("expert_gateup"):
         return touched * GATEUP_BYTES + 2 * T * L + 2 * R * I, 2 * R * 2 * I * L
-    if kernel == "expert_down":
+    if kernel.startswith("expert_down"):
         return touched * (EXPERT_BYTES - GATEUP_BYTES) + 2 * R * I + 4 * R * L, 2 * R * L * I
     if kernel.startswith("pool_"):
         return 2 * L * H + 2 * T * H + 2 * T * L, 2 * T * L * H

@@ -238,6 +238,14 @@ LMOE_API int lmoe_set_option(int key, int value);
  * 512 floats).  Synchronous. */
 LMOE_API int lmoe_selftest_e2m1(float* out);
 
+/* Format self-check of the grouped tensor-core experts: dequantises block b
+ * of 32 E2M1 codes (codes[16b .. 16b+15], low nibble first) with E8M0 scale
+ * byte scales[b] exactly as those kernels do and writes the 32 bf16 values to
+ * out[32b .. 32b+31].  E2M1 times 2^(s-127) is exact in bf16 for every finite
+ * result (OCP MX v1.0; s = 255 gives NaN).  Device pointers; codes and out
+ * 16-byte aligned.  Synchronous. */
+LMOE_API int lmoe_selftest_dequant_bf16(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -77,6 +77,7 @@ def load(path: str | None = None):
     lib.lmoe_error_string.restype = ctypes.c_char_p
     lib.lmoe_last_launch_count.argtypes = []
     lib.lmoe_selftest_e2m1.argtypes = [vp]
+    lib.lmoe_selftest_dequant_bf16.argtypes = [vp, vp, i32, vp]
     lib.lmoe_profile_events.argtypes = [vp, i32]
     lib.lmoe_route_noalloc.argtypes = [dp] + [vp] * 8 + [vp]
     lib.lmoe_set_option.argtypes = [i32, i32]
@@ -84,7 +85,7 @@ def load(path: str | None = None):
     lib.lmoe_last_launch_name.restype = ctypes.c_char_p
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
               "lmoe_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
-              "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option"):
+              "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option", "lmoe_selftest_dequant_bf16"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -241,3 +242,9 @@ def lmoe_profile_events(events):
 
 def lmoe_selftest_e2m1(out):
     _check(load().lmoe_selftest_e2m1(_ptr(out, _F32)), "lmoe_selftest_e2m1")
+
+
+def lmoe_selftest_dequant_bf16(codes, scales, out):
+    """codes: uint8 [nblocks*16], scales: uint8 [nblocks], out: bf16 [nblocks*32] (device tensors)."""
+    n = scales.numel()
+    _check(load().lmoe_selftest_dequant_bf16(_ptr(codes), _ptr(scales), n, _ptr(out)), "lmoe_selftest_dequant_bf16")

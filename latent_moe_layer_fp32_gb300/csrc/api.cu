@@ -16,6 +16,10 @@ constexpr int kExpertTcMinTokensDefault = 512;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
 
+bool experts_tc(int T) { return T >= g_expert_tc_min_t.load(std::memory_order_relaxed); }
+// rows per group of the routing table: what the expert kernels of this regime consume
+int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
+
 thread_local int g_launches = 0;
 constexpr int kMaxNamed = 32;
 thread_local const char* g_names[kMaxNamed];
@@ -80,7 +84,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq;
+  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq, xs;
   int nsplit;
 };
 
@@ -115,6 +119,7 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->pub.y = take(4 * R * L);
   w->ssq = take(4 * R * (L / 32));
   w->pub.z = take(2 * T * L);
+  w->xs = take(2 * R * L);  // x_lat rows in sorted order (grouped tensor-core experts)
   w->pub.total = o;
   return LMOE_OK;
 }
@@ -175,7 +180,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   if (T <= 16) {
     // one launch: router partials, then the last CTA finishes the routing
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, route_small_kernel, x, router_w, router_bias,
-           part, T, H, E, k, H / w.nsplit, expert_max_group(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
+           part, T, H, E, k, H / w.nsplit, group_rows(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
            at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st);
     return LMOE_OK;
   }
@@ -183,7 +188,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
          E, H / w.nsplit);
   LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
          topk_w);
-  LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, expert_max_group(T), offsets,
+  LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, group_rows(T), offsets,
          sorted_rows, row_pos, at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), st);
   return LMOE_OK;
 }
@@ -209,6 +214,37 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
                 const uint8_t* w2_s, float* y, void* ws, cudaStream_t s) {
   const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
+  if (experts_tc(T)) {
+    const int R = T * k;
+    uint16_t* xs = at<uint16_t>(ws, w.xs);
+    LAUNCH(dim3((R + 7) / 8), dim3(256), s, gather_rows_kernel, x_lat, sorted_rows, R, k, L, xs);
+    TcExpertArgs t{};
+    t.groups = at<int4>(ws, w.groups);
+    t.n_groups = at<int32_t>(ws, w.n_groups);
+    t.sorted_rows = sorted_rows;
+    t.inter = I;
+    t.latent = L;
+    t.n_experts = d->n_experts;
+    t.rows = R;
+    t.st = st;
+    t.q = w13_q;
+    t.s = w13_s;
+    t.K = L;
+    t.h_out = at<uint16_t>(ws, w.h);
+    pre_launch(s, "expert_gateup_tc");
+    CHECK(launch_tc_gateup(t, xs, s, di.sms));
+    ++g_launches;
+    t.q = w2_q;
+    t.s = w2_s;
+    t.K = I;
+    t.h_out = nullptr;
+    t.y_out = y;
+    t.ssq_out = at<float>(ws, w.ssq);
+    pre_launch(s, "expert_down_tc");
+    CHECK(launch_tc_down(t, at<uint16_t>(ws, w.h), s, di.sms));
+    ++g_launches;
+    return LMOE_OK;
+  }
   const int G = expert_max_group(T);
   ExpertArgs a{};
   a.groups = at<int4>(ws, w.groups);
@@ -328,8 +364,8 @@ int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t*
     if (!p || !aligned16(p)) return LMOE_EINVAL;
   const int R = d->T * d->top_k;
   LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
-         expert_max_group(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
-  LAUNCH(dim3(d->T), dim3(256), s, row_max_kernel, x_lat, d->latent, at<uint32_t>(ws, w.xmax));
+         group_rows(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
+  if (!experts_tc(d->T)) LAUNCH(dim3(d->T), dim3(256), s, row_max_kernel, x_lat, d->latent, at<uint32_t>(ws, w.xmax));
   return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s));
 }
 
@@ -417,6 +453,15 @@ int lmoe_profile_events(void* const* events, int n) {
   g_events = n > 0 ? events : nullptr;
   g_nevents = n;
   return LMOE_OK;
+}
+
+int lmoe_selftest_dequant_bf16(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out) {
+  if (!codes || !scales || !out || nblocks < 1 || !aligned16(codes) || !aligned16(out)) return LMOE_EINVAL;
+  DevInfo di;
+  CHECK(dev_info(&di));
+  dequant_selftest_kernel<<<(nblocks + 127) / 128, 128>>>(codes, scales, nblocks, out);
+  if (cudaGetLastError() != cudaSuccess) return LMOE_ECUDA;
+  return cudaDeviceSynchronize() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
 int lmoe_selftest_e2m1(float* out) {

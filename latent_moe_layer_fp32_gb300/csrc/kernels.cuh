@@ -69,6 +69,29 @@ struct TcGemmArgs {
 int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* B, cudaStream_t s, int num_sms);
 constexpr int kTcGemmN = 256, kTcGemmK = 64;
 
+// ---- tc_experts.cu ---------------------------------------------------------
+// Grouped W4A16 expert GEMMs on tcgen05 (groups of up to 256 sorted rows).
+struct TcExpertArgs {
+  const uint8_t* q;         // codes [E][rows_per_expert][K/2]
+  const uint8_t* s;         // scales [E][rows_per_expert][K/32]
+  const int4* groups;       // {e, p0, n <= 256, 0}
+  const int32_t* n_groups;
+  const int32_t* sorted_rows;  // down: original row id of each sorted position
+  int K;                    // L (gate/up) or I (down)
+  int inter, latent, n_experts;
+  int rows;                 // R = T * k
+  uint16_t* h_out;          // gate/up: bf16 [R][I] by sorted position
+  float* y_out;             // down: fp32 [R][L] by original row id
+  float* ssq_out;           // down: fp32 [R][L/32] sum of y^2 per 32-column tile
+  Status* st;
+};
+int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream_t s, int num_sms);
+int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms);
+constexpr int kTcExpertGroup = 256;
+__global__ void gather_rows_kernel(const uint16_t* x_lat, const int32_t* sorted_rows, int R, int k, int L,
+                                   uint16_t* x_sorted);
+__global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out);
+
 // ---- misc.cu --------------------------------------------------------------
 __global__ void row_max_kernel(const uint16_t* in, int K, uint32_t* row_max);
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,

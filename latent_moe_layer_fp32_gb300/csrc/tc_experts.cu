@@ -1,0 +1,555 @@
+// Routed experts for many tokens: grouped W4A16 GEMMs on tcgen05.
+//
+// "Muse Spark Open on Gaudi 2", section "The latent MoE: A' with a per-expert
+// norm" and "Soporte de dia 0 para Muse Spark Open en vLLM", section "MoE
+// latente": each routed row r = (token, route) of expert e computes
+//   h_r = bf16(silu(x_lat . Wg_e^T) * (x_lat . Wu_e^T)),   y_r = h_r . Wd_e^T,
+// with MXFP4 weights (OCP MX v1.0: E2M1 codes, one E8M0 scale per 32 K
+// elements) and bf16 activations, fp32 accumulation.
+//
+// One work item = one group of up to 256 rows of one expert (sorted
+// positions p0 .. p0+n-1) x one 128-row tile of the expert's output features.
+// The weight tile is the MMA's A operand (M = 128), the group's activation
+// rows are B (N = n rounded up to 16), so ragged groups cost no padded rows
+// of A.  Per CTA (persistent, one per SM, 15 warps):
+//   warp 0      TMA: raw MXFP4 codes, 128 rows x 256 K per stage (16 KB per
+//               weight matrix), into a ring
+//   warp 1      TMA: activation rows (sorted order), 32-row boxes of 64 K
+//   warp 2      TMEM owner; one thread issues tcgen05.mma kind::f16
+//   warps 3-10  dequantise codes to bf16 (E2M1 x 2^(s-127) is exact in
+//               bf16) in the 128-byte-swizzled K-major layout the MMA reads
+//   warps 11-14 epilogue: tcgen05.ld, SwiGLU -> h (gate/up), or y and the
+//               per-32-column sums of squares for post_expert_norm (down)
+// Gate/up runs the gate and the up tile against the same activation stage
+// into two TMEM accumulators (columns 0-255 and 256-511), so SwiGLU pairs
+// are lane-local; down double-buffers one accumulator.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace lmoe {
+namespace {
+
+constexpr int kXM = 128;                 // weight rows per matrix tile (MMA M)
+constexpr int kXNmax = 256;              // activation rows per group (MMA N, max)
+constexpr int kXTile = kXM * 128;        // 16 KB: 128 rows x 128 B (codes of 256 K, or bf16 of 64 K)
+constexpr int kXBStage = kXNmax * 128;   // 32 KB: 256 activation rows x 64 K bf16
+constexpr int kXBBox = 32 * 128;         // one 32-row activation box
+constexpr int kDqWarps = 8, kEpWarps = 4;
+constexpr int kXThreads = (3 + kDqWarps + kEpWarps) * 32;
+
+template <int MODE>
+struct XCfg;
+template <>
+struct XCfg<0> {  // gate/up: two weight matrices per item, single accumulator pair
+  static constexpr int NMAT = 2, RAW = 2, AST = 2, BST = 3, NACC = 1;
+};
+template <>
+struct XCfg<1> {  // down: one weight matrix, double-buffered accumulator
+  static constexpr int NMAT = 1, RAW = 4, AST = 3, BST = 3, NACC = 2;
+};
+
+template <int MODE>
+constexpr int xring_bytes() {
+  using C = XCfg<MODE>;
+  return C::RAW * C::NMAT * kXTile + C::AST * C::NMAT * kXTile + C::BST * kXBStage;
+}
+template <int MODE>
+constexpr int xsmem_bytes() {
+  return xring_bytes<MODE>() + 1024 + 256;
+}
+static_assert(xsmem_bytes<0>() <= 232448 && xsmem_bytes<1>() <= 232448, "shared memory budget");
+
+// ---------------------------------------------------------------------------
+// MXFP4 -> bf16.  E2M1 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 have bf16 bit
+// patterns 0, 3F00, 3F80, 3FC0, 4000, 4040, 4080, 40C0; the E8M0 scale
+// 2^(s-127) adds s-127 to the exponent field of every nonzero magnitude,
+// exact while the result stays a normal number (2 <= s <= 252).  A block's
+// eight scaled patterns are split into low-byte and high-byte tables and
+// looked up with byte permutes, 3-bit code magnitudes as selectors.
+// ---------------------------------------------------------------------------
+struct DqTable {
+  uint32_t la, lb, ha, hb;  // low / high bytes of the patterns of magnitudes 0-3 and 4-7
+};
+
+__device__ __forceinline__ DqTable dq_table(uint32_t s) {
+  const uint32_t d = s * 128u - 127u * 128u;  // (s - 127) << 7, two's complement
+  const uint32_t p01 = 0x3F000000u + (d << 16);
+  const uint32_t p23 = 0x3FC03F80u + d * 0x10001u;
+  const uint32_t p45 = 0x40404000u + d * 0x10001u;
+  const uint32_t p67 = 0x40C04080u + d * 0x10001u;
+  DqTable t;
+  t.la = __byte_perm(p01, p23, 0x6420);
+  t.ha = __byte_perm(p01, p23, 0x7531);
+  t.lb = __byte_perm(p45, p67, 0x6420);
+  t.hb = __byte_perm(p45, p67, 0x7531);
+  return t;
+}
+
+// Eight codes (one word, element i in nibble i) -> four bf16x2 words.
+__device__ __forceinline__ void dq8(uint32_t w, const DqTable& t, uint32_t* o) {
+  const uint32_t mags = w & 0x77777777u;
+  const uint32_t w4 = w << 4;
+  // byte i of sa / sb carries the sign of element i / 4+i in its top bit
+  const uint32_t sa = __byte_perm(w4, w, 0x5140);
+  const uint32_t sb = __byte_perm(w4, w, 0x7362);
+  uint32_t lo = __byte_perm(t.la, t.lb, mags);
+  uint32_t hi = __byte_perm(t.ha, t.hb, mags) | (sa & 0x80808080u);
+  o[0] = __byte_perm(lo, hi, 0x5140);
+  o[1] = __byte_perm(lo, hi, 0x7362);
+  const uint32_t mh = mags >> 16;
+  lo = __byte_perm(t.la, t.lb, mh);
+  hi = __byte_perm(t.ha, t.hb, mh) | (sb & 0x80808080u);
+  o[2] = __byte_perm(lo, hi, 0x5140);
+  o[3] = __byte_perm(lo, hi, 0x7362);
+}
+
+// Scales outside the exponent-add range (subnormal, overflowing or NaN
+// results): the value in fp32, then bf16 (exact: every finite product is
+// representable in bf16).
+__device__ __noinline__ void dq_block_exact(uint4 c, uint32_t s, uint32_t* o) {
+  const float sc = e8m0_to_f32(s);
+  const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t pair = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t code = (wv[i >> 2] >> (8 * (i & 3) + 4 * h)) & 15u;
+      const uint32_t m = code & 7u;
+      float mag = m < 2 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)(m & 1u), (int)(m >> 1) - 1);
+      if (code & 8u) mag = -mag;
+      pair |= (uint32_t)f32_to_bf16_bits(mag * sc) << (16 * h);
+    }
+    o[i] = pair;
+  }
+}
+
+// 32 codes (16 bytes) with scale byte s -> 32 bf16 (16 words).
+__device__ __forceinline__ void dq_block(uint4 c, uint32_t s, uint32_t* o) {
+  if (s >= 2u && s <= 252u) {
+    const DqTable t = dq_table(s);
+    dq8(c.x, t, o);
+    dq8(c.y, t, o + 4);
+    dq8(c.z, t, o + 8);
+    dq8(c.w, t, o + 12);
+  } else {
+    dq_block_exact(c, s, o);
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+}  // namespace
+
+// One group of the item list, checked: false (and an error recorded) for an
+// entry the routing table could not have produced.
+struct XItem {
+  int e, p0, n, ft;
+};
+
+__device__ __forceinline__ bool x_item(const TcExpertArgs& a, int it, int nft, XItem* x) {
+  const int4 g = a.groups[it / nft];
+  x->e = g.x;
+  x->p0 = g.y;
+  x->n = g.z;
+  x->ft = it % nft;
+  if (g.x < 0 || g.x >= a.n_experts || g.z < 1 || g.z > kXNmax || g.y < 0 || g.y + g.z > a.rows) {
+    set_error(a.st, LMOE_EDEVICE_CHECK, 60);
+    return false;
+  }
+  return true;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kXThreads, 1)
+    tc_expert_kernel(const TcExpertArgs a, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_act) {
+  using C = XCfg<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_raw = smem;                                   // [RAW][NMAT] code tiles
+  uint8_t* s_a = s_raw + C::RAW * C::NMAT * kXTile;        // [AST][NMAT] bf16 weight tiles
+  uint8_t* s_b = s_a + C::AST * C::NMAT * kXTile;          // [BST] activation stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_b + C::BST * kXBStage);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + C::RAW;
+  uint64_t* a_full = raw_empty + C::RAW;
+  uint64_t* a_empty = a_full + C::AST;
+  uint64_t* b_full = a_empty + C::AST;
+  uint64_t* b_empty = b_full + C::BST;
+  uint64_t* acc_full = b_empty + C::BST;
+  uint64_t* acc_empty = acc_full + C::NACC;
+  uint64_t* done = acc_empty + C::NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::RAW; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kDqWarps);
+    }
+    for (int i = 0; i < C::AST; ++i) {
+      mbar_init(&a_full[i], kDqWarps);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < C::BST; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < C::NACC; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpWarps);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 2) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();
+  pdl_trigger();
+
+  const int nft = (MODE == 0 ? a.inter : a.latent) / kXM;  // feature tiles per group
+  const int n_items = *a.n_groups * nft;
+  const int K = a.K, nks = K / 64, nkr = K / 256;
+  const int rows_pe = MODE == 0 ? 2 * a.inter : a.latent;  // weight rows per expert
+
+  if (warp == 0) {
+    // ---------------- raw code producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int rs = 0, issued = 0;
+      uint32_t rph = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        XItem x;
+        if (!x_item(a, it, nft, &x)) continue;
+        for (int kr = 0; kr < nkr; ++kr) {
+          if (!mbar_wait(&raw_empty[rs], rph ^ 1, a.st, 61)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[rs], C::NMAT * kXTile);
+#pragma unroll
+          for (int m = 0; m < C::NMAT; ++m)
+            tma_load_2d(s_raw + (rs * C::NMAT + m) * kXTile, &tm_q, kr * 128,
+                        x.e * rows_pe + m * a.inter + x.ft * kXM, &raw_full[rs], pol);
+          ++issued;
+          if (++rs == C::RAW) {
+            rs = 0;
+            rph ^= 1;
+          }
+        }
+      }
+      for (int i = 0; i < C::RAW && i < issued; ++i) {  // the last copies land before exit
+        if (--rs < 0) {
+          rs = C::RAW - 1;
+          rph ^= 1;
+        }
+        mbar_wait(&raw_full[rs], rph, a.st, 62);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- activation producer ----------------
+    const uint64_t pol = policy_evict_last();
+    int bs = 0, issued = 0;
+    uint32_t bph = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      XItem x;
+      if (!x_item(a, it, nft, &x)) continue;
+      const int nb = (x.n + 31) >> 5;
+      for (int ks = 0; ks < nks; ++ks) {
+        int good = 1;
+        if (lane == 0) good = mbar_wait(&b_empty[bs], bph ^ 1, a.st, 63);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&b_full[bs], nb * kXBBox);
+        __syncwarp();
+        if (lane < nb)
+          tma_load_2d(s_b + bs * kXBStage + lane * kXBBox, &tm_act, ks * 64, x.p0 + lane * 32, &b_full[bs], pol);
+        ++issued;
+        if (++bs == C::BST) {
+          bs = 0;
+          bph ^= 1;
+        }
+      }
+    }
+    if (lane == 0)
+      for (int i = 0; i < C::BST && i < issued; ++i) {
+        if (--bs < 0) {
+          bs = C::BST - 1;
+          bph ^= 1;
+        }
+        mbar_wait(&b_full[bs], bph, a.st, 64);
+      }
+  } else if (warp == 2) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int as = 0, bs = 0, acc = 0;
+      uint32_t aph = 0, bph = 0, cph = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        XItem x;
+        if (!x_item(a, it, nft, &x)) continue;
+        const uint32_t idesc = idesc_bf16_f32(kXM, (x.n + 15) & ~15);
+        if (!mbar_wait(&acc_empty[acc], cph ^ 1, a.st, 65)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (MODE == 0 ? 0u : (uint32_t)acc * 256u);
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(&a_full[as], aph, a.st, 66) || !mbar_wait(&b_full[bs], bph, a.st, 67)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(s_b + bs * kXBStage);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int m = 0; m < C::NMAT; ++m)
+              tc_mma_bf16(d + m * 256u, smem_desc_sw128(smem_u32(s_a + (as * C::NMAT + m) * kXTile) + kk * 32),
+                          smem_desc_sw128(b0 + kk * 32), idesc, (ks | kk) != 0);
+          tc_commit(&a_empty[as]);
+          tc_commit(&b_empty[bs]);
+          if (++as == C::AST) {
+            as = 0;
+            aph ^= 1;
+          }
+          if (++bs == C::BST) {
+            bs = 0;
+            bph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == C::NACC) {
+          acc = 0;
+          cph ^= 1;
+        }
+      }
+      tc_commit(done);  // every MMA issued has completed before TMEM is released
+      mbar_wait(done, 0, a.st, 68);
+    }
+  } else if (warp < 3 + kDqWarps) {
+    // ---------------- dequantisation: codes -> bf16 weight tiles ----------------
+    // gate/up: thread -> one row of the gate (0-127) or up (128-255) tile, both
+    // 32-blocks of each 64-K step; down: thread -> one 32-block of one row.
+    const int dq = threadIdx.x - 96;
+    const int m = MODE == 0 ? dq >> 7 : 0;
+    const int rr = dq & 127;
+    const int b_first = MODE == 0 ? 0 : dq >> 7;
+    constexpr int NB = MODE == 0 ? 2 : 1;
+    const int sw = rr & 7;
+    int rs = 0, as = 0;
+    uint32_t rph = 0, aph = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      XItem x;
+      if (!x_item(a, it, nft, &x)) continue;
+      const size_t grow = (size_t)x.e * rows_pe + (size_t)m * a.inter + (size_t)x.ft * kXM + rr;
+      const uint8_t* srow = a.s + grow * (size_t)(K / 32);
+      for (int kr = 0; kr < nkr && ok; ++kr) {
+        const uint2 sc8 = __ldg(reinterpret_cast<const uint2*>(srow + kr * 8));
+        if (!mbar_wait(&raw_full[rs], rph, a.st, 70)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* rawt = s_raw + (rs * C::NMAT + m) * kXTile + rr * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (!mbar_wait(&a_empty[as], aph ^ 1, a.st, 71)) {
+            ok = false;
+            break;
+          }
+          uint8_t* at = s_a + (as * C::NMAT + m) * kXTile + rr * 128;
+#pragma unroll
+          for (int bi = 0; bi < NB; ++bi) {
+            const int b = MODE == 0 ? bi : b_first;
+            const int kb = 2 * j + b;  // 32-block within the raw stage
+            const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
+            const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
+            uint32_t o[16];
+            dq_block(c, (sword >> (8 * (kb & 3))) & 0xFFu, o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(at + (((4 * b + q) ^ sw) << 4)) =
+                  make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+          fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[as]);
+          if (++as == C::AST) {
+            as = 0;
+            aph ^= 1;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        if (++rs == C::RAW) {
+          rs = 0;
+          rph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> h (gate/up) or y, ssq (down) ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    int acc = 0;
+    uint32_t cph = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      XItem x;
+      if (!x_item(a, it, nft, &x)) continue;
+      if (!mbar_wait(&acc_full[acc], cph, a.st, 72)) break;
+      tc_fence_after();
+      const int f = x.ft * kXM + q * 32 + lane;  // output feature of this lane
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 0 ? 0u : (uint32_t)acc * 256u);
+      for (int c0 = 0; c0 < x.n; c0 += 32) {
+        if (MODE == 0) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + c0, g);
+          tmem_ld32(tb + 256 + c0, u);
+          tmem_ld_wait();
+          uint16_t* hp = a.h_out + (size_t)(x.p0 + c0) * a.inter + f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (c0 + i < x.n) {
+              const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv / (1.0f + expf(-gv)) * uv);
+            }
+          }
+        } else {
+          uint32_t v[32];
+          tmem_ld32(tb + c0, v);
+          tmem_ld_wait();
+          const int my_row = c0 + lane < x.n ? a.sorted_rows[x.p0 + c0 + lane] : 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int rid = __shfl_sync(0xffffffffu, my_row, i);
+            if (c0 + i < x.n) a.y_out[(size_t)rid * a.latent + f] = __uint_as_float(v[i]);
+          }
+          // sum of squares over this warp's 32 features for each of the 32 columns:
+          // halve the column set at every step, lane l ends with column l
+          float s[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]) * __uint_as_float(v[i]);
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {
+            const bool upper = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = upper ? s[i] : s[i + w];
+              const float keep = upper ? s[i + w] : s[i];
+              s[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+          }
+          if (c0 + lane < x.n) a.ssq_out[(size_t)my_row * (a.latent / 32) + (x.ft * kXM + q * 32) / 32] = s[0];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == C::NACC) {
+        acc = 0;
+        cph ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int MODE>
+int launch_tc_expert(const TcExpertArgs& a, const uint16_t* act, cudaStream_t s, int num_sms) {
+  const int K = a.K;
+  if (K % 256 || a.inter % kXM || a.latent % kXM) return LMOE_EUNSUPPORTED;
+  constexpr int smem = xsmem_bytes<MODE>();
+  static std::atomic<unsigned long long> attr_done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ECUDA;
+  if (!(attr_done.load() >> (dev & 63) & 1ull)) {
+    if (cudaFuncSetAttribute(tc_expert_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return LMOE_ECUDA;
+    attr_done.fetch_or(1ull << (dev & 63));
+  }
+  const int rows_pe = MODE == 0 ? 2 * a.inter : a.latent;
+  CUtensorMap tq, ta;
+  {
+    const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)a.n_experts * rows_pe};
+    const uint64_t strides[1] = {(uint64_t)K / 2};
+    const uint32_t box[2] = {128, kXM};
+    if (get_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LMOE_ECUDA;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)a.rows};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {64, 32};
+    if (get_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return LMOE_ECUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kXThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_expert_kernel<MODE>, a, tq, ta) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+}
+
+int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream_t s, int num_sms) {
+  return launch_tc_expert<0>(a, x_sorted, s, num_sms);
+}
+
+int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms) {
+  return launch_tc_expert<1>(a, h, s, num_sms);
+}
+
+// x_sorted[p] = x_lat[sorted_rows[p] / k]: one warp per sorted row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x_lat,
+                                                          const int32_t* __restrict__ sorted_rows, int R, int k,
+                                                          int L, uint16_t* __restrict__ x_sorted) {
+  pdl_wait();
+  pdl_trigger();
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (p >= R) return;
+  const int t = sorted_rows[p] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x_lat + (size_t)t * L);
+  uint4* dst = reinterpret_cast<uint4*>(x_sorted + (size_t)p * L);
+  for (int i = lane; i < L / 8; i += 32) dst[i] = __ldg(src + i);
+}
+
+// Device self-check of the expert dequantisation: block b of 32 codes
+// (codes[16 b .. 16 b + 15]) with scale byte scales[b] -> out[32 b .. 32 b + 31].
+__global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  const uint4 c = *reinterpret_cast<const uint4*>(codes + 16 * (size_t)b);
+  uint32_t o[16];
+  dq_block(c, scales[b], o);
+  uint4* dst = reinterpret_cast<uint4*>(out + 32 * (size_t)b);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+}  // namespace lmoe

@@ -52,8 +52,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
+    headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    newest_header = max((os.path.getmtime(h) for h in headers), default=0.0)
+
     def compile_one(src):
         obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        if (not force and os.path.exists(obj) and not extra
+                and os.path.getmtime(obj) >= max(os.path.getmtime(src), newest_header)):
+            return obj  # object newer than its source and every header
         cmd = [cc, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -16,6 +16,12 @@ constexpr int kExpertTcMinTokensDefault = 512;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
 
+// the router as a tensor-core GEMM: above the fused small-T routing, from the
+// dense-projection threshold on, for expert counts that fill whole 32-column chunks
+bool router_tc(const lmoe_dims* d) {
+  return d->T > 16 && d->T >= g_dense_min_t.load(std::memory_order_relaxed) && d->n_experts % 32 == 0;
+}
+
 bool experts_tc(int T) { return T >= g_expert_tc_min_t.load(std::memory_order_relaxed); }
 // rows per group of the routing table: what the expert kernels of this regime consume
 int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
@@ -84,7 +90,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq, xs;
+  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq, xs, wr3;
   int nsplit;
 };
 
@@ -120,6 +126,7 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->ssq = take(4 * R * (L / 32));
   w->pub.z = take(2 * T * L);
   w->xs = take(2 * R * L);  // x_lat rows in sorted order (grouped tensor-core experts)
+  w->wr3 = take(2 * E * 3 * (size_t)d->hidden);  // router weights as three bf16 parts (tensor-core router)
   w->pub.total = o;
   return LMOE_OK;
 }
@@ -184,9 +191,35 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
            at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st);
     return LMOE_OK;
   }
-  LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T, H,
-         E, H / w.nsplit);
-  LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, w.nsplit, router_bias, T, E, k, topk_idx,
+  int nsplit = w.nsplit;
+  if (router_tc(d)) {
+    // logits on the tensor cores: x (bf16) against the three bf16 parts of Wr, split-K partials
+    uint16_t* w3 = at<uint16_t>(ws, w.wr3);
+    LAUNCH(dim3(2 * di.sms), dim3(256), s, router_split_kernel, router_w, E, H, w3);
+    const int kblocks = 3 * H / 64, tiles_m = (T + 127) / 128;
+    nsplit = 1;
+    for (int c = 16; c >= 2; --c)
+      if (kblocks % c == 0 && tiles_m * c <= di.sms) {
+        nsplit = c;
+        break;
+      }
+    TcGemmArgs g{};
+    g.M = T;
+    g.N = E;
+    g.K = 3 * H;
+    g.st = st;
+    g.out_f32 = part;
+    g.a_kblocks = H / 64;
+    g.n_tile = E;
+    g.nsplit = nsplit;
+    pre_launch(s, "router_tc_gemm");
+    CHECK(launch_tc_gemm_bf16(g, x, w3, s, di.sms));
+    ++g_launches;
+  } else {
+    LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T,
+           H, E, H / w.nsplit);
+  }
+  LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, nsplit, router_bias, T, E, k, topk_idx,
          topk_w);
   LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, group_rows(T), offsets,
          sorted_rows, row_pos, at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), st);

@@ -15,6 +15,7 @@ __global__ void route_small_kernel(const uint16_t* x, const float* wr, const flo
                                    int E, int k, int split_len, int G, int32_t* topk_idx, float* topk_w,
                                    int32_t* offsets, int32_t* sorted_rows, int32_t* row_pos, int4* groups,
                                    int32_t* n_groups, int32_t* ticket, Status* st);
+__global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3);
 __global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32_t* offsets, int32_t* sorted_rows,
                              int32_t* row_pos, int4* groups, int32_t* n_groups, Status* st);
 
@@ -61,10 +62,14 @@ int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 // out[M][N] = bf16_rne(A[M][K] . B[N][K]^T) on tcgen05; N % 256 == 0, K % 64 == 0,
 // A, B, out 16-byte aligned.
 struct TcGemmArgs {
-  uint16_t* out;        // bf16 [M][N]
+  uint16_t* out;        // bf16 [M][N] (unless out_f32 is set)
   uint32_t* row_max;    // optional: per row, atomic max of |out| as fp32 bits (zeroed by the caller)
   int M, N, K;
   Status* st;
+  float* out_f32;       // optional: fp32 partial sums [nsplit][M][N] instead of bf16 out
+  int a_kblocks;        // > 0: A's 64-wide k-block index wraps modulo this (A reused along K)
+  int n_tile;           // output columns per tile: 256 (0), or a multiple of 32 below it
+  int nsplit;           // K split into this many ranges, one partial each (0 or 1: none)
 };
 int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* B, cudaStream_t s, int num_sms);
 constexpr int kTcGemmN = 256, kTcGemmK = 64;

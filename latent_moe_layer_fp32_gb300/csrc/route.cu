@@ -352,4 +352,33 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
   build_table<256>(topk_idx, T * k, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm);
 }
 
+// ---------------------------------------------------------------------------
+// Router weights for the tensor-core router: w = w1 + w2 + w3 exactly, each a
+// bf16 holding the next 8 significant bits of the fp32 value (w1, w2 by
+// truncation, w3 by rounding the last 8 bits, which it holds exactly for any
+// |w| >= 2^-110).  Laid out [E][3H] as (w1 | w2 | w3), so that
+//   x . w = x . w1 + x . w2 + x . w3
+// is one GEMM over K = 3H against x repeated three times.  Products of the bf16
+// x with each part are exact in fp32, so the tensor core reproduces an fp32
+// dot product up to the order of the fp32 sum.  Finite weights required.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ wr, int E, int H,
+                                                           uint16_t* __restrict__ w3) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t n = (size_t)E * H;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / H, h = i % H;
+    const float w = wr[i];
+    const uint32_t b1 = __float_as_uint(w) >> 16;
+    const float r1 = w - __uint_as_float(b1 << 16);
+    const uint32_t b2 = __float_as_uint(r1) >> 16;
+    const float r2 = r1 - __uint_as_float(b2 << 16);
+    uint16_t* row = w3 + e * 3 * H;
+    row[h] = (uint16_t)b1;
+    row[H + h] = (uint16_t)b2;
+    row[2 * H + h] = f32_to_bf16_bits(r2);
+  }
+}
+
 }  // namespace lmoe

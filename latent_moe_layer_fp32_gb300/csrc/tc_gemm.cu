@@ -62,8 +62,11 @@ __global__ void __launch_bounds__(256, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int tiles_m = (a.M + kTM - 1) / kTM, tiles_n = a.N / kTN, ntiles = tiles_m * tiles_n;
-  const int nk = a.K / kTK;
+  const int n_tile = a.n_tile > 0 ? a.n_tile : kTN;
+  const int nsplit = a.nsplit > 1 ? a.nsplit : 1;
+  const int tiles_m = (a.M + kTM - 1) / kTM, tiles_n = a.N / n_tile, tiles_mn = tiles_m * tiles_n;
+  const int ntiles = tiles_mn * nsplit;
+  const int nk = a.K / kTK / nsplit;  // k-blocks per tile
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -75,15 +78,16 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     int issued = 0;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const int mt = t % tiles_m, nt = t / tiles_m;
-      for (int kb = 0; kb < nk; ++kb) {
+      const int mt = t % tiles_m, nt = (t / tiles_m) % tiles_n, ks = t / tiles_mn;
+      for (int kb = ks * nk; kb < (ks + 1) * nk; ++kb) {
         if (!mbar_wait(&empty[s], ph ^ 1, a.st, 21)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kTAbytes + kTBbytes);
-        tma_load_2d(sA + s * kTAbytes, &tmA, kb * kTK, mt * kTM, &full[s], pol_b);
-        tma_load_2d(sB + s * kTBbytes, &tmB, kb * kTK, nt * kTN, &full[s], pol_b);
+        mbar_arrive_expect_tx(&full[s], kTAbytes + n_tile * kTK * 2);
+        tma_load_2d(sA + s * kTAbytes, &tmA, (a.a_kblocks > 0 ? kb % a.a_kblocks : kb) * kTK, mt * kTM, &full[s],
+                    pol_b);
+        tma_load_2d(sB + s * kTBbytes, &tmB, kb * kTK, nt * n_tile, &full[s], pol_b);
         ++issued;
         if (++s == kTStages) {
           s = 0;
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = idesc_bf16_f32(kTM, kTN);
+    const uint32_t idesc = idesc_bf16_f32(kTM, n_tile);
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
@@ -142,16 +146,26 @@ __global__ void __launch_bounds__(256, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const int mt = t % tiles_m, nt = t / tiles_m;
+      const int mt = t % tiles_m, nt = (t / tiles_m) % tiles_n, ks = t / tiles_mn;
       if (!mbar_wait(&accf[acc], aph, a.st, 26)) break;
       tc_fence_after();
       const int row = mt * kTM + wq * 32 + lane;
       float rmax = 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < kTN / 32; ++ch) {
+      for (int ch = 0; ch < n_tile / 32; ++ch) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(wq * 32) << 16) + acc * kTN + ch * 32, r);
         tmem_ld_wait();
+        if (a.out_f32) {
+          if (row < a.M) {
+            float4* dst = reinterpret_cast<float4*>(a.out_f32 + ((size_t)ks * a.M + row) * a.N + nt * n_tile + ch * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          }
+          continue;
+        }
         uint32_t o[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -161,7 +175,7 @@ __global__ void __launch_bounds__(256, 1)
           o[i] = (uint32_t)lo | ((uint32_t)hi << 16);
         }
         if (row < a.M) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)row * a.N + nt * kTN + ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)row * a.N + nt * n_tile + ch * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
@@ -185,7 +199,10 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* B, cudaStream_t s, int num_sms) {
-  if (a.N % kTN || a.K % kTK || a.M < 1) return LMOE_EUNSUPPORTED;
+  const int n_tile = a.n_tile > 0 ? a.n_tile : kTN;
+  const int nsplit = a.nsplit > 1 ? a.nsplit : 1;
+  if (n_tile % 32 || n_tile > kTN || a.N % n_tile || a.K % (kTK * nsplit) || a.M < 1) return LMOE_EUNSUPPORTED;
+  if (a.a_kblocks > 0 && (a.K / kTK) % a.a_kblocks) return LMOE_EUNSUPPORTED;
   constexpr int smem = kTStages * (kTAbytes + kTBbytes) + 1024 + 256;
   static_assert(smem <= 232448, "shared memory budget");
   static std::atomic<unsigned long long> attr_done{0};
@@ -198,8 +215,9 @@ int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* 
   }
   CUtensorMap ta, tb;
   {
-    const uint64_t dims[2] = {(uint64_t)a.K, (uint64_t)a.M};
-    const uint64_t strides[1] = {(uint64_t)a.K * 2};
+    const uint64_t ka = a.a_kblocks > 0 ? (uint64_t)a.a_kblocks * kTK : (uint64_t)a.K;  // A's own width
+    const uint64_t dims[2] = {ka, (uint64_t)a.M};
+    const uint64_t strides[1] = {ka * 2};
     const uint32_t box[2] = {kTK, kTM};
     if (get_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return LMOE_ECUDA;
@@ -207,11 +225,11 @@ int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* 
   {
     const uint64_t dims[2] = {(uint64_t)a.K, (uint64_t)a.N};
     const uint64_t strides[1] = {(uint64_t)a.K * 2};
-    const uint32_t box[2] = {kTK, kTN};
+    const uint32_t box[2] = {kTK, (uint32_t)n_tile};
     if (get_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return LMOE_ECUDA;
   }
-  const int ntiles = ((a.M + kTM - 1) / kTM) * (a.N / kTN);
+  const int ntiles = ((a.M + kTM - 1) / kTM) * (a.N / n_tile) * nsplit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ntiles < num_sms ? ntiles : num_sms);
   cfg.blockDim = dim3(256);

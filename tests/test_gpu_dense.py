@@ -7,6 +7,7 @@ layer is checked once with the tensor-core projections on the small shape.
 from __future__ import annotations
 
 import contextlib
+import dataclasses
 
 import numpy as np
 import pytest
@@ -111,3 +112,25 @@ def test_regimes_agree_on_rounding(lm):
         res[regime] = to_host(x_lat)
     bound = 2.0 * sum_err(d.H, np.abs(bf(x)), np.abs(bf(hw["pooler_w"])))
     check_bf16_close(res["tensor"], res["stream"], "tensor vs stream", bound, frac=0.05)
+
+
+ROUTE_CASES = [("tiny_e32", 200), ("tiny_e32", 1000), ("verify_t8", 300)]
+
+
+@pytest.mark.parametrize("regime", ["stream", "tensor"])
+@pytest.mark.parametrize("name,T", ROUTE_CASES, ids=[f"{n}_T{t}" for n, t in ROUTE_CASES])
+def test_router_regimes(lm, orc, name, T, regime):
+    """The router's logits on CUDA cores (fp32 FMA) or on the tensor cores
+    (x against the three bf16 parts of the fp32 weights, split-K): both give
+    the oracle's top-k outside near ties and its renormalised weights."""
+    from test_gpu_parity import check_route, run_route
+    base = dataclasses.replace(synth.CONFIGS["tiny"], E=32) if name == "tiny_e32" else synth.CONFIGS[name]
+    d = synth.with_tokens(base, T)
+    hw = host_weights(d)
+    w = device_weights(d)
+    x = synth.make_x(d)
+    with dense_from(lm, 1 if regime == "tensor" else STREAM_ONLY):
+        got = run_route(lm, d, to_dev(x), w)
+        names = [lm.lmoe_last_launch_name(i) for i in range(lm.lmoe_last_launch_count())]
+    assert ("router_tc_gemm" in names) == (regime == "tensor"), names
+    check_route(orc, d, x, hw, got)

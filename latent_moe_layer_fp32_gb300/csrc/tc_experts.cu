@@ -7,7 +7,7 @@
 // with MXFP4 weights (OCP MX v1.0: E2M1 codes, one E8M0 scale per 32 K
 // elements) and bf16 activations, fp32 accumulation.
 //
-// One work item = one group of up to 256 rows of one expert (sorted
+// One work item = one group of up to 192 rows of one expert (sorted
 // positions p0 .. p0+n-1) x one 128-row tile of the expert's output features.
 // The weight tile is the MMA's A operand (M = 128), the group's activation
 // rows are B (N = n rounded up to 16), so ragged groups cost no padded rows
@@ -15,14 +15,17 @@
 //   warp 0      TMA: raw MXFP4 codes, 128 rows x 256 K per stage (16 KB per
 //               weight matrix), into a ring
 //   warp 1      TMA: activation rows (sorted order), 32-row boxes of 64 K
-//   warp 2      TMEM owner; one thread issues tcgen05.mma kind::f16
+//   warp 2      TMEM owner; one thread issues tcgen05.mma kind::f16 with A
+//               read from tensor memory and B from shared memory
 //   warps 3-10  dequantise codes to bf16 (E2M1 x 2^(s-127) is exact in
-//               bf16) in the 128-byte-swizzled K-major layout the MMA reads
+//               bf16); a thread owns one weight row, which is one TMEM lane,
+//               and stores its 64 K of a step with tcgen05.st, so the
+//               dequantised operand never passes through shared memory
 //   warps 11-14 epilogue: tcgen05.ld, SwiGLU -> h (gate/up), or y and the
 //               per-32-column sums of squares for post_expert_norm (down)
-// Gate/up runs the gate and the up tile against the same activation stage
-// into two TMEM accumulators (columns 0-255 and 256-511), so SwiGLU pairs
-// are lane-local; down double-buffers one accumulator.
+// Tensor memory (512 columns): accumulators of 192 columns (gate/up: gate at
+// 0, up at 192, so SwiGLU pairs are lane-local; down: two buffers), and from
+// column 384 the A stages, 32 columns (64 K of bf16) per weight matrix.
 #include <atomic>
 
 #include "common.cuh"
@@ -34,9 +37,12 @@ namespace lmoe {
 namespace {
 
 constexpr int kXM = 128;                 // weight rows per matrix tile (MMA M)
-constexpr int kXNmax = 256;              // activation rows per group (MMA N, max)
-constexpr int kXTile = kXM * 128;        // 16 KB: 128 rows x 128 B (codes of 256 K, or bf16 of 64 K)
-constexpr int kXBStage = kXNmax * 128;   // 32 KB: 256 activation rows x 64 K bf16
+constexpr int kXNmax = kTcExpertGroup;   // activation rows per group (MMA N, max): 192
+constexpr int kXTile = kXM * 128;        // 16 KB: 128 rows x 128 B of codes (256 K)
+constexpr int kXBStage = kXNmax * 128;   // 24 KB: 192 activation rows x 64 K bf16
+constexpr int kXAcc = 192;               // TMEM columns per accumulator
+constexpr int kXACol = 384;              // first TMEM column of the A stages
+static_assert(kXNmax <= kXAcc && kXNmax % 32 == 0, "group rows fit an accumulator");
 constexpr int kXBBox = 32 * 128;         // one 32-row activation box
 constexpr int kDqWarps = 8, kEpWarps = 4;
 constexpr int kXThreads = (3 + kDqWarps + kEpWarps) * 32;
@@ -45,17 +51,19 @@ template <int MODE>
 struct XCfg;
 template <>
 struct XCfg<0> {  // gate/up: two weight matrices per item, single accumulator pair
-  static constexpr int NMAT = 2, RAW = 2, AST = 2, BST = 3, NACC = 1;
+  static constexpr int NMAT = 2, RAW = 3, AST = 2, BST = 4, NACC = 1;
 };
 template <>
 struct XCfg<1> {  // down: one weight matrix, double-buffered accumulator
-  static constexpr int NMAT = 1, RAW = 4, AST = 3, BST = 3, NACC = 2;
+  static constexpr int NMAT = 1, RAW = 4, AST = 4, BST = 4, NACC = 2;
 };
+static_assert(kXACol + XCfg<0>::AST * XCfg<0>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
+static_assert(kXACol + XCfg<1>::AST * XCfg<1>::NMAT * 32 <= 512 && XCfg<1>::NACC * kXAcc <= kXACol, "TMEM columns");
 
 template <int MODE>
 constexpr int xring_bytes() {
   using C = XCfg<MODE>;
-  return C::RAW * C::NMAT * kXTile + C::AST * C::NMAT * kXTile + C::BST * kXBStage;
+  return C::RAW * C::NMAT * kXTile + C::BST * kXBStage;
 }
 template <int MODE>
 constexpr int xsmem_bytes() {
@@ -110,7 +118,7 @@ __device__ __forceinline__ void dq8(uint32_t w, const DqTable& t, uint32_t* o) {
 // Scales outside the exponent-add range (subnormal, overflowing or NaN
 // results): the value in fp32, then bf16 (exact: every finite product is
 // representable in bf16).
-__device__ __noinline__ void dq_block_exact(uint4 c, uint32_t s, uint32_t* o) {
+__device__ __forceinline__ void dq_block_exact(uint4 c, uint32_t s, uint32_t* o) {
   const float sc = e8m0_to_f32(s);
   const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -139,10 +147,6 @@ __device__ __forceinline__ void dq_block(uint4 c, uint32_t s, uint32_t* o) {
   } else {
     dq_block_exact(c, s, o);
   }
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 }  // namespace
@@ -174,8 +178,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_raw = smem;                                   // [RAW][NMAT] code tiles
-  uint8_t* s_a = s_raw + C::RAW * C::NMAT * kXTile;        // [AST][NMAT] bf16 weight tiles
-  uint8_t* s_b = s_a + C::AST * C::NMAT * kXTile;          // [BST] activation stages
+  uint8_t* s_b = s_raw + C::RAW * C::NMAT * kXTile;        // [BST] activation stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_b + C::BST * kXBStage);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + C::RAW;
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(kXM, (x.n + 15) & ~15);
         if (!mbar_wait(&acc_empty[acc], cph ^ 1, a.st, 65)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (MODE == 0 ? 0u : (uint32_t)acc * 256u);
+        const uint32_t d = tmem + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(&a_full[as], aph, a.st, 66) || !mbar_wait(&b_full[bs], bph, a.st, 67)) {
             ok = false;
@@ -315,12 +318,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
           }
           tc_fence_after();
           const uint32_t b0 = smem_u32(s_b + bs * kXBStage);
+          const uint32_t a0 = tmem + kXACol + (uint32_t)(as * C::NMAT) * 32u;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
             for (int m = 0; m < C::NMAT; ++m)
-              tc_mma_bf16(d + m * 256u, smem_desc_sw128(smem_u32(s_a + (as * C::NMAT + m) * kXTile) + kk * 32),
-                          smem_desc_sw128(b0 + kk * 32), idesc, (ks | kk) != 0);
+              tc_mma_bf16_ts(d + m * kXAcc, a0 + m * 32u + kk * 8u, smem_desc_sw128(b0 + kk * 32), idesc,
+                             (ks | kk) != 0);
           tc_commit(&a_empty[as]);
           tc_commit(&b_empty[bs]);
           if (++as == C::AST) {
@@ -343,15 +347,18 @@ __global__ void __launch_bounds__(kXThreads, 1)
       mbar_wait(done, 0, a.st, 68);
     }
   } else if (warp < 3 + kDqWarps) {
-    // ---------------- dequantisation: codes -> bf16 weight tiles ----------------
-    // gate/up: thread -> one row of the gate (0-127) or up (128-255) tile, both
-    // 32-blocks of each 64-K step; down: thread -> one 32-block of one row.
-    const int dq = threadIdx.x - 96;
-    const int m = MODE == 0 ? dq >> 7 : 0;
-    const int rr = dq & 127;
-    const int b_first = MODE == 0 ? 0 : dq >> 7;
-    constexpr int NB = MODE == 0 ? 2 : 1;
+    // ---------------- dequantisation: codes -> bf16 A stages in TMEM ----------------
+    // A warp may only touch the TMEM lanes of its quarter (warp % 4): warp w
+    // handles rows 32 (w % 4) .. +31.  Gate/up: warps 3-6 the gate tile, 7-10 the
+    // up tile, both 32-blocks of each 64-K step; down: warps 3-6 the first and
+    // 7-10 the second 32-block of each step.
+    const int dw = warp - 3, q = warp & 3;
+    const int m = MODE == 0 ? dw >> 2 : 0;
+    const int b_only = MODE == 0 ? 0 : dw >> 2;
+    const int rr = q * 32 + lane;
     const int sw = rr & 7;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    constexpr int NB = MODE == 0 ? 2 : 1;
     int rs = 0, as = 0;
     uint32_t rph = 0, aph = 0;
     bool ok = true;
@@ -360,8 +367,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (!x_item(a, it, nft, &x)) continue;
       const size_t grow = (size_t)x.e * rows_pe + (size_t)m * a.inter + (size_t)x.ft * kXM + rr;
       const uint8_t* srow = a.s + grow * (size_t)(K / 32);
+      uint2 sc_next = __ldg(reinterpret_cast<const uint2*>(srow));
       for (int kr = 0; kr < nkr && ok; ++kr) {
-        const uint2 sc8 = __ldg(reinterpret_cast<const uint2*>(srow + kr * 8));
+        const uint2 sc8 = sc_next;  // this stage's 8 scale bytes, loaded one stage ahead
+        if (kr + 1 < nkr) sc_next = __ldg(reinterpret_cast<const uint2*>(srow + (kr + 1) * 8));
         if (!mbar_wait(&raw_full[rs], rph, a.st, 70)) {
           ok = false;
           break;
@@ -369,25 +378,27 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint8_t* rawt = s_raw + (rs * C::NMAT + m) * kXTile + rr * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          uint32_t o[16 * NB];
+#pragma unroll
+          for (int bi = 0; bi < NB; ++bi) {
+            const int b = MODE == 0 ? bi : b_only;
+            const int kb = 2 * j + b;  // 32-block within the raw stage
+            const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
+            const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
+            dq_block(c, (sword >> (8 * (kb & 3))) & 0xFFu, o + 16 * bi);
+          }
           if (!mbar_wait(&a_empty[as], aph ^ 1, a.st, 71)) {
             ok = false;
             break;
           }
-          uint8_t* at = s_a + (as * C::NMAT + m) * kXTile + rr * 128;
-#pragma unroll
-          for (int bi = 0; bi < NB; ++bi) {
-            const int b = MODE == 0 ? bi : b_first;
-            const int kb = 2 * j + b;  // 32-block within the raw stage
-            const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
-            const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
-            uint32_t o[16];
-            dq_block(c, (sword >> (8 * (kb & 3))) & 0xFFu, o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(at + (((4 * b + q) ^ sw) << 4)) =
-                  make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
-          fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+          tc_fence_after();
+          const uint32_t acol = tmem + lane_base + kXACol + (uint32_t)(as * C::NMAT + m) * 32u;
+          if (MODE == 0)
+            tmem_st32(acol, o);
+          else
+            tmem_st16(acol + 16u * b_only, o);
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[as]);
           if (++as == C::AST) {
@@ -414,12 +425,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (!mbar_wait(&acc_full[acc], cph, a.st, 72)) break;
       tc_fence_after();
       const int f = x.ft * kXM + q * 32 + lane;  // output feature of this lane
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 0 ? 0u : (uint32_t)acc * 256u);
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
       for (int c0 = 0; c0 < x.n; c0 += 32) {
         if (MODE == 0) {
           uint32_t g[32], u[32];
           tmem_ld32(tb + c0, g);
-          tmem_ld32(tb + 256 + c0, u);
+          tmem_ld32(tb + kXAcc + c0, u);
           tmem_ld_wait();
           uint16_t* hp = a.h_out + (size_t)(x.p0 + c0) * a.inter + f;
 #pragma unroll

@@ -92,6 +92,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Status
   }
 }
 
+// Same for a waiter that is not on the critical path (it waits for a whole
+// work item): sleeps `ns` between polls so it does not take issue slots.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, Status* st, int where, uint32_t ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer();
+  for (;;) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      set_error(st, LMOE_ETIMEOUT, where);
+      return false;
+    }
+  }
+}
+
 // TMA bulk copy global -> shared, completion counted on `bar` (bytes).
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -92,7 +92,7 @@ struct TcExpertArgs {
 };
 int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream_t s, int num_sms);
 int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms);
-constexpr int kTcExpertGroup = 192;
+constexpr int kTcExpertGroup = 160;
 __global__ void gather_rows_kernel(const uint16_t* x_lat, const int32_t* sorted_rows, int R, int k, int L,
                                    uint16_t* x_sorted);
 __global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out);

@@ -7,11 +7,11 @@
 // with MXFP4 weights (OCP MX v1.0: E2M1 codes, one E8M0 scale per 32 K
 // elements) and bf16 activations, fp32 accumulation.
 //
-// One work item = one group of up to 192 rows of one expert (sorted
+// One work item = one group of up to 160 rows of one expert (sorted
 // positions p0 .. p0+n-1) x one 128-row tile of the expert's output features.
 // The weight tile is the MMA's A operand (M = 128), the group's activation
 // rows are B (N = n rounded up to 16), so ragged groups cost no padded rows
-// of A.  Per CTA (persistent, one per SM, 15 warps):
+// of A.  Per CTA (persistent, one per SM, 19 warps):
 //   warp 0      TMA: raw MXFP4 codes, 128 rows x 256 K per stage (16 KB per
 //               weight matrix), into a ring
 //   warp 1      TMA: activation rows (sorted order), 32-row boxes of 64 K
@@ -21,11 +21,12 @@
 //               bf16); a thread owns one weight row, which is one TMEM lane,
 //               and stores its 64 K of a step with tcgen05.st, so the
 //               dequantised operand never passes through shared memory
-//   warps 11-14 epilogue: tcgen05.ld, SwiGLU -> h (gate/up), or y and the
-//               per-32-column sums of squares for post_expert_norm (down)
-// Tensor memory (512 columns): accumulators of 192 columns (gate/up: gate at
-// 0, up at 192, so SwiGLU pairs are lane-local; down: two buffers), and from
-// column 384 the A stages, 32 columns (64 K of bf16) per weight matrix.
+//   warps 11-18 epilogue: tcgen05.ld, SwiGLU -> h (gate/up), or y and the
+//               per-32-column sums of squares for post_expert_norm (down);
+//               two warps per TMEM lane quarter take alternate 32-column chunks
+// Tensor memory (512 columns): accumulators of 160 columns (gate/up: gate at
+// 0, up at 160, so SwiGLU pairs are lane-local; down: two buffers), and from
+// column 320 the A stages, 32 columns (64 K of bf16) per weight matrix.
 #include <atomic>
 
 #include "common.cuh"
@@ -37,33 +38,33 @@ namespace lmoe {
 namespace {
 
 constexpr int kXM = 128;                 // weight rows per matrix tile (MMA M)
-constexpr int kXNmax = kTcExpertGroup;   // activation rows per group (MMA N, max): 192
+constexpr int kXNmax = kTcExpertGroup;   // activation rows per group (MMA N, max): 160
 constexpr int kXTile = kXM * 128;        // 16 KB: 128 rows x 128 B of codes (256 K)
-constexpr int kXBStage = kXNmax * 128;   // 24 KB: 192 activation rows x 64 K bf16
-constexpr int kXAcc = 192;               // TMEM columns per accumulator
-constexpr int kXACol = 384;              // first TMEM column of the A stages
+constexpr int kXBStage = kXNmax * 128;   // 20 KB: 160 activation rows x 64 K bf16
+constexpr int kXAcc = 160;               // TMEM columns per accumulator
+constexpr int kXACol = 320;              // first TMEM column of the A stages
 static_assert(kXNmax <= kXAcc && kXNmax % 32 == 0, "group rows fit an accumulator");
 constexpr int kXBBox = 32 * 128;         // one 32-row activation box
-constexpr int kDqWarps = 8, kEpWarps = 4;
+constexpr int kDqWarps = 8, kEpWarps = 8;
 constexpr int kXThreads = (3 + kDqWarps + kEpWarps) * 32;
 
 template <int MODE>
 struct XCfg;
 template <>
 struct XCfg<0> {  // gate/up: two weight matrices per item, single accumulator pair
-  static constexpr int NMAT = 2, RAW = 3, AST = 2, BST = 4, NACC = 1;
+  static constexpr int NMAT = 2, RAW = 3, ST = 3, NACC = 1;
 };
 template <>
 struct XCfg<1> {  // down: one weight matrix, double-buffered accumulator
-  static constexpr int NMAT = 1, RAW = 4, AST = 4, BST = 4, NACC = 2;
+  static constexpr int NMAT = 1, RAW = 4, ST = 6, NACC = 2;
 };
-static_assert(kXACol + XCfg<0>::AST * XCfg<0>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
-static_assert(kXACol + XCfg<1>::AST * XCfg<1>::NMAT * 32 <= 512 && XCfg<1>::NACC * kXAcc <= kXACol, "TMEM columns");
+static_assert(kXACol + XCfg<0>::ST * XCfg<0>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
+static_assert(kXACol + XCfg<1>::ST * XCfg<1>::NMAT * 32 <= 512 && XCfg<1>::NACC * kXAcc <= kXACol, "TMEM columns");
 
 template <int MODE>
 constexpr int xring_bytes() {
   using C = XCfg<MODE>;
-  return C::RAW * C::NMAT * kXTile + C::BST * kXBStage;
+  return C::RAW * C::NMAT * kXTile + C::ST * kXBStage;
 }
 template <int MODE>
 constexpr int xsmem_bytes() {
@@ -100,7 +101,7 @@ __device__ __forceinline__ DqTable dq_table(uint32_t s) {
 // Eight codes (one word, element i in nibble i) -> four bf16x2 words.
 __device__ __forceinline__ void dq8(uint32_t w, const DqTable& t, uint32_t* o) {
   const uint32_t mags = w & 0x77777777u;
-  const uint32_t w4 = w << 4;
+  const uint32_t w4 = w * 16u;  // multiply forms of the shifts run on the FMA pipe, not the integer ALU
   // byte i of sa / sb carries the sign of element i / 4+i in its top bit
   const uint32_t sa = __byte_perm(w4, w, 0x5140);
   const uint32_t sb = __byte_perm(w4, w, 0x7362);
@@ -108,7 +109,7 @@ __device__ __forceinline__ void dq8(uint32_t w, const DqTable& t, uint32_t* o) {
   uint32_t hi = __byte_perm(t.ha, t.hb, mags) | (sa & 0x80808080u);
   o[0] = __byte_perm(lo, hi, 0x5140);
   o[1] = __byte_perm(lo, hi, 0x7362);
-  const uint32_t mh = mags >> 16;
+  const uint32_t mh = __umulhi(mags, 0x10000u);  // mags >> 16
   lo = __byte_perm(t.la, t.lb, mh);
   hi = __byte_perm(t.ha, t.hb, mh) | (sb & 0x80808080u);
   o[2] = __byte_perm(lo, hi, 0x5140);
@@ -136,9 +137,10 @@ __device__ __forceinline__ void dq_block_exact(uint4 c, uint32_t s, uint32_t* o)
   }
 }
 
-// 32 codes (16 bytes) with scale byte s -> 32 bf16 (16 words).
-__device__ __forceinline__ void dq_block(uint4 c, uint32_t s, uint32_t* o) {
-  if (s >= 2u && s <= 252u) {
+// 32 codes (16 bytes) with scale byte s -> 32 bf16 (16 words).  `fast`: the
+// caller has checked 2 <= s <= 252.
+__device__ __forceinline__ void dq_block(uint4 c, uint32_t s, uint32_t* o, bool fast) {
+  if (fast) {
     const DqTable t = dq_table(s);
     dq8(c.x, t, o);
     dq8(c.y, t, o + 4);
@@ -178,15 +180,16 @@ __global__ void __launch_bounds__(kXThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_raw = smem;                                   // [RAW][NMAT] code tiles
-  uint8_t* s_b = s_raw + C::RAW * C::NMAT * kXTile;        // [BST] activation stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_b + C::BST * kXBStage);
+  uint8_t* s_b = s_raw + C::RAW * C::NMAT * kXTile;        // [ST] activation stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_b + C::ST * kXBStage);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + C::RAW;
-  uint64_t* a_full = raw_empty + C::RAW;
-  uint64_t* a_empty = a_full + C::AST;
-  uint64_t* b_full = a_empty + C::AST;
-  uint64_t* b_empty = b_full + C::BST;
-  uint64_t* acc_full = b_empty + C::BST;
+  // step stage s: A (TMEM columns) and B (shared memory) of one 64-K step.
+  // full[s]: the dequant warps' arrivals + the activation TMA's arrival and
+  // bytes; empty[s]: one MMA commit frees both halves.
+  uint64_t* full = raw_empty + C::RAW;
+  uint64_t* empty = full + C::ST;
+  uint64_t* acc_full = empty + C::ST;
   uint64_t* acc_empty = acc_full + C::NACC;
   uint64_t* done = acc_empty + C::NACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -197,13 +200,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kDqWarps);
     }
-    for (int i = 0; i < C::AST; ++i) {
-      mbar_init(&a_full[i], kDqWarps);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < C::BST; ++i) {
-      mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+    for (int i = 0; i < C::ST; ++i) {
+      mbar_init(&full[i], kDqWarps + 1);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -273,36 +272,36 @@ __global__ void __launch_bounds__(kXThreads, 1)
       const int nb = (x.n + 31) >> 5;
       for (int ks = 0; ks < nks; ++ks) {
         int good = 1;
-        if (lane == 0) good = mbar_wait(&b_empty[bs], bph ^ 1, a.st, 63);
+        if (lane == 0) good = mbar_wait(&empty[bs], bph ^ 1, a.st, 63);
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&b_full[bs], nb * kXBBox);
+        if (lane == 0) mbar_arrive_expect_tx(&full[bs], nb * kXBBox);
         __syncwarp();
         if (lane < nb)
-          tma_load_2d(s_b + bs * kXBStage + lane * kXBBox, &tm_act, ks * 64, x.p0 + lane * 32, &b_full[bs], pol);
+          tma_load_2d(s_b + bs * kXBStage + lane * kXBBox, &tm_act, ks * 64, x.p0 + lane * 32, &full[bs], pol);
         ++issued;
-        if (++bs == C::BST) {
+        if (++bs == C::ST) {
           bs = 0;
           bph ^= 1;
         }
       }
     }
-    if (lane == 0)
-      for (int i = 0; i < C::BST && i < issued; ++i) {
+    if (lane == 0)  // the last copies land before exit (the stages' empty commits follow them)
+      for (int i = 0; i < C::ST && i < issued; ++i) {
         if (--bs < 0) {
-          bs = C::BST - 1;
+          bs = C::ST - 1;
           bph ^= 1;
         }
-        mbar_wait(&b_full[bs], bph, a.st, 64);
+        mbar_wait(&empty[bs], bph, a.st, 64);
       }
   } else if (warp == 2) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      int as = 0, bs = 0, acc = 0;
-      uint32_t aph = 0, bph = 0, cph = 0;
+      int as = 0, acc = 0;
+      uint32_t aph = 0, cph = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         XItem x;
@@ -312,12 +311,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
         for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait(&a_full[as], aph, a.st, 66) || !mbar_wait(&b_full[bs], bph, a.st, 67)) {
+          if (!mbar_wait(&full[as], aph, a.st, 66)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = smem_u32(s_b + bs * kXBStage);
+          const uint32_t b0 = smem_u32(s_b + as * kXBStage);
           const uint32_t a0 = tmem + kXACol + (uint32_t)(as * C::NMAT) * 32u;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -325,15 +324,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
             for (int m = 0; m < C::NMAT; ++m)
               tc_mma_bf16_ts(d + m * kXAcc, a0 + m * 32u + kk * 8u, smem_desc_sw128(b0 + kk * 32), idesc,
                              (ks | kk) != 0);
-          tc_commit(&a_empty[as]);
-          tc_commit(&b_empty[bs]);
-          if (++as == C::AST) {
+          tc_commit(&empty[as]);
+          if (++as == C::ST) {
             as = 0;
             aph ^= 1;
-          }
-          if (++bs == C::BST) {
-            bs = 0;
-            bph ^= 1;
           }
         }
         if (!ok) break;
@@ -362,6 +356,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
     int rs = 0, as = 0;
     uint32_t rph = 0, aph = 0;
     bool ok = true;
+    // the TMEM store of a step completes while the next step is dequantised:
+    // its full[] arrival is deferred until then (pend_as = its stage, or -1)
+    int pend_as = -1;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       XItem x;
       if (!x_item(a, it, nft, &x)) continue;
@@ -371,6 +368,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
       for (int kr = 0; kr < nkr && ok; ++kr) {
         const uint2 sc8 = sc_next;  // this stage's 8 scale bytes, loaded one stage ahead
         if (kr + 1 < nkr) sc_next = __ldg(reinterpret_cast<const uint2*>(srow + (kr + 1) * 8));
+        // all eight in the exponent-add range [2, 252]: bytewise (s - 2) <= 250
+        const bool fast = (__vcmpleu4(__vsub4(sc8.x, 0x02020202u), 0xFAFAFAFAu) &
+                           __vcmpleu4(__vsub4(sc8.y, 0x02020202u), 0xFAFAFAFAu)) == 0xFFFFFFFFu;
         if (!mbar_wait(&raw_full[rs], rph, a.st, 70)) {
           ok = false;
           break;
@@ -385,10 +385,18 @@ __global__ void __launch_bounds__(kXThreads, 1)
             const int kb = 2 * j + b;  // 32-block within the raw stage
             const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
             const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
-            dq_block(c, (sword >> (8 * (kb & 3))) & 0xFFu, o + 16 * bi);
+            const uint32_t sb = (sword >> (8 * (kb & 3))) & 0xFFu;
+            dq_block(c, sb, o + 16 * bi, fast || (sb >= 2u && sb <= 252u));
           }
-          if (!mbar_wait(&a_empty[as], aph ^ 1, a.st, 71)) {
+          if (pend_as >= 0) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[pend_as]);
+          }
+          if (!mbar_wait(&empty[as], aph ^ 1, a.st, 71)) {
             ok = false;
+            pend_as = -1;
             break;
           }
           tc_fence_after();
@@ -397,11 +405,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
             tmem_st32(acol, o);
           else
             tmem_st16(acol + 16u * b_only, o);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[as]);
-          if (++as == C::AST) {
+          pend_as = as;
+          if (++as == C::ST) {
             as = 0;
             aph ^= 1;
           }
@@ -414,19 +419,26 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
       }
     }
+    if (pend_as >= 0) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[pend_as]);
+    }
   } else {
     // ---------------- epilogue: TMEM -> h (gate/up) or y, ssq (down) ----------------
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int q = warp & 3;                      // TMEM lane quarter this warp may read
+    const int half = (warp - 3 - kDqWarps) >> 2;  // which alternate 32-column chunks
     int acc = 0;
     uint32_t cph = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       XItem x;
       if (!x_item(a, it, nft, &x)) continue;
-      if (!mbar_wait(&acc_full[acc], cph, a.st, 72)) break;
+      if (!mbar_wait_sleep(&acc_full[acc], cph, a.st, 72, 256)) break;
       tc_fence_after();
       const int f = x.ft * kXM + q * 32 + lane;  // output feature of this lane
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
-      for (int c0 = 0; c0 < x.n; c0 += 32) {
+      for (int c0 = 32 * half; c0 < x.n; c0 += 64) {
         if (MODE == 0) {
           uint32_t g[32], u[32];
           tmem_ld32(tb + c0, g);
@@ -557,7 +569,7 @@ __global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* sca
   if (b >= nblocks) return;
   const uint4 c = *reinterpret_cast<const uint4*>(codes + 16 * (size_t)b);
   uint32_t o[16];
-  dq_block(c, scales[b], o);
+  dq_block(c, scales[b], o, scales[b] >= 2 && scales[b] <= 252);
   uint4* dst = reinterpret_cast<uint4*>(out + 32 * (size_t)b);
 #pragma unroll
   for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);

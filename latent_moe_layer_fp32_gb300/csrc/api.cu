@@ -15,14 +15,22 @@ constexpr int kDenseMinTokensDefault = 64;
 constexpr int kExpertTcMinTokensDefault = 512;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
+// the options as read once at the start of the current call on this thread, so
+// that every decision inside one call sees the same regime
+thread_local int t_dense_min_t = kDenseMinTokensDefault;
+thread_local int t_expert_tc_min_t = kExpertTcMinTokensDefault;
+void snapshot_options() {
+  t_dense_min_t = g_dense_min_t.load(std::memory_order_relaxed);
+  t_expert_tc_min_t = g_expert_tc_min_t.load(std::memory_order_relaxed);
+}
 
 // the router as a tensor-core GEMM: above the fused small-T routing, from the
 // dense-projection threshold on, for expert counts that fill whole 32-column chunks
 bool router_tc(const lmoe_dims* d) {
-  return d->T > 16 && d->T >= g_dense_min_t.load(std::memory_order_relaxed) && d->n_experts % 32 == 0;
+  return d->T > 16 && d->T >= t_dense_min_t && d->n_experts % 32 == 0;
 }
 
-bool experts_tc(int T) { return T >= g_expert_tc_min_t.load(std::memory_order_relaxed); }
+bool experts_tc(int T) { return T >= t_expert_tc_min_t; }
 // rows per group of the routing table: what the expert kernels of this regime consume
 int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
 
@@ -167,6 +175,7 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttr
 int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayout* w, cudaStream_t s,
              bool need_ws = true) {
   g_launches = 0;
+  snapshot_options();
   CHECK(check_dims(d));
   CHECK(dev_info(di));
   CHECK(layout(d, di->sms, w));
@@ -226,12 +235,20 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   return LMOE_OK;
 }
 
+// x_sorted: when set (tensor-core pooler only), x_lat rows are also written in
+// expert-sorted order (row_pos = each route row's sorted position)
 int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
-             uint32_t* xmax, Status* st, cudaStream_t s) {
-  const bool dense = d->T >= g_dense_min_t.load(std::memory_order_relaxed);
+             uint32_t* xmax, Status* st, cudaStream_t s, const int32_t* row_pos = nullptr,
+             uint16_t* x_sorted = nullptr) {
+  const bool dense = x_sorted != nullptr || d->T >= t_dense_min_t;
   pre_launch(s, dense ? "pool_tc_gemm" : "pool_gemv");
   if (dense) {
     TcGemmArgs g{x_lat, xmax, d->T, d->latent, d->hidden, st};
+    if (x_sorted) {
+      g.scatter_pos = row_pos;
+      g.scatter_k = d->top_k;
+      g.scatter_out = x_sorted;
+    }
     CHECK(launch_tc_gemm_bf16(g, x, pooler_w, s, di.sms));
   } else {
     GemvArgs g{pooler_w, x, x_lat, xmax, d->latent, d->hidden, d->T, st};
@@ -244,13 +261,13 @@ int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uin
 // groups must already be in the workspace; xmax must hold each token's max |x_lat|
 int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
                 const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
-                const uint8_t* w2_s, float* y, void* ws, cudaStream_t s) {
+                const uint8_t* w2_s, float* y, void* ws, cudaStream_t s, bool xs_ready = false) {
   const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
   if (experts_tc(T)) {
     const int R = T * k;
     uint16_t* xs = at<uint16_t>(ws, w.xs);
-    LAUNCH(dim3((R + 7) / 8), dim3(256), s, gather_rows_kernel, x_lat, sorted_rows, R, k, L, xs);
+    if (!xs_ready) LAUNCH(dim3((R + 7) / 8), dim3(256), s, gather_rows_kernel, x_lat, sorted_rows, R, k, L, xs);
     TcExpertArgs t{};
     t.groups = at<int4>(ws, w.groups);
     t.n_groups = at<int32_t>(ws, w.n_groups);
@@ -323,9 +340,11 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
     LAUNCH(dim3((unsigned)((n + 7) / 8)), dim3(256), s, ssq_kernel, y, d->T * d->top_k, d->latent,
            at<float>(ws, w.ssq));
   }
-  LAUNCH(dim3(d->T, (d->latent + 255) / 256), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
+  int csplit = 1;  // column splits per token: enough CTAs for the GPU at small T
+  while (csplit < d->latent / 256 && d->T * csplit < 2 * di.sms) csplit *= 2;
+  LAUNCH(dim3(d->T, csplit), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
          topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts, d->eps, zb, st);
-  const bool dense = d->T >= g_dense_min_t.load(std::memory_order_relaxed);
+  const bool dense = d->T >= t_dense_min_t;
   pre_launch(s, dense ? "unpool_tc_gemm" : "unpool_gemv");
   if (dense) {
     TcGemmArgs g{out, nullptr, d->T, d->hidden, d->latent, st};
@@ -435,8 +454,12 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   Status* st = at<Status>(ws, w.pub.status);
   CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets), srows,
                   at<int32_t>(ws, w.pub.row_pos), ws, s));
-  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, at<uint32_t>(ws, w.xmax), st, s));
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s));
+  // with both the pooler and the experts on the tensor cores, the pooler's epilogue
+  // also writes x_lat in expert-sorted order (no separate gather)
+  const bool scatter = experts_tc(d->T) && d->T >= t_dense_min_t;
+  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, at<uint32_t>(ws, w.xmax), st, s,
+                 scatter ? at<int32_t>(ws, w.pub.row_pos) : nullptr, scatter ? at<uint16_t>(ws, w.xs) : nullptr));
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, scatter));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);
 }

@@ -70,6 +70,11 @@ struct TcGemmArgs {
   int a_kblocks;        // > 0: A's 64-wide k-block index wraps modulo this (A reused along K)
   int n_tile;           // output columns per tile: 256 (0), or a multiple of 32 below it
   int nsplit;           // K split into this many ranges, one partial each (0 or 1: none)
+  // optional (bf16 output only): also write output row m to rows scatter_pos[m*scatter_k + j]
+  // (j < scatter_k) of scatter_out [*][N] -- x_lat rows in expert-sorted order for the experts
+  const int32_t* scatter_pos;
+  int scatter_k;
+  uint16_t* scatter_out;
 };
 int launch_tc_gemm_bf16(const TcGemmArgs& a, const uint16_t* A, const uint16_t* B, cudaStream_t s, int num_sms);
 constexpr int kTcGemmN = 256, kTcGemmK = 64;

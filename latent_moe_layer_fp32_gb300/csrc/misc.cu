@@ -96,7 +96,10 @@ __global__ void __launch_bounds__(256) ssq_kernel(const float* __restrict__ y, i
 //   ss_j  = sum over the row's 32-column tiles of ssq (fixed order)
 //   rinv  = 1 / sqrt(ss_j / L + eps)
 //   z[l]  = sum_j w[t][j] * ((y * rinv) * g[e_j][l]),  zb = bf16(z)
-// (each CTA recomputes the k factors rinv for its token: k x L/32 partials)
+// Grid (T, S): CTA (t, c) takes columns [c L/S, (c+1) L/S) of token t, four
+// consecutive columns per thread and step (16-byte loads of y); S > 1 only
+// when T alone would leave SMs idle.  Each CTA recomputes the k factors rinv of
+// its token from the k x L/32 partials.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ssq,
                                                       const int32_t* __restrict__ topk_idx,
                                                       const float* __restrict__ topk_w,
@@ -126,16 +129,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
   }
   __syncthreads();
-  {
-    const int l = blockIdx.y * 256 + tid;
-    if (l >= L) return;
-    float z = 0.f;
+  const int span = L / gridDim.y, c_end = (blockIdx.y + 1) * span;
+  for (int l = blockIdx.y * span + 4 * tid; l < c_end; l += 4 * 256) {
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
-      const float yv = y[((size_t)t * k + j) * L + l];
-      const float yh = __fmul_rn(__fmul_rn(yv, s_rinv[j]), bf16_bits_to_f32(norm_g[(size_t)s_e[j] * L + l]));
-      z = __fadd_rn(z, __fmul_rn(s_w[j], yh));
+      const float4 yv = __ldcs(reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * L + l));
+      const uint2 gw = *reinterpret_cast<const uint2*>(norm_g + (size_t)s_e[j] * L + l);
+      const float yy[4] = {yv.x, yv.y, yv.z, yv.w};
+      const float gg[4] = {bf16_bits_to_f32(gw.x & 0xFFFFu), bf16_bits_to_f32(gw.x >> 16),
+                           bf16_bits_to_f32(gw.y & 0xFFFFu), bf16_bits_to_f32(gw.y >> 16)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float yh = __fmul_rn(__fmul_rn(yy[q], s_rinv[j]), gg[q]);
+        z[q] = __fadd_rn(z[q], __fmul_rn(s_w[j], yh));
+      }
     }
-    zb[(size_t)t * L + l] = f32_to_bf16_bits(z);
+    uint2 out;
+    out.x = (uint32_t)f32_to_bf16_bits(z[0]) | ((uint32_t)f32_to_bf16_bits(z[1]) << 16);
+    out.y = (uint32_t)f32_to_bf16_bits(z[2]) | ((uint32_t)f32_to_bf16_bits(z[3]) << 16);
+    *reinterpret_cast<uint2*>(zb + (size_t)t * L + l) = out;
   }
 }
 

@@ -159,8 +159,12 @@ struct XItem {
   int e, p0, n, ft;
 };
 
-__device__ __forceinline__ bool x_item(const TcExpertArgs& a, int it, int nft, XItem* x) {
-  const int4 g = a.groups[it / nft];
+// Group entry of item `it` (loaded one item ahead by every role).
+__device__ __forceinline__ int4 x_group(const TcExpertArgs& a, int it, int nft, int n_items) {
+  return it < n_items ? __ldg(&a.groups[it / nft]) : make_int4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ bool x_item(const TcExpertArgs& a, int4 g, int it, int nft, XItem* x) {
   x->e = g.x;
   x->p0 = g.y;
   x->n = g.z;
@@ -232,9 +236,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
       int rs = 0, issued = 0;
       uint32_t rph = 0;
       bool ok = true;
+      int4 g_next = x_group(a, blockIdx.x, nft, n_items);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 g_cur = g_next;
+        g_next = x_group(a, it + gridDim.x, nft, n_items);
         XItem x;
-        if (!x_item(a, it, nft, &x)) continue;
+        if (!x_item(a, g_cur, it, nft, &x)) continue;
         for (int kr = 0; kr < nkr; ++kr) {
           if (!mbar_wait(&raw_empty[rs], rph ^ 1, a.st, 61)) {
             ok = false;
@@ -266,9 +273,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
     int bs = 0, issued = 0;
     uint32_t bph = 0;
     bool ok = true;
+    int4 g_next = x_group(a, blockIdx.x, nft, n_items);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int4 g_cur = g_next;
+      g_next = x_group(a, it + gridDim.x, nft, n_items);
       XItem x;
-      if (!x_item(a, it, nft, &x)) continue;
+      if (!x_item(a, g_cur, it, nft, &x)) continue;
       const int nb = (x.n + 31) >> 5;
       for (int ks = 0; ks < nks; ++ks) {
         int good = 1;
@@ -303,9 +313,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
       int as = 0, acc = 0;
       uint32_t aph = 0, cph = 0;
       bool ok = true;
+      int4 g_next = x_group(a, blockIdx.x, nft, n_items);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 g_cur = g_next;
+        g_next = x_group(a, it + gridDim.x, nft, n_items);
         XItem x;
-        if (!x_item(a, it, nft, &x)) continue;
+        if (!x_item(a, g_cur, it, nft, &x)) continue;
         const uint32_t idesc = idesc_bf16_f32(kXM, (x.n + 15) & ~15);
         if (!mbar_wait(&acc_empty[acc], cph ^ 1, a.st, 65)) break;
         tc_fence_after();
@@ -359,9 +372,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
     // the TMEM store of a step completes while the next step is dequantised:
     // its full[] arrival is deferred until then (pend_as = its stage, or -1)
     int pend_as = -1;
+    int4 g_next = x_group(a, blockIdx.x, nft, n_items);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int4 g_cur = g_next;
+      g_next = x_group(a, it + gridDim.x, nft, n_items);
       XItem x;
-      if (!x_item(a, it, nft, &x)) continue;
+      if (!x_item(a, g_cur, it, nft, &x)) continue;
       const size_t grow = (size_t)x.e * rows_pe + (size_t)m * a.inter + (size_t)x.ft * kXM + rr;
       const uint8_t* srow = a.s + grow * (size_t)(K / 32);
       uint2 sc_next = __ldg(reinterpret_cast<const uint2*>(srow));
@@ -431,9 +447,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const int half = (warp - 3 - kDqWarps) >> 2;  // which alternate 32-column chunks
     int acc = 0;
     uint32_t cph = 0;
+    int4 g_next = x_group(a, blockIdx.x, nft, n_items);
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const int4 g_cur = g_next;
+      g_next = x_group(a, it + gridDim.x, nft, n_items);
       XItem x;
-      if (!x_item(a, it, nft, &x)) continue;
+      if (!x_item(a, g_cur, it, nft, &x)) continue;
       if (!mbar_wait_sleep(&acc_full[acc], cph, a.st, 72, 256)) break;
       tc_fence_after();
       const int f = x.ft * kXM + q * 32 + lane;  // output feature of this lane
@@ -445,11 +464,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tmem_ld32(tb + kXAcc + c0, u);
           tmem_ld_wait();
           uint16_t* hp = a.h_out + (size_t)(x.p0 + c0) * a.inter + f;
+          // silu(g) * u with the fast exponential and reciprocal (relative error
+          // ~1e-6, far below the bf16 rounding of h that follows)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (c0 + i < x.n) {
               const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv / (1.0f + expf(-gv)) * uv);
+              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv * __frcp_rn(1.0f + __expf(-gv)) * uv);
             }
           }
         } else {

@@ -178,6 +178,12 @@ __global__ void __launch_bounds__(256, 1)
           uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)row * a.N + nt * n_tile + ch * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          for (int j = 0; j < a.scatter_k; ++j) {
+            const int p = __ldg(a.scatter_pos + (size_t)row * a.scatter_k + j);
+            uint4* sd = reinterpret_cast<uint4*>(a.scatter_out + (size_t)p * a.N + nt * n_tile + ch * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sd[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          }
         }
       }
       tc_fence_before();

@@ -34,7 +34,10 @@
  *  - Calls sharing one workspace must not overlap in time.
  *  - Constraints checked on the host: hidden, latent, inter multiples of 128;
  *    1 <= top_k <= 8; top_k <= n_experts <= 256; 1 <= T <= 65536; every
- *    pointer 16-byte aligned; a compute-capability 10.3 device.
+ *    pointer 16-byte aligned; a compute-capability 10.3 device (else
+ *    LMOE_EINVAL / LMOE_EUNSUPPORTED).  Supported shapes (else
+ *    LMOE_EUNSUPPORTED): hidden, latent, inter multiples of 256; latent and
+ *    inter at most 8192, and multiples of 2048 when above 2048.
  */
 #ifndef LMOE_H
 #define LMOE_H

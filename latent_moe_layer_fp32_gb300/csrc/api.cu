@@ -84,6 +84,8 @@ int check_dims(const lmoe_dims* d) {
   // projections in 256- or 512-element chunks
   if (d->hidden % 256 || d->latent % 256 || d->inter % 256) return LMOE_EUNSUPPORTED;
   if ((d->latent > 2048 && d->latent % 2048) || (d->inter > 2048 && d->inter % 2048)) return LMOE_EUNSUPPORTED;
+  // the decode expert kernels keep a group's activation rows (whole K) in shared memory
+  if (d->latent > 8192 || d->inter > 8192) return LMOE_EUNSUPPORTED;
   return LMOE_OK;
 }
 

@@ -11,24 +11,32 @@
 // two m16 tiles).  gate/up: 16 gate rows + the matching 16 up rows (an m16
 // tile pairs 8 gate rows with their 8 up rows, so SwiGLU is local to a lane);
 // down: 32 consecutive output rows.  Each item streams its rows once (all of
-// K) for every row of its group.
+// K) for every row of its group.  A CTA takes a contiguous range of items,
+// so consecutive items mostly share a group.
 //
-// CTA = W consumer warps + 1 producer warp.  Per K chunk the producer issues
-// two TMA tensor copies of the codes (16 rows x kc/2 bytes each, a 3-D view
-// {128 B, rows, K/256} with 128-byte swizzle, so each copy is one 16 KB
-// request and ldmatrix reads it without bank conflicts), two of the E8M0
-// scales and one bulk copy per activation row, into per-warp mbarrier rings
-// of D slots; consumer warp w takes items w, w+W, ... of the CTA's range.
+// CTA = Q consumer warps + 1 producer warp + 1 epilogue warp.
+//  - producer: per K chunk, two TMA tensor copies of the codes (16 rows x
+//    kc/2 bytes each, a 3-D view {128 B, rows, K/256} with 128-byte swizzle,
+//    so each copy is one 16 KB request and ldmatrix reads it without bank
+//    conflicts) and two of the E8M0 scales, into a ring of D slots.  When
+//    the group changes it loads the group's activation rows (bf16, whole K)
+//    into the activation panel, once the consumers released the old one.
+//  - consumers: convert a fresh panel once (bf16 -> f16 times a per-row power
+//    of two, exact; undone in the epilogue; the power comes from the row's
+//    max |value| that the producing kernel recorded), then share every slot,
+//    warp j taking the chunk's 128-byte planes j, j+Q, ...  They hand their
+//    fp32 partials to the epilogue warp through a double-buffered exchange
+//    and go straight on to the next item.
+//  - epilogue: adds the Q partials in warp order (fixed summation order) and
+//    finishes the item (SwiGLU -> h, or y plus its sums of squares).
+// Every wait is an mbarrier wait bounded in time.
 //
 // Consumer per 32-element scale block: ldmatrix.x4 hands each lane 4 code
 // bytes of two rows; cvt.rn.f16x2.e2m1x2 turns each byte into two exact f16
 // values; two mma.sync m16n8k16 (f16 in, fp32 accumulate) cover the block's
 // 32 K positions in a fixed permutation that the activation fragment follows;
 // the fresh block result is scaled by the block's E8M0 value (expanded once
-// per chunk into a per-warp fp32 table) and added to the fp32 accumulator.
-// Activations arrive as bf16 rows; each warp converts its plane's columns to
-// f16 times a per-row power of two (exact; undone in the epilogue), the power
-// coming from the row's max |value| that the producing kernel recorded.
+// per plane into a per-warp fp32 table) and added to the fp32 accumulator.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.cuh"
@@ -40,24 +48,30 @@ enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 constexpr int kRows = 32;  // weight rows per item: two m16 tiles
 constexpr int kKC = 2048;  // K elements per chunk when K > 2048 (else the whole K): 16 KB code boxes
 
-// Header the producer writes into the first slot of every item.
-struct ItemMeta {
+// Group header the producer writes next to the activation panel.
+struct PanelHdr {
   int p0, ntok, pad0, pad1;
   int aexp[8];  // per token of the group: power of two mapping its activation row into f16 range
   int rows[8];  // per token: sorted_rows[p0 + j] (the original route row id)
 };
-static_assert(sizeof(ItemMeta) <= 128, "item header");
 
-template <int G>
+// Item header a consumer passes to the epilogue warp with the partials.
+struct ItemHdr {
+  int p0, ntok, tile, pad;
+  int aexp[8];
+  int rows[8];
+};
+
+// One ring slot: codes and scales of a K chunk of one item.
 struct Layout {
   static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (16 KB)
   static constexpr int kCodes = 2 * kBox;      // box A (rows 0-15 of the item), box B (rows 16-31)
   static constexpr int kScales = kRows * (kKC / 32);
-  static constexpr int kActRow = kKC * 2 + 64;  // padded: conflict-free 16-byte loads
-  static constexpr int kActs = G * kActRow;
-  static constexpr int kMeta = 128;  // item header: p0, ntok, per-token exponent and row id
-  static constexpr int kSlot = (kCodes + kScales + kActs + kMeta + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
+  static constexpr int kSlot = (kCodes + kScales + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
 };
+
+constexpr int kMaxSlots = 8;
+constexpr int kMaxK = 8192;  // activation panel: up to G rows of this many elements
 
 // Expand the E8M0 bytes of one 128-byte plane (8 blocks; scale region
 // [32 rows][nb], blocks p*8 .. p*8+7) into fp32 2^(s-127) in the warp's table
@@ -137,36 +151,62 @@ __device__ __forceinline__ void plane_blocks(uint32_t sbase, uint32_t act_addr, 
   }
 }
 
-template <int MODE, int G, int NGRP, int Q, int D>
-__global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
-    expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s) {
-  // NGRP groups of Q consumer warps; group gi owns a ring of D slots and the
-  // CTA items gi, gi+NGRP, ...; its Q warps share every slot, member j taking
-  // the chunk's 128-byte planes j, j+Q, ...; the members' fp32 partials are
-  // added in member order at the end of each item.
-  using Lay = Layout<G>;
-  constexpr int NW = NGRP * Q;
-  constexpr int NV = (G == 1) ? 1 : 2;  // token columns per lane that can hold a valid token
-  constexpr int kRed = 2 * 2 * NV * 32;  // floats per member partial (two buffers, by item parity)
+
+// Shared-memory plan of one CTA (bytes), shared by the kernel and the launch.
+template <int G, int Q>
+struct Smem {
+  static constexpr int NV = (G == 1) ? 1 : 2;        // token columns per lane that can hold a valid token
+  static constexpr int kPart = 2 * 2 * NV * 32;      // floats per warp partial: [mtile][lo/hi][v][lane]
+  static __host__ __device__ int panel_row(int K) { return K * 2 + 64; }  // padded: conflict-free 16-byte loads
+  static __host__ __device__ int fixed(int K) {
+    return G * panel_row(K) + Q * 256 * 4 + 2 * Q * kPart * 4 + 2 * (int)sizeof(ItemHdr) + (int)sizeof(PanelHdr) +
+           (2 * kMaxSlots + 8) * 8;
+  }
+  static __host__ __device__ int bytes(int K, int D) { return D * Layout::kSlot + fixed(K) + 1024; }
+};
+
+template <int MODE, int G, int Q>
+__global__ void __launch_bounds__(32 * (Q + 2), 1)
+    expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
+                  int D) {
+  using Lay = Layout;
+  using SM = Smem<G, Q>;
+  constexpr int NV = SM::NV;
+  constexpr int kPart = SM::kPart;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1 KB alignment for the swizzled boxes
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* tables = reinterpret_cast<float*>(smem + NGRP * D * Lay::kSlot);      // [NW][8*2*8*2]
-  float* red = tables + NW * 256;                                              // [2][NW][kRed]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * NW * kRed);
-  uint64_t* empty = full + NGRP * D;
+  const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
+  const int prow = SM::panel_row(K);
+  uint8_t* panel = smem + D * Lay::kSlot;                                  // [G][prow]: activation rows
+  float* tables = reinterpret_cast<float*>(panel + G * prow);             // [Q][256]: per-warp scale table
+  float* red = tables + Q * 256;                                          // [2][Q][kPart]: partials
+  ItemHdr* ihdr = reinterpret_cast<ItemHdr*>(red + 2 * Q * kPart);        // [2]
+  PanelHdr* phdr = reinterpret_cast<PanelHdr*>(ihdr + 2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(phdr + 1);                 // [D] slot loaded (1 + tx)
+  uint64_t* empty = full + kMaxSlots;                                     // [D] slot released (Q)
+  uint64_t* pfull = empty + kMaxSlots;                                    // panel loaded (1 + tx)
+  uint64_t* pready = pfull + 1;                                           // panel converted (Q)
+  uint64_t* pempty = pready + 1;                                          // panel released (Q)
+  uint64_t* rfull = pempty + 1;                                           // [2] partials written (Q)
+  uint64_t* rempty = rfull + 2;                                           // [2] partials taken (1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
   const int Ks = K / 32;
   const int tiles = (MODE == MODE_GATEUP) ? a.inter / 16 : a.latent / kRows;
   const int rows_per_expert = (MODE == MODE_GATEUP) ? 2 * a.inter : a.latent;
-  const int kact_row = kc * 2 + 64;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NGRP * D; ++i) {
+    for (int i = 0; i < D; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], Q);
+    }
+    mbar_init(pfull, 1);
+    mbar_init(pready, Q);
+    mbar_init(pempty, Q);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&rfull[i], Q);
+      mbar_init(&rempty[i], 1);
     }
     fence_barrier_init();
   }
@@ -179,237 +219,132 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
   const int nloc = it1 - it0;
 
-  if (warp == NW) {
+  if (warp == Q) {
     // ------------------------------ producer ------------------------------
     const uint64_t pol = policy_evict_first();
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
     }
-    int seq[NGRP];
-#pragma unroll
-    for (int gi = 0; gi < NGRP; ++gi) seq[gi] = 0;
+    int seq = 0, pseq = 0, cur = -1;
     bool ok = true;
-    // metadata of 32 items at a time, item (batch + lane) in lane `lane`
-    int m_e = 0, m_p0 = 0, m_ntok = 0, m_rows[G], m_exp[G];
-    int batch = -1;
-    for (int base = 0; base < nloc && ok; base += NGRP) {
-      const int ng = min(NGRP, nloc - base);
-      if (base / 32 != batch) {
-        batch = base / 32;
-        const int itl = batch * 32 + lane;
-        m_ntok = 0;
-        if (itl < nloc) {
-          const int4 gq = a.groups[(it0 + itl) / tiles];
-          m_e = gq.x;
-          m_p0 = gq.y;
-          m_ntok = gq.z;
-        }
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          m_rows[jj] = 0;
-          m_exp[jj] = 0;
-          if (jj < m_ntok) m_rows[jj] = a.sorted_rows[m_p0 + jj];
-        }
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj)
-          if (jj < m_ntok) m_exp[jj] = act_exponent(a.act_max[(MODE == MODE_GATEUP) ? m_rows[jj] / a.top_k : m_p0 + jj]);
+    for (int j = 0; j < nloc && ok; ++j) {
+      const int it = it0 + j, grp = it / tiles, tile = it % tiles;
+      const int4 gq = a.groups[grp];
+      const int e = gq.x, p0 = gq.y, ntok = gq.z;
+      // first rows of box A and box B
+      int rowA, rowB;
+      if (MODE == MODE_GATEUP) {
+        rowA = e * rows_per_expert + tile * 16;
+        rowB = rowA + a.inter;
+      } else {
+        rowA = e * rows_per_expert + tile * kRows;
+        rowB = rowA + 16;
       }
       for (int c = 0; c < nch && ok; ++c) {
-        for (int gi = 0; gi < ng; ++gi) {
-          const int it = it0 + base + gi;
-          const int tile = it % tiles;
-          const int src = (base + gi) & 31;
-          const int e = __shfl_sync(0xffffffffu, m_e, src);
-          const int p0 = __shfl_sync(0xffffffffu, m_p0, src);
-          const int ntok = __shfl_sync(0xffffffffu, m_ntok, src);
-          int my_row = 0, my_exp = 0;  // token `lane` of this item
-#pragma unroll
-          for (int jj = 0; jj < G; ++jj) {
-            const int rv = __shfl_sync(0xffffffffu, m_rows[jj], src);
-            const int ev = __shfl_sync(0xffffffffu, m_exp[jj], src);
-            if (lane == jj) {
-              my_row = rv;
-              my_exp = ev;
-            }
-          }
-          const int d = seq[gi] % D;
-          const uint32_t par = ((seq[gi] / D) & 1) ^ 1;
-          ++seq[gi];
-          int got = 1;
-          if (lane == 0) got = mbar_wait(&empty[gi * D + d], par, a.st, 1);
-          if (!__shfl_sync(0xffffffffu, got, 0)) {
+        const int d = seq % D;
+        const uint32_t par = ((seq / D) & 1) ^ 1;
+        ++seq;
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[d], par, a.st, 1);
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* slot = smem + d * Lay::kSlot;
+        uint64_t* bar = &full[d];
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
+          tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
+          tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
+        }
+        __syncwarp();
+        if (lane == 1 || lane == 2) {
+          uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
+          const int srow = lane == 1 ? rowA : rowB;
+          if (nch > 1)
+            tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
+          else  // one chunk: the 16 rows' scales are contiguous
+            bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
+        }
+        __syncwarp();
+        if (c == 0 && grp != cur) {
+          // New group: its activation rows go to the panel once every consumer
+          // released the previous group's.  Issued after this item's first
+          // chunk, so the ring keeps streaming weights meanwhile; the old
+          // group's chunks are all issued, so the wait cannot close a cycle.
+          cur = grp;
+          int pg = 1;
+          if (lane == 0) pg = mbar_wait(pempty, (pseq & 1) ^ 1, a.st, 4);
+          if (!__shfl_sync(0xffffffffu, pg, 0)) {
             ok = false;
             break;
           }
-          uint8_t* slot = smem + (gi * D + d) * Lay::kSlot;
-          uint64_t* bar = &full[gi * D + d];
-          // first rows of box A and box B
-          int rowA, rowB;
-          if (MODE == MODE_GATEUP) {
-            rowA = e * rows_per_expert + tile * 16;
-            rowB = rowA + a.inter;
-          } else {
-            rowA = e * rows_per_expert + tile * kRows;
-            rowB = rowA + 16;
-          }
-          if (c == 0) {
-            ItemMeta* meta = reinterpret_cast<ItemMeta*>(slot + Lay::kCodes + Lay::kScales + Lay::kActs);
-            if (lane == 0) {
-              meta->p0 = p0;
-              meta->ntok = ntok;
-            }
-            if (lane < G) {
-              meta->aexp[lane] = my_exp;
-              meta->rows[lane] = my_row;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb + (uint32_t)ntok * kc * 2);
-          __syncwarp();
-          if (lane == 0) {
-            tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
-            tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
-          } else if (lane == 1 || lane == 2) {
-            uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
-            const int srow = lane == 1 ? rowA : rowB;
-            if (nch > 1)
-              tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
-            else  // one chunk: the 16 rows' scales are contiguous
-              bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
-          }
-          // activation rows: token j's copy from lane j (its row id is in my_row)
+          int my_row = 0, my_exp = 0;
           if (lane < ntok) {
-            const int j = lane;
-            const int arow = (MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + j;
-            bulk_g2s(slot + Lay::kCodes + Lay::kScales + j * kact_row, a.act + (size_t)arow * K + c * kc, kc * 2,
-                     bar);
+            my_row = a.sorted_rows[p0 + lane];
+            my_exp = act_exponent(a.act_max[(MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + lane]);
           }
+          if (lane == 0) {
+            phdr->p0 = p0;
+            phdr->ntok = ntok;
+          }
+          if (lane < G) {
+            phdr->aexp[lane] = my_exp;
+            phdr->rows[lane] = my_row;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(pfull, (uint32_t)ntok * K * 2);
+          __syncwarp();
+          if (lane < ntok) {
+            const int arow = (MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + lane;
+            const uint16_t* src = a.act + (size_t)arow * K;
+            for (int k0 = 0; k0 < K; k0 += 8192)  // pieces of at most 16 KB
+              bulk_g2s(panel + lane * prow + k0 * 2, src + k0, (uint32_t)min(8192, K - k0) * 2, pfull);
+          }
+          ++pseq;
           __syncwarp();
         }
       }
     }
     // drain: no copy may still be in flight when this warp leaves
     if (lane == 0) {
-#pragma unroll
-      for (int gi = 0; gi < NGRP; ++gi)
-        for (int s = max(0, seq[gi] - D); s < seq[gi]; ++s)
-          mbar_wait(&full[gi * D + (s % D)], (s / D) & 1, a.st, 2);
+      for (int s = max(0, seq - D); s < seq; ++s) mbar_wait(&full[s % D], (s / D) & 1, a.st, 2);
+      if (pseq > 0) mbar_wait(pfull, (pseq - 1) & 1, a.st, 5);
     }
     return;
   }
 
-  // -------------------------------- consumer --------------------------------
-  const int gi = warp / Q, mem = warp % Q;
-  const int g = lane >> 2, q = lane & 3;
-  // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
-  const int lm = lane >> 3, rr = lane & 7;
-  float* table = tables + warp * 256;
-  int item_count = 0;
-  // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
-  uint32_t box_off[2];
-  int row_in_box[2];
+  if (warp == Q + 1) {
+    // ------------------------------ epilogue ------------------------------
+    const int g = lane >> 2, q = lane & 3;
+    for (int j = 0; j < nloc; ++j) {
+      const int pb = j & 1;
+      if (!mbar_wait(&rfull[pb], (j >> 1) & 1, a.st, 6)) break;
+      const ItemHdr* h = ihdr + pb;
+      const int p0 = h->p0, ntok = h->ntok, tile = h->tile;
+      int aexp[G], arow_id[G];
 #pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    int box, row;
-    if (MODE == MODE_GATEUP) {
-      box = lm & 1;  // gate box (lo) / up box (hi)
-      row = m * 8 + rr;
-    } else {
-      box = m;
-      row = (lm & 1) * 8 + rr;
-    }
-    box_off[m] = box * 16 * (kc / 2);
-    row_in_box[m] = row;
-  }
-  const int nplanes = nb / 8;
-  int seq = 0;
-  bool alive = true;
-  for (int j = gi; j < nloc; j += NGRP) {
-    const int it = it0 + j;
-    const int tile = it % tiles;
-    int p0 = 0, ntok = 0;
-    int aexp[G], arow_id[G];  // from the item header (first chunk's slot)
-    float acc[2][2][NV];  // [mtile][lo/hi row][token column]
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) acc[m][h][v] = 0.f;
-    for (int c = 0; c < nch && alive; ++c) {
-      const int d = seq % D;
-      const uint32_t par = (seq / D) & 1;
-      ++seq;
-      if (!mbar_wait(&full[gi * D + d], par, a.st, 3)) {
-        alive = false;
-        break;
+      for (int jj = 0; jj < G; ++jj) {
+        aexp[jj] = h->aexp[jj];
+        arow_id[jj] = h->rows[jj];
       }
-      const uint8_t* slot = smem + (gi * D + d) * Lay::kSlot;
-      if (c == 0) {
-        const ItemMeta* meta = reinterpret_cast<const ItemMeta*>(slot + Lay::kCodes + Lay::kScales + Lay::kActs);
-        p0 = meta->p0;
-        ntok = meta->ntok;
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          aexp[jj] = meta->aexp[jj];
-          arow_id[jj] = meta->rows[jj];
-        }
-      }
-      const uint32_t sbase = smem_u32(slot);
-      const uint32_t act_addr = smem_u32(slot + Lay::kCodes + Lay::kScales) + (g < G ? g : 0) * kact_row + q * 16;
-      for (int pl = mem; pl < nplanes; pl += Q) {
-        expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
-        // this plane's activation columns (256 per token): bf16 -> f16 * 2^e in place
-#pragma unroll
-        for (int jj = 0; jj < G; ++jj) {
-          if (jj < ntok) {
-            uint4* pa = reinterpret_cast<uint4*>(const_cast<uint8_t*>(slot) + Lay::kCodes + Lay::kScales +
-                                                 jj * kact_row + pl * 512) + lane;
-            const uint4 v = *pa;
-            const float sc = ldexpf(1.0f, aexp[jj]);
-            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(in[u] & 0xffffu) * sc, bf16_bits_to_f32(in[u] >> 16) * sc);
-              o[u] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            *pa = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
-        __syncwarp();
-        plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
-        __syncwarp();
-      }
-      if (lane == 0) mbar_arrive(&empty[gi * D + d]);
-    }
-    // ------------------- member partials, added in member order -------------------
-    // Two buffers by item parity: a member may write item i+1's partials while
-    // member 0 still reads item i's, so one barrier per item suffices (a member
-    // reaches item i+2's write only after the barrier of item i+1, which member
-    // 0 passes after finishing item i).
-    float* rbuf = red + (item_count & 1) * NW * kRed;
-    ++item_count;
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) rbuf[warp * kRed + ((m * 2 + h) * NV + v) * 32 + lane] = acc[m][h][v];
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(Q * 32) : "memory");
-    if (mem == 0) {
+      const float* rb = red + pb * Q * kPart;
+      float acc[2][2][NV];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            float t = rbuf[(gi * Q) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
-            for (int o = 1; o < Q; ++o) t += rbuf[(gi * Q + o) * kRed + ((m * 2 + h) * NV + v) * 32 + lane];
-            acc[m][h][v] = t;
+            const int o = ((m * 2 + hh) * NV + v) * 32 + lane;
+            float t = rb[o];
+#pragma unroll
+            for (int w = 1; w < Q; ++w) t += rb[w * kPart + o];
+            acc[m][hh][v] = t;
           }
-      // ------------------------------ epilogue ------------------------------
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[pb]);
       // gate/up m-tile m holds features tile*16 + m*8 + g; down m-tile m holds
       // output rows tile*32 + m*16 + g (+8 for the hi half)
       float ssq[NV];
@@ -436,8 +371,7 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
               ssq[v] = fmaxf(ssq[v], fabsf(bf16_bits_to_f32(hb)));  // gate/up: running max |h|
             }
           } else {
-            const int r = r_tok;
-            float* yr = a.y_out + (size_t)r * a.latent + tile * kRows;
+            float* yr = a.y_out + (size_t)r_tok * a.latent + tile * kRows;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               const float y0 = acc[m][0][v] * inv, y1 = acc[m][1][v] * inv;
@@ -477,6 +411,134 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
         }
       }
     }
+    return;
+  }
+
+  // -------------------------------- consumer --------------------------------
+  const int g = lane >> 2, q = lane & 3;
+  // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
+  const int lm = lane >> 3, rr = lane & 7;
+  float* table = tables + warp * 256;
+  // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
+  uint32_t box_off[2];
+  int row_in_box[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    int box, row;
+    if (MODE == MODE_GATEUP) {
+      box = lm & 1;  // gate box (lo) / up box (hi)
+      row = m * 8 + rr;
+    } else {
+      box = m;
+      row = (lm & 1) * 8 + rr;
+    }
+    box_off[m] = box * 16 * (kc / 2);
+    row_in_box[m] = row;
+  }
+  const int nplanes = nb / 8;
+  // this lane's activation row in the panel (token g; rows past the group's count are never read back)
+  const uint32_t act_row = smem_u32(panel) + (g < G ? g : 0) * prow + q * 16;
+  int seq = 0, pseq = 0, cur = -1;
+  int p0 = 0, ntok = 0;
+  int aexp[G], arow_id[G];
+#pragma unroll
+  for (int jj = 0; jj < G; ++jj) aexp[jj] = arow_id[jj] = 0;
+  bool alive = true;
+  for (int j = 0; j < nloc && alive; ++j) {
+    const int it = it0 + j, grp = it / tiles, tile = it % tiles;
+    if (grp != cur) {
+      // a fresh panel: convert it in place (bf16 -> f16 * 2^e), all consumer warps
+      cur = grp;
+      if (!mbar_wait(pfull, pseq & 1, a.st, 7)) break;
+      p0 = phdr->p0;
+      ntok = phdr->ntok;
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        aexp[jj] = phdr->aexp[jj];
+        arow_id[jj] = phdr->rows[jj];
+      }
+      const int units = K / 8;  // 16-byte units per row
+      for (int u = warp * 32 + lane; u < ntok * units; u += Q * 32) {
+        const int r = u / units, cu = u - r * units;
+        uint4* pa = reinterpret_cast<uint4*>(panel + r * prow + cu * 16);
+        const uint4 v = *pa;
+        const float sc = ldexpf(1.0f, phdr->aexp[r]);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(in[t] & 0xffffu) * sc, bf16_bits_to_f32(in[t] >> 16) * sc);
+          o[t] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        *pa = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pready);
+      if (!mbar_wait(pready, pseq & 1, a.st, 8)) break;
+      ++pseq;
+    }
+    float acc[2][2][NV];  // [mtile][lo/hi row][token column]
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[m][h][v] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const int d = seq % D;
+      const uint32_t par = (seq / D) & 1;
+      ++seq;
+      if (!mbar_wait(&full[d], par, a.st, 3)) {
+        alive = false;
+        break;
+      }
+      const uint8_t* slot = smem + d * Lay::kSlot;
+      const uint32_t sbase = smem_u32(slot);
+      const uint32_t act_addr = act_row + c * kc * 2;
+      for (int pl = warp; pl < nplanes; pl += Q) {
+        expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
+        __syncwarp();
+        plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&empty[d]);
+    }
+    if (!alive) break;
+    const bool last_of_group = (j + 1 == nloc) || ((it + 1) / tiles != grp);
+    if (last_of_group) {
+      // panel reads (and this warp's conversion writes) come before the next bulk copy into it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pempty);
+    }
+    // partials to the epilogue warp (double-buffered by item parity)
+    const int pb = j & 1;
+    if (!mbar_wait(&rempty[pb], ((j >> 1) & 1) ^ 1, a.st, 9)) break;
+    float* rbuf = red + (pb * Q + warp) * kPart;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) rbuf[((m * 2 + h) * NV + v) * 32 + lane] = acc[m][h][v];
+    if (warp == 0) {
+      ItemHdr* h = ihdr + pb;
+      if (lane == 0) {
+        h->p0 = p0;
+        h->ntok = ntok;
+        h->tile = tile;
+      }
+      if (lane < G) {
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+          if (jj == lane) {
+            h->aexp[lane] = aexp[jj];
+            h->rows[lane] = arow_id[jj];
+          }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rfull[pb]);
   }
 }
 
@@ -485,21 +547,23 @@ __global__ void __launch_bounds__(32 * (NGRP * Q + 1), 1)
 // ---------------------------------------------------------------------------
 int expert_max_group(int T) { return T <= 1 ? 1 : 8; }
 
-template <int MODE, int G, int NGRP, int Q, int D>
+template <int MODE, int G, int Q>
 static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
-  using Lay = Layout<G>;
-  auto kern = expert_kernel<MODE, G, NGRP, Q, D>;
-  constexpr int NV = (G == 1) ? 1 : 2;
-  constexpr int smem = NGRP * D * Lay::kSlot + NGRP * Q * (256 + 2 * 2 * 2 * NV * 32) * 4 + 2 * NGRP * D * 8 +
-                       1024;  // +1 KB alignment slack
-  static_assert(smem <= 232448, "shared memory budget");
-  static unsigned long long attr_done = 0;  // one bit per device, per template instance
+  using SM = Smem<G, Q>;
+  auto kern = expert_kernel<MODE, G, Q>;
+  constexpr int kSmemMax = 232448;
+  if (a.K > kMaxK) return LMOE_EUNSUPPORTED;
+  // as many ring slots as fit next to the panel (at least 2)
+  const int D = min(kMaxSlots, (kSmemMax - SM::fixed(a.K) - 1024) / Layout::kSlot);
+  if (D < 2) return LMOE_EUNSUPPORTED;
+  const int smem = SM::bytes(a.K, D);
+  static int attr_done[64] = {};  // per device: largest dynamic shared memory size set so far
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!(attr_done >> (dev & 63) & 1ull)) {
+  if (attr_done[dev & 63] < smem) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return LMOE_ECUDA;
-    attr_done |= 1ull << (dev & 63);
+    attr_done[dev & 63] = smem;
   }
   // K chunk: the whole K when K <= kKC, else kKC (K is a multiple of kKC then)
   a.kc = a.K <= kKC ? a.K : kKC;
@@ -525,7 +589,7 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(32 * (NGRP * Q + 1));
+  cfg.blockDim = dim3(32 * (Q + 2));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -533,17 +597,17 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, tq, ts) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+  return cudaLaunchKernelEx(&cfg, kern, a, tq, ts, D) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 1, 8, 5>(a, s, num_sms);
-  return launch_one<MODE_GATEUP, 8, 1, 8, 3>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 8>(a, s, num_sms);
+  return launch_one<MODE_GATEUP, 8, 8>(a, s, num_sms);
 }
 
 int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_DOWN, 1, 1, 8, 5>(a, s, num_sms);
-  return launch_one<MODE_DOWN, 8, 1, 8, 3>(a, s, num_sms);
+  if (max_group == 1) return launch_one<MODE_DOWN, 1, 8>(a, s, num_sms);
+  return launch_one<MODE_DOWN, 8, 8>(a, s, num_sms);
 }
 
 }  // namespace lmoe

@@ -74,9 +74,12 @@ def test_bad_dims_rejected(lm, field, value):
 
 
 def test_unsupported_width(lm):
-    # K is streamed in 2048-element chunks above 2048, and in 128-byte planes
-    for h, l, i in [(8192, 2560, 4096), (8192, 4096, 3328), (8192 + 128, 4096, 4096)]:
+    # K is streamed in 2048-element chunks above 2048, and in 128-byte planes; a
+    # group's activation rows (K <= 8192) sit in shared memory
+    for h, l, i in [(8192, 2560, 4096), (8192, 4096, 3328), (8192 + 128, 4096, 4096), (8192, 10240, 4096),
+                    (8192, 4096, 10240)]:
         assert lm.lmoe_workspace_bytes(lm.dims_of(1, h, l, i, 256, 8, 1e-6)) == 0
+    assert lm.lmoe_workspace_bytes(lm.dims_of(1, 8192, 8192, 8192, 256, 8, 1e-6)) > 0
 
 
 def test_regime_options_round_trip(lm):

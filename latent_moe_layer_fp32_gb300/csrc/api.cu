@@ -74,6 +74,29 @@ int dev_info(DevInfo* out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The small kernels (routing, combine, helpers) prefer the largest shared-memory
+// carveout: an SM configured for them can then also host a CTA of the weight-
+// streaming kernel launched behind them (up to ~200 KB of shared memory), which
+// starts while they run instead of after.  Once per device.
+int set_carveouts() {
+  static unsigned long long done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ECUDA;
+  if (done >> (dev & 63) & 1ull) return LMOE_OK;
+  const void* fns[] = {
+      reinterpret_cast<const void*>(route_small_kernel), reinterpret_cast<const void*>(router_partial_kernel),
+      reinterpret_cast<const void*>(topk_kernel),        reinterpret_cast<const void*>(table_kernel),
+      reinterpret_cast<const void*>(combine_kernel),     reinterpret_cast<const void*>(ssq_kernel),
+      reinterpret_cast<const void*>(groups_from_offsets_kernel),
+      reinterpret_cast<const void*>(gather_rows_kernel), reinterpret_cast<const void*>(router_split_kernel)};
+  for (const void* f : fns)
+    if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess)
+      return LMOE_ECUDA;
+  done |= 1ull << (dev & 63);
+  return LMOE_OK;
+}
+
 int check_dims(const lmoe_dims* d) {
   if (!d) return LMOE_EINVAL;
   if (d->T < 1 || d->T > 65536 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k ||
@@ -100,7 +123,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, route_count, zero_bytes, groups, part, xmax, h, hmax, ssq, xs, wr3;
+  size_t n_groups, route_count, zero_bytes, groups, part, h, ssq, xs, wr3;
   int nsplit;
 };
 
@@ -115,13 +138,11 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
     o = al(o + bytes);
     return at;
   };
-  // zeroed at the start of every call: status word, counters, row max words
+  // zeroed at the start of every call: status word, counters
   w->pub.status = 0;
   w->n_groups = 16;
-  w->route_count = 24;
-  w->xmax = 64;
-  w->hmax = 64 + 4 * T;
-  w->zero_bytes = 64 + 4 * T + 4 * R;
+  w->route_count = 64;  // small-T routing tickets: [0] last block overall, [1 + b] last split of block b (b < 16)
+  w->zero_bytes = 160;
   take(w->zero_bytes);
   w->pub.topk_idx = take(4 * R);
   w->pub.topk_w = take(4 * R);
@@ -180,6 +201,7 @@ int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayou
   snapshot_options();
   CHECK(check_dims(d));
   CHECK(dev_info(di));
+  CHECK(set_carveouts());
   CHECK(layout(d, di->sms, w));
   if (need_ws) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
@@ -196,7 +218,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   Status* st = at<Status>(ws, w.pub.status);
   float* part = at<float>(ws, w.part);
   if (T <= 16) {
-    // one launch: router partials, then the last CTA finishes the routing
+    // one launch: router partials, then the last CTAs finish the routing
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, route_small_kernel, x, router_w, router_bias,
            part, T, H, E, k, H / w.nsplit, group_rows(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
            at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st);
@@ -239,13 +261,15 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
 
 // x_sorted: when set (tensor-core pooler only), x_lat rows are also written in
 // expert-sorted order (row_pos = each route row's sorted position)
+// wait_mode (decode regime): kWaitAtEnd when nothing earlier in the stream can
+// still be writing x (in lmoe_forward it follows the call's own memset and routing)
 int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
-             uint32_t* xmax, Status* st, cudaStream_t s, const int32_t* row_pos = nullptr,
-             uint16_t* x_sorted = nullptr) {
+             Status* st, cudaStream_t s, const int32_t* row_pos = nullptr,
+             uint16_t* x_sorted = nullptr, int wait_mode = kWaitFirst) {
   const bool dense = x_sorted != nullptr || d->T >= t_dense_min_t;
   pre_launch(s, dense ? "pool_tc_gemm" : "pool_gemv");
   if (dense) {
-    TcGemmArgs g{x_lat, xmax, d->T, d->latent, d->hidden, st};
+    TcGemmArgs g{x_lat, d->T, d->latent, d->hidden, st};
     if (x_sorted) {
       g.scatter_pos = row_pos;
       g.scatter_k = d->top_k;
@@ -253,17 +277,21 @@ int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uin
     }
     CHECK(launch_tc_gemm_bf16(g, x, pooler_w, s, di.sms));
   } else {
-    GemvArgs g{pooler_w, x, x_lat, xmax, d->latent, d->hidden, d->T, st};
+    GemvArgs g{pooler_w, x, x_lat, d->latent, d->hidden, d->T, st, wait_mode};
     CHECK(launch_gemv_bf16(g, s, di.sms));
   }
   ++g_launches;
   return LMOE_OK;
 }
 
-// groups must already be in the workspace; xmax must hold each token's max |x_lat|
+// groups must already be in the workspace
+// groups_early: the group list was written by a kernel before the preceding one
+// (lmoe_forward: the routing precedes the pooler), so the gate/up kernel may
+// stream its first weights before waiting for its predecessor
 int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
                 const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
-                const uint8_t* w2_s, float* y, void* ws, cudaStream_t s, bool xs_ready = false) {
+                const uint8_t* w2_s, float* y, void* ws, cudaStream_t s, bool xs_ready = false,
+                bool groups_early = false) {
   const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
   if (experts_tc(T)) {
@@ -310,22 +338,20 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.q = w13_q;
   a.s = w13_s;
   a.act = x_lat;
-  a.act_max = at<uint32_t>(ws, w.xmax);
   a.K = L;
   a.h_out = at<uint16_t>(ws, w.h);
-  a.h_max = at<uint32_t>(ws, w.hmax);
+  a.early = groups_early ? 1 : 0;
   pre_launch(s, "expert_gateup");
   CHECK(launch_gateup(a, T, G, s, di.sms));
   ++g_launches;
   a.q = w2_q;
   a.s = w2_s;
   a.act = at<uint16_t>(ws, w.h);
-  a.act_max = at<uint32_t>(ws, w.hmax);
   a.K = I;
   a.h_out = nullptr;
-  a.h_max = nullptr;
   a.y_out = y;
   a.ssq_out = at<float>(ws, w.ssq);
+  a.early = 1;  // the gate/up kernel waited for whatever wrote the group list
   pre_launch(s, "expert_down");
   CHECK(launch_down(a, T, G, s, di.sms));
   ++g_launches;
@@ -349,10 +375,11 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
   const bool dense = d->T >= t_dense_min_t;
   pre_launch(s, dense ? "unpool_tc_gemm" : "unpool_gemv");
   if (dense) {
-    TcGemmArgs g{out, nullptr, d->T, d->hidden, d->latent, st};
+    TcGemmArgs g{out, d->T, d->hidden, d->latent, st};
     CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
   } else {
-    GemvArgs g{unpooler_w, zb, out, nullptr, d->hidden, d->latent, d->T, st};
+    // the unpooler weights depend on nothing earlier: they stream while the combine finishes
+    GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st, kWaitAfterWeights};
     CHECK(launch_gemv_bf16(g, s, di.sms));
   }
   ++g_launches;
@@ -403,7 +430,7 @@ int lmoe_pool(const lmoe_dims* d, const uint16_t* x, const uint16_t* pooler_w, u
   CHECK(prologue(d, ws, ws_bytes, &di, &w, s, ws != nullptr));
   if (!aligned16(x) || !aligned16(pooler_w) || !aligned16(x_lat) || !x || !pooler_w || !x_lat) return LMOE_EINVAL;
   Status* st = ws ? at<Status>(ws, w.pub.status) : nullptr;
-  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, nullptr, st, s));
+  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, st, s));
 }
 
 int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
@@ -419,7 +446,6 @@ int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t*
   const int R = d->T * d->top_k;
   LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
          group_rows(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
-  if (!experts_tc(d->T)) LAUNCH(dim3(d->T), dim3(256), s, row_max_kernel, x_lat, d->latent, at<uint32_t>(ws, w.xmax));
   return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s));
 }
 
@@ -459,9 +485,12 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   // with both the pooler and the experts on the tensor cores, the pooler's epilogue
   // also writes x_lat in expert-sorted order (no separate gather)
   const bool scatter = experts_tc(d->T) && d->T >= t_dense_min_t;
-  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, at<uint32_t>(ws, w.xmax), st, s,
-                 scatter ? at<int32_t>(ws, w.pub.row_pos) : nullptr, scatter ? at<uint16_t>(ws, w.xs) : nullptr));
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, scatter));
+  // The pooler depends only on x and its weights, so in the decode regime it runs
+  // alongside the routing kernels and waits for them only at its end.
+  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s,
+                 scatter ? at<int32_t>(ws, w.pub.row_pos) : nullptr, scatter ? at<uint16_t>(ws, w.xs) : nullptr,
+                 kWaitAtEnd));
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, scatter, true));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);
 }

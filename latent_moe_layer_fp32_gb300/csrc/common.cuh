@@ -127,28 +127,6 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       : "memory");
 }
 
-// Whether the streaming kernels run an L2 prefetch ahead of their smem rings.
-#ifndef LMOE_L2_PREFETCH
-#define LMOE_L2_PREFETCH 0
-#endif
-
-// Bulk prefetch of [src, src+bytes) into L2 (bytes a multiple of 16, src 16-byte aligned).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  if (!LMOE_L2_PREFETCH) return;
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// Prefetch a contiguous range in pieces of at most 16 KB.
-__device__ __forceinline__ void prefetch_l2_range(const void* src, size_t bytes) {
-  const char* p = static_cast<const char*>(src);
-  while (bytes > 0) {
-    const uint32_t n = bytes > 16384 ? 16384u : static_cast<uint32_t>(bytes);
-    prefetch_l2(p, n);
-    p += n;
-    bytes -= n;
-  }
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -22,11 +22,11 @@
 //    the group changes it loads the group's activation rows (bf16, whole K)
 //    into the activation panel, once the consumers released the old one.
 //  - consumers: convert a fresh panel once (bf16 -> f16 times a per-row power
-//    of two, exact; undone in the epilogue; the power comes from the row's
-//    max |value| that the producing kernel recorded), then share every slot,
-//    warp j taking the chunk's 128-byte planes j, j+Q, ...  They hand their
-//    fp32 partials to the epilogue warp through a double-buffered exchange
-//    and go straight on to the next item.
+//    of two that puts the row's largest magnitude in [2^14, 2^15): exact for
+//    every element down to 2^-17 of that scale; undone in the epilogue), then
+//    share every slot, warp j taking the chunk's 128-byte planes j, j+Q, ...
+//    They hand their fp32 partials to the epilogue warp through a
+//    double-buffered exchange and go straight on to the next item.
 //  - epilogue: adds the Q partials in warp order (fixed summation order) and
 //    finishes the item (SwiGLU -> h, or y plus its sums of squares).
 // Every wait is an mbarrier wait bounded in time.
@@ -48,17 +48,16 @@ enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 constexpr int kRows = 32;  // weight rows per item: two m16 tiles
 constexpr int kKC = 2048;  // K elements per chunk when K > 2048 (else the whole K): 16 KB code boxes
 
-// Group header the producer writes next to the activation panel.
+// Group header the producer writes next to an activation panel.
 struct PanelHdr {
   int p0, ntok, pad0, pad1;
-  int aexp[8];  // per token of the group: power of two mapping its activation row into f16 range
   int rows[8];  // per token: sorted_rows[p0 + j] (the original route row id)
 };
 
 // Item header a consumer passes to the epilogue warp with the partials.
 struct ItemHdr {
   int p0, ntok, tile, pad;
-  int aexp[8];
+  int aexp[8];  // per token of the group: power of two mapping its activation row into f16 range
   int rows[8];
 };
 
@@ -151,16 +150,18 @@ __device__ __forceinline__ void plane_blocks(uint32_t sbase, uint32_t act_addr, 
   }
 }
 
-
 // Shared-memory plan of one CTA (bytes), shared by the kernel and the launch.
+// NP activation panels: two when one group's rows are small (G = 1), so the
+// next group's rows load while the current group is still being consumed.
 template <int G, int Q>
 struct Smem {
+  static constexpr int NP = (G == 1) ? 2 : 1;
   static constexpr int NV = (G == 1) ? 1 : 2;        // token columns per lane that can hold a valid token
   static constexpr int kPart = 2 * 2 * NV * 32;      // floats per warp partial: [mtile][lo/hi][v][lane]
   static __host__ __device__ int panel_row(int K) { return K * 2 + 64; }  // padded: conflict-free 16-byte loads
   static __host__ __device__ int fixed(int K) {
-    return G * panel_row(K) + Q * 256 * 4 + 2 * Q * kPart * 4 + 2 * (int)sizeof(ItemHdr) + (int)sizeof(PanelHdr) +
-           (2 * kMaxSlots + 8) * 8;
+    return NP * G * panel_row(K) + Q * 256 * 4 + 2 * Q * kPart * 4 + Q * G * 4 + 2 * (int)sizeof(ItemHdr) +
+           NP * (int)sizeof(PanelHdr) + (2 * kMaxSlots + 2 * NP + 6) * 8;
   }
   static __host__ __device__ int bytes(int K, int D) { return D * Layout::kSlot + fixed(K) + 1024; }
 };
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
                   int D) {
   using Lay = Layout;
   using SM = Smem<G, Q>;
+  constexpr int NP = SM::NP;
   constexpr int NV = SM::NV;
   constexpr int kPart = SM::kPart;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -178,17 +180,19 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
   const int prow = SM::panel_row(K);
-  uint8_t* panel = smem + D * Lay::kSlot;                                  // [G][prow]: activation rows
-  float* tables = reinterpret_cast<float*>(panel + G * prow);             // [Q][256]: per-warp scale table
+  uint8_t* panels = smem + D * Lay::kSlot;                                 // [NP][G][prow]: activation rows
+  float* tables = reinterpret_cast<float*>(panels + NP * G * prow);       // [Q][256]: per-warp scale table
   float* red = tables + Q * 256;                                          // [2][Q][kPart]: partials
-  ItemHdr* ihdr = reinterpret_cast<ItemHdr*>(red + 2 * Q * kPart);        // [2]
-  PanelHdr* phdr = reinterpret_cast<PanelHdr*>(ihdr + 2);
-  uint64_t* full = reinterpret_cast<uint64_t*>(phdr + 1);                 // [D] slot loaded (1 + tx)
+  float* smax = red + 2 * Q * kPart;                                      // [Q][G]: per-warp row maxima
+  ItemHdr* ihdr = reinterpret_cast<ItemHdr*>(smax + Q * G);               // [2]
+  PanelHdr* phdr = reinterpret_cast<PanelHdr*>(ihdr + 2);                 // [NP]
+  uint64_t* full = reinterpret_cast<uint64_t*>(phdr + NP);                // [D] slot loaded (1 + tx)
   uint64_t* empty = full + kMaxSlots;                                     // [D] slot released (Q)
-  uint64_t* pfull = empty + kMaxSlots;                                    // panel loaded (1 + tx)
-  uint64_t* pready = pfull + 1;                                           // panel converted (Q)
-  uint64_t* pempty = pready + 1;                                          // panel released (Q)
-  uint64_t* rfull = pempty + 1;                                           // [2] partials written (Q)
+  uint64_t* pfull = empty + kMaxSlots;                                    // [NP] panel loaded (1 + tx)
+  uint64_t* pempty = pfull + NP;                                          // [NP] panel released (Q)
+  uint64_t* pmaxed = pempty + NP;                                         // row maxima written (Q)
+  uint64_t* pready = pmaxed + 1;                                          // panel converted (Q)
+  uint64_t* rfull = pready + 1;                                           // [2] partials written (Q)
   uint64_t* rempty = rfull + 2;                                           // [2] partials taken (1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,9 +205,12 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], Q);
     }
-    mbar_init(pfull, 1);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], Q);
+    }
+    mbar_init(pmaxed, Q);
     mbar_init(pready, Q);
-    mbar_init(pempty, Q);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&rfull[i], Q);
       mbar_init(&rempty[i], 1);
@@ -211,8 +218,15 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
+  // Programmatic dependent launch: the routing table and the weights come from
+  // kernels that completed before this grid was launched (the preceding kernel
+  // waits for its own predecessor before it lets this one start), so the
+  // producer streams its first slots of weights before waiting; the activation
+  // rows (the preceding kernel's output) are read only after the wait.
+  if (warp != Q || !a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int n_items = *a.n_groups * tiles;
   const int it0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
@@ -226,12 +240,31 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
     }
+    // The routing of this CTA's groups, read once up front (one round trip each):
+    // lane l holds the entry of group g_first + l, and, for groups of up to G
+    // rows, lane l of set s the row id of token l % G of group
+    // g_first + s * (32 / G) + l / G.  Groups past these come from memory.
+    constexpr int GPS = 32 / G;  // groups per set of row ids
+    constexpr int NSET = (G == 1) ? 1 : 2;
+    const int g_first = it0 / tiles;
+    const int g_last = nloc > 0 ? (it1 - 1) / tiles : g_first - 1;
+    int4 ent = make_int4(0, 0, 0, 0);
+    if (g_first + lane <= g_last) ent = a.groups[g_first + lane];
+    const int4* groups = a.groups;
+    auto entry = [ent, g_first, groups](int grp) -> int4 {
+      const int off = grp - g_first;
+      if (off < 32) {
+        return make_int4(__shfl_sync(0xffffffffu, ent.x, off), __shfl_sync(0xffffffffu, ent.y, off),
+                         __shfl_sync(0xffffffffu, ent.z, off), 0);
+      }
+      return groups[grp];
+    };
     int seq = 0, pseq = 0, cur = -1;
     bool ok = true;
-    for (int j = 0; j < nloc && ok; ++j) {
-      const int it = it0 + j, grp = it / tiles, tile = it % tiles;
-      const int4 gq = a.groups[grp];
-      const int e = gq.x, p0 = gq.y, ntok = gq.z;
+    // codes and scales of chunk c of local item j into the next ring slot
+    auto issue = [&](int j, int c) -> bool {
+      const int it = it0 + j, tile = it % tiles;
+      const int e = entry(it / tiles).x;
       // first rows of box A and box B
       int rowA, rowB;
       if (MODE == MODE_GATEUP) {
@@ -241,66 +274,99 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
         rowA = e * rows_per_expert + tile * kRows;
         rowB = rowA + 16;
       }
+      const int d = seq % D;
+      const uint32_t par = ((seq / D) & 1) ^ 1;
+      ++seq;
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&empty[d], par, a.st, 1);
+      if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+      uint8_t* slot = smem + d * Lay::kSlot;
+      uint64_t* bar = &full[d];
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
+        tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
+        tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
+      }
+      __syncwarp();
+      if (lane == 1 || lane == 2) {
+        uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
+        const int srow = lane == 1 ? rowA : rowB;
+        if (nch > 1)
+          tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
+        else  // one chunk: the 16 rows' scales are contiguous
+          bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
+      }
+      __syncwarp();
+      return true;
+    };
+    // the ring's first D slots are free: fill them before waiting
+    int issued = 0;
+    const int total = nloc * nch;
+    while (a.early && ok && issued < total && issued < D) {
+      ok = issue(issued / nch, issued % nch);
+      ++issued;
+    }
+    int rowv[NSET];
+#pragma unroll
+    for (int st = 0; st < NSET; ++st) {
+      rowv[st] = 0;
+      const int off = st * GPS + lane / G;  // < 32: its entry is in lane `off`
+      const int gy = __shfl_sync(0xffffffffu, ent.y, off), gz = __shfl_sync(0xffffffffu, ent.z, off);
+      if (g_first + off <= g_last && lane % G < gz) rowv[st] = a.sorted_rows[gy + lane % G];
+    }
+    if (a.early) {
+      pdl_wait();
+      pdl_trigger();
+    }
+    for (int j = 0; j < nloc && ok; ++j) {
+      const int it = it0 + j, grp = it / tiles;
       for (int c = 0; c < nch && ok; ++c) {
-        const int d = seq % D;
-        const uint32_t par = ((seq / D) & 1) ^ 1;
-        ++seq;
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[d], par, a.st, 1);
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          ok = false;
-          break;
+        if (j * nch + c >= issued) {
+          ok = issue(j, c);
+          ++issued;
+          if (!ok) break;
         }
-        uint8_t* slot = smem + d * Lay::kSlot;
-        uint64_t* bar = &full[d];
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
-          tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
-          tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
-        }
-        __syncwarp();
-        if (lane == 1 || lane == 2) {
-          uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
-          const int srow = lane == 1 ? rowA : rowB;
-          if (nch > 1)
-            tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
-          else  // one chunk: the 16 rows' scales are contiguous
-            bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
-        }
-        __syncwarp();
         if (c == 0 && grp != cur) {
-          // New group: its activation rows go to the panel once every consumer
-          // released the previous group's.  Issued after this item's first
-          // chunk, so the ring keeps streaming weights meanwhile; the old
-          // group's chunks are all issued, so the wait cannot close a cycle.
+          // New group: its activation rows go to the next panel once every
+          // consumer released what that panel held.  Issued after this item's
+          // first chunk, so the ring keeps streaming weights meanwhile; the
+          // older groups' chunks are all issued, so the wait cannot close a cycle.
           cur = grp;
+          const int4 g4 = entry(grp);
+          const int p0 = g4.y, ntok = g4.z;
+          const int pb = pseq % NP;
           int pg = 1;
-          if (lane == 0) pg = mbar_wait(pempty, (pseq & 1) ^ 1, a.st, 4);
+          if (lane == 0) pg = mbar_wait(&pempty[pb], ((pseq / NP) & 1) ^ 1, a.st, 4);
           if (!__shfl_sync(0xffffffffu, pg, 0)) {
             ok = false;
             break;
           }
-          int my_row = 0, my_exp = 0;
-          if (lane < ntok) {
+          const int off = grp - g_first;
+          int my_row = 0;
+          if (off < NSET * GPS) {
+            int v = 0;
+#pragma unroll
+            for (int st = 0; st < NSET; ++st)
+              if (st == off / GPS) v = rowv[st];
+            my_row = __shfl_sync(0xffffffffu, v, ((off % GPS) * G + lane % G) & 31);
+          } else if (lane < ntok) {
             my_row = a.sorted_rows[p0 + lane];
-            my_exp = act_exponent(a.act_max[(MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + lane]);
           }
+          PanelHdr* h = phdr + pb;
           if (lane == 0) {
-            phdr->p0 = p0;
-            phdr->ntok = ntok;
+            h->p0 = p0;
+            h->ntok = ntok;
           }
-          if (lane < G) {
-            phdr->aexp[lane] = my_exp;
-            phdr->rows[lane] = my_row;
-          }
+          if (lane < G) h->rows[lane] = my_row;
           __syncwarp();
-          if (lane == 0) mbar_arrive_expect_tx(pfull, (uint32_t)ntok * K * 2);
+          if (lane == 0) mbar_arrive_expect_tx(&pfull[pb], (uint32_t)ntok * K * 2);
           __syncwarp();
           if (lane < ntok) {
             const int arow = (MODE == MODE_GATEUP) ? my_row / a.top_k : p0 + lane;
             const uint16_t* src = a.act + (size_t)arow * K;
+            uint8_t* dst = panels + (pb * G + lane) * prow;
             for (int k0 = 0; k0 < K; k0 += 8192)  // pieces of at most 16 KB
-              bulk_g2s(panel + lane * prow + k0 * 2, src + k0, (uint32_t)min(8192, K - k0) * 2, pfull);
+              bulk_g2s(dst + k0 * 2, src + k0, (uint32_t)min(8192, K - k0) * 2, &pfull[pb]);
           }
           ++pseq;
           __syncwarp();
@@ -310,7 +376,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     // drain: no copy may still be in flight when this warp leaves
     if (lane == 0) {
       for (int s = max(0, seq - D); s < seq; ++s) mbar_wait(&full[s % D], (s / D) & 1, a.st, 2);
-      if (pseq > 0) mbar_wait(pfull, (pseq - 1) & 1, a.st, 5);
+      for (int s = max(0, pseq - NP); s < pseq; ++s) mbar_wait(&pfull[s % NP], (s / NP) & 1, a.st, 5);
     }
     return;
   }
@@ -366,9 +432,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               const float gv = acc[m][0][v] * inv, uv = acc[m][1][v] * inv;
-              const uint16_t hb = f32_to_bf16_bits(gv / (1.0f + expf(-gv)) * uv);
-              a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = hb;
-              ssq[v] = fmaxf(ssq[v], fabsf(bf16_bits_to_f32(hb)));  // gate/up: running max |h|
+              a.h_out[(size_t)p * a.inter + tile * 16 + m * 8 + g] = f32_to_bf16_bits(gv / (1.0f + expf(-gv)) * uv);
             }
           } else {
             float* yr = a.y_out + (size_t)r_tok * a.latent + tile * kRows;
@@ -380,18 +444,6 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
               ssq[v] = fmaf(y0, y0, fmaf(y1, y1, ssq[v]));
             }
           }
-        }
-      }
-      if (MODE == MODE_GATEUP) {
-        // row max of |h| over this tile's 16 features, folded into the row's max word
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          float mv = ssq[v];
-          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 4));
-          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 8));
-          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 16));
-          const int tok = 2 * q + v;
-          if (g == 0 && tok < ntok) atomicMax(&a.h_max[p0 + tok], __float_as_uint(mv));
         }
       }
       if (MODE == MODE_DOWN && a.ssq_out) {
@@ -436,10 +488,10 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     row_in_box[m] = row;
   }
   const int nplanes = nb / 8;
-  // this lane's activation row in the panel (token g; rows past the group's count are never read back)
-  const uint32_t act_row = smem_u32(panel) + (g < G ? g : 0) * prow + q * 16;
+  const int units = K / 8;  // 16-byte units per activation row
   int seq = 0, pseq = 0, cur = -1;
   int p0 = 0, ntok = 0;
+  uint32_t act_row = 0;  // this lane's activation row (token g) in the current panel
   int aexp[G], arow_id[G];
 #pragma unroll
   for (int jj = 0; jj < G; ++jj) aexp[jj] = arow_id[jj] = 0;
@@ -447,34 +499,66 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   for (int j = 0; j < nloc && alive; ++j) {
     const int it = it0 + j, grp = it / tiles, tile = it % tiles;
     if (grp != cur) {
-      // a fresh panel: convert it in place (bf16 -> f16 * 2^e), all consumer warps
+      // a fresh panel: each row's largest magnitude sets its power of two, then
+      // the rows are converted in place (bf16 -> f16 * 2^e), all consumer warps
       cur = grp;
-      if (!mbar_wait(pfull, pseq & 1, a.st, 7)) break;
-      p0 = phdr->p0;
-      ntok = phdr->ntok;
+      const int pb = pseq % NP;
+      if (!mbar_wait(&pfull[pb], (pseq / NP) & 1, a.st, 7)) break;
+      const PanelHdr* h = phdr + pb;
+      uint8_t* panel = panels + pb * G * prow;
+      p0 = h->p0;
+      ntok = h->ntok;
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) arow_id[jj] = h->rows[jj];
+      for (int r = 0; r < ntok; ++r) {
+        float m = 0.f;
+        for (int u = warp * 32 + lane; u < units; u += Q * 32) {
+          const uint4 v = *reinterpret_cast<const uint4*>(panel + r * prow + u * 16);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w4[t] & 0xffffu)), fabsf(bf16_bits_to_f32(w4[t] >> 16))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) smax[warp * G + r] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pmaxed);
+      if (!mbar_wait(pmaxed, pseq & 1, a.st, 10)) break;
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) {
-        aexp[jj] = phdr->aexp[jj];
-        arow_id[jj] = phdr->rows[jj];
-      }
-      const int units = K / 8;  // 16-byte units per row
-      for (int u = warp * 32 + lane; u < ntok * units; u += Q * 32) {
-        const int r = u / units, cu = u - r * units;
-        uint4* pa = reinterpret_cast<uint4*>(panel + r * prow + cu * 16);
-        const uint4 v = *pa;
-        const float sc = ldexpf(1.0f, phdr->aexp[r]);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+        aexp[jj] = 0;
+        if (jj < ntok) {
+          float m = smax[jj];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(in[t] & 0xffffu) * sc, bf16_bits_to_f32(in[t] >> 16) * sc);
-          o[t] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int w = 1; w < Q; ++w) m = fmaxf(m, smax[w * G + jj]);
+          aexp[jj] = act_exponent(__float_as_uint(m));
         }
-        *pa = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      for (int r = 0; r < ntok; ++r) {
+        int er = 0;
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+          if (jj == r) er = aexp[jj];
+        const float sc = ldexpf(1.0f, er);
+        for (int u = warp * 32 + lane; u < units; u += Q * 32) {
+          uint4* pa = reinterpret_cast<uint4*>(panel + r * prow + u * 16);
+          const uint4 v = *pa;
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(in[t] & 0xffffu) * sc, bf16_bits_to_f32(in[t] >> 16) * sc);
+            o[t] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *pa = make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
       if (!mbar_wait(pready, pseq & 1, a.st, 8)) break;
+      act_row = smem_u32(panel) + (g < G ? g : 0) * prow + q * 16;
       ++pseq;
     }
     float acc[2][2][NV];  // [mtile][lo/hi row][token column]
@@ -509,7 +593,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       // panel reads (and this warp's conversion writes) come before the next bulk copy into it
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(pempty);
+      if (lane == 0) mbar_arrive(&pempty[(pseq - 1) % NP]);
     }
     // partials to the epilogue warp (double-buffered by item parity)
     const int pb = j & 1;

@@ -57,52 +57,86 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
   __syncthreads();
   const int it0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
-  // The weights depend on nothing earlier in the stream: start pulling this
-  // CTA's rows into L2 before waiting on the preceding kernel.
-  if (warp == W && lane == 0) {
-    int last_mt = -1;
-    for (int it = it0; it < it1; ++it) {
-      const int mt = it % mtiles;
-      if (mt != last_mt) prefetch_l2_range(a.w + (size_t)mt * 16 * K, (size_t)16 * K * 2);
-      last_mt = mt;
-    }
-  }
-  pdl_wait();
-  pdl_trigger();
+  const int mode = a.wait_mode;
 
   if (warp == W) {
-    if (lane != 0) return;
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
-    const uint64_t pol = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
-    int seq[W];
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+      const uint64_t pol = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      // Chunk c of an item goes to consumer warp c % W; chunks are issued in
+      // (item, chunk) order.  With kWaitAfterWeights the weight copies of the
+      // first chunks (while their warps' slots are still unused) go out before
+      // the wait and their token rows after it.
+      int seq[W];
 #pragma unroll
-    for (int w = 0; w < W; ++w) seq[w] = 0;
-    bool ok = true;
-    for (int it = it0; it < it1 && ok; ++it) {
-      // token group outer, row tile inner: consecutive items share tokens
-      const int tg = it / mtiles, mt = it % mtiles;
-      for (int c = 0; c < nch; ++c) {
-        const int w = c % W;
-        const int d = seq[w] % D;
-        const uint32_t par = ((seq[w] / D) & 1) ^ 1;
-        ++seq[w];
-        if (!mbar_wait(&empty[w * D + d], par, a.st, 11)) {
-          ok = false;
-          break;
-        }
-        uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
-        uint64_t* bar = &full[w * D + d];
-        mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // out-of-range token rows are zero-filled, bytes still count
-        tma_load_3d(slot, &tm_w, 0, mt * 16, c * (kGemvKC / 64), bar, pol);
-        tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * (kGemvKC / 64), bar, pol_x);
+      for (int w = 0; w < W; ++w) seq[w] = 0;
+      int npre = 0;
+      if (mode == kWaitAfterWeights) {
+        bool room = true;
+        for (int it = it0; it < it1 && room; ++it)
+          for (int c = 0; c < nch; ++c) {
+            const int w = c % W;
+            if (seq[w] >= D) {
+              room = false;
+              break;
+            }
+            const int d = seq[w]++;
+            uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
+            uint64_t* bar = &full[w * D + d];
+            mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // token rows follow after the wait
+            tma_load_3d(slot, &tm_w, 0, (it % mtiles) * 16, c * (kGemvKC / 64), bar, pol);
+            ++npre;
+          }
+#pragma unroll
+        for (int w = 0; w < W; ++w) seq[w] = 0;
       }
-    }
+      if (mode != kWaitAtEnd) {
+        pdl_wait();
+        pdl_trigger();
+      }
+      bool ok = true;
+      int lin = 0;
+      for (int it = it0; it < it1 && ok; ++it) {
+        // token group outer, row tile inner: consecutive items share tokens
+        const int tg = it / mtiles, mt = it % mtiles;
+        for (int c = 0; c < nch; ++c, ++lin) {
+          const int w = c % W;
+          const int d = seq[w] % D;
+          const uint32_t par = ((seq[w] / D) & 1) ^ 1;
+          ++seq[w];
+          uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
+          uint64_t* bar = &full[w * D + d];
+          if (lin >= npre) {
+            if (!mbar_wait(&empty[w * D + d], par, a.st, 11)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // out-of-range token rows are zero-filled, bytes still count
+            tma_load_3d(slot, &tm_w, 0, mt * 16, c * (kGemvKC / 64), bar, pol);
+          }
+          tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * (kGemvKC / 64), bar, pol_x);
+        }
+      }
 #pragma unroll
-    for (int w = 0; w < W; ++w)
-      for (int s = max(0, seq[w] - D); s < seq[w]; ++s) mbar_wait(&full[w * D + (s % D)], (s / D) & 1, a.st, 12);
+      for (int w = 0; w < W; ++w)
+        for (int s = max(0, seq[w] - D); s < seq[w]; ++s) mbar_wait(&full[w * D + (s % D)], (s / D) & 1, a.st, 12);
+    }
+    // The other lanes wait for lane 0 here: a lane parked in griddepcontrol.wait
+    // would hold the whole warp, lane 0's copies included, until the preceding
+    // kernel completes.
+    __syncwarp();
+    if (mode == kWaitAtEnd) {
+      pdl_wait();
+      pdl_trigger();
+    }
     return;
+  }
+  // consumers read only shared memory and write outputs nothing earlier in the stream touches
+  if (mode != kWaitAtEnd) {
+    pdl_wait();
+    pdl_trigger();
   }
 
   const int g = lane >> 2, q = lane & 3;
@@ -175,18 +209,14 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
             o[g] = b_lo;
             o[g + 8] = b_hi;
           }
-          if (a.col_max) {
-            // max |out| of this token over the tile's 16 rows, folded into the token's max word
-            float mv = fmaxf(fabsf(bf16_bits_to_f32(b_lo)), fabsf(bf16_bits_to_f32(b_hi)));
-            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 4));
-            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 8));
-            mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, 16));
-            if (g == 0 && tok < ntok) atomicMax(&a.col_max[t0 + tok], __float_as_uint(mv));
-          }
         }
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+  }
+  if (mode == kWaitAtEnd) {
+    pdl_wait();
+    pdl_trigger();
   }
 }
 

@@ -14,7 +14,7 @@ __global__ void topk_kernel(const float* part, int nsplit, const float* bias, in
 __global__ void route_small_kernel(const uint16_t* x, const float* wr, const float* bias, float* part, int T, int H,
                                    int E, int k, int split_len, int G, int32_t* topk_idx, float* topk_w,
                                    int32_t* offsets, int32_t* sorted_rows, int32_t* row_pos, int4* groups,
-                                   int32_t* n_groups, int32_t* ticket, Status* st);
+                                   int32_t* n_groups, int32_t* tickets, Status* st);
 __global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3);
 __global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32_t* offsets, int32_t* sorted_rows,
                              int32_t* row_pos, int4* groups, int32_t* n_groups, Status* st);
@@ -26,7 +26,6 @@ struct ExpertArgs {
   const uint8_t* q;         // codes [E][rows_per_expert][K/2]
   const uint8_t* s;         // scales [E][rows_per_expert][K/32]
   const uint16_t* act;      // bf16 activations, row-major [*][K] (x_lat by token, or h by sorted position)
-  const uint32_t* act_max;  // per activation row: max |value| as fp32 bits
   const int4* groups;       // group list
   const int32_t* n_groups;  // device count of groups
   const int32_t* sorted_rows;
@@ -37,10 +36,11 @@ struct ExpertArgs {
   int top_k;
   int n_experts;
   uint16_t* h_out;          // gate/up: bf16 [R_sorted][I]
-  uint32_t* h_max;          // gate/up: per sorted row, atomic max of |h| as fp32 bits (zeroed by the caller)
   float* y_out;             // down: fp32 [R][L] by original row id
   float* ssq_out;           // down: fp32 [R][L/32] sum of y^2 per 32-row tile (may be null)
   Status* st;
+  int early;                // 1: the group list comes from a kernel before the preceding one, so the
+                            // first weights stream before the programmatic-launch wait; 0: wait first
 };
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms);
@@ -48,13 +48,19 @@ int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int n
 int expert_max_group(int T);
 
 // ---- gemv.cu --------------------------------------------------------------
+// When the kernel waits for the preceding kernel of the stream (programmatic
+// dependent launch): before anything (0); after issuing the weight copies of its
+// first ring slots, which depend on nothing earlier (1); at its very end, the
+// whole projection depending on nothing earlier in the stream (2).
+enum { kWaitFirst = 0, kWaitAfterWeights = 1, kWaitAtEnd = 2 };
+
 struct GemvArgs {
   const uint16_t* w;    // bf16 [N][K]
   const uint16_t* act;  // bf16 [T][K]
   uint16_t* out;        // bf16 [T][N]
-  uint32_t* col_max;    // optional: per token, atomic max of |out| as fp32 bits (zeroed by the caller)
   int N, K, T;
   Status* st;
+  int wait_mode;        // kWaitFirst, kWaitAfterWeights or kWaitAtEnd
 };
 int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 
@@ -63,7 +69,6 @@ int launch_gemv_bf16(const GemvArgs& a, cudaStream_t s, int num_sms);
 // A, B, out 16-byte aligned.
 struct TcGemmArgs {
   uint16_t* out;        // bf16 [M][N] (unless out_f32 is set)
-  uint32_t* row_max;    // optional: per row, atomic max of |out| as fp32 bits (zeroed by the caller)
   int M, N, K;
   Status* st;
   float* out_f32;       // optional: fp32 partial sums [nsplit][M][N] instead of bf16 out
@@ -103,7 +108,6 @@ __global__ void gather_rows_kernel(const uint16_t* x_lat, const int32_t* sorted_
 __global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* scales, int nblocks, uint16_t* out);
 
 // ---- misc.cu --------------------------------------------------------------
-__global__ void row_max_kernel(const uint16_t* in, int K, uint32_t* row_max);
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
                                            int4* groups, int32_t* n_groups, Status* st);
 __global__ void ssq_kernel(const float* y, int R, int L, float* ssq);

@@ -1,45 +1,10 @@
-// Small kernels around the streaming ones: activation preparation, the group
-// list for caller-supplied routing tables, post_expert_norm + weighted sum,
-// and the E2M1 conversion self-test.
+// Small kernels around the streaming ones: the group list for caller-supplied
+// routing tables, post_expert_norm + weighted sum, and the E2M1 conversion
+// self-test.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace lmoe {
-
-__device__ __forceinline__ float block_max_256(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float m = red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
-  __syncthreads();
-  return m;
-}
-
-// One CTA (256 threads) per row: row_max[row] = max |x| over the bf16 row, as
-// fp32 bits (the expert kernels derive each row's f16 scaling from it).
-__global__ void __launch_bounds__(256) row_max_kernel(const uint16_t* __restrict__ in, int K,
-                                                      uint32_t* __restrict__ row_max) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float red[8];
-  const size_t row = blockIdx.x;
-  const uint4* src = reinterpret_cast<const uint4*>(in + row * K);
-  float m = 0.f;
-  for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      m = fmaxf(m, fabsf(bf16_bits_to_f32(w[j] & 0xffffu)));
-      m = fmaxf(m, fabsf(bf16_bits_to_f32(w[j] >> 16)));
-    }
-  }
-  m = block_max_256(m, red);
-  if (threadIdx.x == 0) row_max[row] = __float_as_uint(m);
-}
 
 // Group list (groups of <= G rows per expert) from a caller-supplied table,
 // with the table checked: offsets[0] == 0, monotone, offsets[E] == R, and

@@ -312,9 +312,14 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
 
 // ---------------------------------------------------------------------------
 // Small-T routing in one launch: the router partials of router_partial_kernel
-// (same grid), and the last CTA to finish -- it sees every partial -- sums
-// them in split order, selects the top k of every token and builds the
-// table.  Requires T <= 64 (the last CTA's warps take the tokens in turn).
+// (same grid), then two levels of "last CTA finishes":
+//  1. per (32-expert block, 8-token block): the last of its split CTAs sums
+//     the block's partials in split order (+ bias) into final logits, stored
+//     over split 0 of the partials (it alone reads or writes that block);
+//  2. the last block to finish level 1 selects the top k of every token (one
+//     warp per token, in turns) and builds the table.
+// tickets[0] counts level 2, tickets[1 + block] level 1; all start at zero.
+// Requires T <= 16 (at most 16 level-1 blocks).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                                                           const float* __restrict__ bias, float* __restrict__ part,
@@ -323,15 +328,31 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
                                                           int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ sorted_rows,
                                                           int32_t* __restrict__ row_pos, int4* __restrict__ groups,
-                                                          int32_t* __restrict__ n_groups, int32_t* ticket,
+                                                          int32_t* __restrict__ n_groups, int32_t* tickets,
                                                           Status* st) {
   router_partial_body(x, wr, part, T, H, E, split_len);
   __shared__ int s_last;
+  const int blk = blockIdx.y * gridDim.x + blockIdx.x;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this CTA's partials before its ticket
-    const int total = gridDim.x * gridDim.y * gridDim.z;
-    s_last = (atomicAdd(ticket, 1) == total - 1);
+    s_last = (atomicAdd(&tickets[1 + blk], 1) == (int)gridDim.z - 1);
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  {
+    // thread (u, el): token blockIdx.y*8 + u, expert blockIdx.x*32 + el
+    const int t = blockIdx.y * kRouterTok + (threadIdx.x >> 5), e = blockIdx.x * 32 + (threadIdx.x & 31);
+    if (t < T && e < E) {
+      const float v = token_logit(part, gridDim.z, bias, T, E, t, e);
+      __stcg(part + (size_t)t * E + e, v);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this block's logits before the level-2 ticket
+    s_last = (atomicAdd(&tickets[0], 1) == (int)(gridDim.x * gridDim.y) - 1);
     if (s_last) __threadfence();
   }
   __syncthreads();
@@ -340,10 +361,14 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
   __shared__ TableSmem<256> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t0 = 0; t0 < T; t0 += 8) {
-    // every thread sums one expert's split partials for up to 8 tokens (independent loads)
-    if (threadIdx.x < E)
-      for (int u = 0; u < 8 && t0 + u < T; ++u)
-        s_lg[u][threadIdx.x] = token_logit(part, gridDim.z, bias, T, E, t0 + u, threadIdx.x);
+    // thread e loads expert e's final logit of up to 8 tokens (independent loads)
+    if (threadIdx.x < E) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (t0 + u < T) ? __ldcg(part + (size_t)(t0 + u) * E + threadIdx.x) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s_lg[u][threadIdx.x] = v[u];
+    }
     __syncthreads();
     if (t0 + warp < T)
       topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)(t0 + warp) * k, topk_w + (size_t)(t0 + warp) * k, lane);

@@ -150,7 +150,6 @@ __global__ void __launch_bounds__(256, 1)
       if (!mbar_wait(&accf[acc], aph, a.st, 26)) break;
       tc_fence_after();
       const int row = mt * kTM + wq * 32 + lane;
-      float rmax = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < n_tile / 32; ++ch) {
         uint32_t r[32];
@@ -171,7 +170,6 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < 16; ++i) {
           const uint16_t lo = f32_to_bf16_bits(__uint_as_float(r[2 * i]));
           const uint16_t hi = f32_to_bf16_bits(__uint_as_float(r[2 * i + 1]));
-          rmax = fmaxf(rmax, fmaxf(fabsf(bf16_bits_to_f32(lo)), fabsf(bf16_bits_to_f32(hi))));
           o[i] = (uint32_t)lo | ((uint32_t)hi << 16);
         }
         if (row < a.M) {
@@ -189,7 +187,6 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[acc]);
-      if (a.row_max && row < a.M) atomicMax(&a.row_max[row], __float_as_uint(rmax));
       if (++acc == 2) {
         acc = 0;
         aph ^= 1;

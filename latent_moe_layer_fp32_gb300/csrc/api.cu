@@ -74,6 +74,30 @@ int dev_info(DevInfo* out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A second stream per host thread and device, forked from and joined back to
+// the caller's stream with events, so that independent steps of one call run
+// side by side (the many-token routing next to the pooler).  Created on first
+// use and kept for the life of the thread.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+int side_stream(SideStream** out) {
+  thread_local SideStream side[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ECUDA;
+  SideStream& ss = side[dev & 63];
+  if (ss.s == nullptr) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return LMOE_ECUDA;
+  }
+  *out = &ss;
+  return LMOE_OK;
+}
+
 // The small kernels (routing, combine, helpers) prefer the largest shared-memory
 // carveout: an SM configured for them can then also host a CTA of the weight-
 // streaming kernel launched behind them (up to ~200 KB of shared memory), which
@@ -86,6 +110,8 @@ int set_carveouts() {
   const void* fns[] = {
       reinterpret_cast<const void*>(route_small_kernel), reinterpret_cast<const void*>(router_partial_kernel),
       reinterpret_cast<const void*>(topk_kernel),        reinterpret_cast<const void*>(table_kernel),
+      reinterpret_cast<const void*>(topk_hist_kernel),   reinterpret_cast<const void*>(table_scan_kernel),
+      reinterpret_cast<const void*>(table_scatter_kernel),
       reinterpret_cast<const void*>(combine_kernel),     reinterpret_cast<const void*>(ssq_kernel),
       reinterpret_cast<const void*>(groups_from_offsets_kernel),
       reinterpret_cast<const void*>(gather_rows_kernel), reinterpret_cast<const void*>(router_split_kernel)};
@@ -123,7 +149,7 @@ int router_splits(const lmoe_dims* d, int sms) {
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, route_count, zero_bytes, groups, part, h, ssq, xs, wr3;
+  size_t n_groups, route_count, zero_bytes, groups, part, h, ssq, xs, wr3, rank, chunk;
   int nsplit;
 };
 
@@ -150,6 +176,8 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->pub.sorted_rows = take(4 * R);
   w->pub.row_pos = take(4 * R);
   w->groups = take(16 * (R + E + 1));
+  w->rank = take(4 * R);                                        // many-token table: row rank in its chunk and expert
+  w->chunk = take(4 * ((T + kChunkTok - 1) / kChunkTok) * E);  // per chunk and expert: count, then base position
   w->part = take(4 * (size_t)16 * T * E);
   w->pub.x_lat = take(2 * T * L);
   w->h = take(2 * R * I);
@@ -228,7 +256,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   if (router_tc(d)) {
     // logits on the tensor cores: x (bf16) against the three bf16 parts of Wr, split-K partials
     uint16_t* w3 = at<uint16_t>(ws, w.wr3);
-    LAUNCH(dim3(2 * di.sms), dim3(256), s, router_split_kernel, router_w, E, H, w3);
+    LAUNCH(dim3((H + 1023) / 1024, E), dim3(256), s, router_split_kernel, router_w, E, H, w3);
     const int kblocks = 3 * H / 64, tiles_m = (T + 127) / 128;
     nsplit = 1;
     for (int c = 16; c >= 2; --c)
@@ -252,10 +280,15 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T,
            H, E, H / w.nsplit);
   }
-  LAUNCH(dim3(T), dim3(256), s, topk_kernel, (const float*)part, nsplit, router_bias, T, E, k, topk_idx,
-         topk_w);
-  LAUNCH(dim3(1), dim3(1024), s, table_kernel, (const int32_t*)topk_idx, T * k, E, group_rows(T), offsets,
-         sorted_rows, row_pos, at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), st);
+  const int R = T * k, nchunks = (T + kChunkTok - 1) / kChunkTok;
+  int32_t* rank = at<int32_t>(ws, w.rank);
+  int32_t* chunk = at<int32_t>(ws, w.chunk);
+  LAUNCH(dim3(nchunks), dim3(1024), s, topk_hist_kernel, (const float*)part, nsplit, router_bias, T, E, k, topk_idx,
+         topk_w, rank, chunk);
+  LAUNCH(dim3(1), dim3(256), s, table_scan_kernel, chunk, nchunks, E, R, group_rows(T), offsets,
+         at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups));
+  LAUNCH(dim3((R + 255) / 256), dim3(256), s, table_scatter_kernel, (const int32_t*)topk_idx, (const int32_t*)rank,
+         (const int32_t*)chunk, R, E, k, sorted_rows, row_pos);
   return LMOE_OK;
 }
 
@@ -480,17 +513,27 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   uint16_t* x_lat = at<uint16_t>(ws, w.pub.x_lat);
   float* y = at<float>(ws, w.pub.y);
   Status* st = at<Status>(ws, w.pub.status);
-  CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets), srows,
-                  at<int32_t>(ws, w.pub.row_pos), ws, s));
-  // with both the pooler and the experts on the tensor cores, the pooler's epilogue
-  // also writes x_lat in expert-sorted order (no separate gather)
-  const bool scatter = experts_tc(d->T) && d->T >= t_dense_min_t;
-  // The pooler depends only on x and its weights, so in the decode regime it runs
-  // alongside the routing kernels and waits for them only at its end.
-  CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s,
-                 scatter ? at<int32_t>(ws, w.pub.row_pos) : nullptr, scatter ? at<uint16_t>(ws, w.xs) : nullptr,
-                 kWaitAtEnd));
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, scatter, true));
+  // The pooler depends only on x and its weights.  Small T: it runs alongside the
+  // one-launch routing and waits for it only at its end (programmatic launch).
+  // Many tokens: the routing kernels run on a side stream next to it.
+  const bool fork = d->T > 16;
+  if (fork) {
+    SideStream* ss = nullptr;
+    CHECK(side_stream(&ss));
+    if (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+      return LMOE_ECUDA;
+    CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
+                    srows, at<int32_t>(ws, w.pub.row_pos), ws, ss->s));
+    if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return LMOE_ECUDA;
+    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
+    if (cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) return LMOE_ECUDA;
+  } else {
+    CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
+                    srows, at<int32_t>(ws, w.pub.row_pos), ws, s));
+    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
+  }
+  // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);
 }

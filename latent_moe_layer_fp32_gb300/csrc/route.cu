@@ -89,7 +89,7 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // Writes topk_idx[k], topk_w[k] for the token (softmax over all E,
 // renormalised over the k picks; ties to the lower expert index).
 __device__ __forceinline__ void topk_one_token(const float* lg_s, int E, int k, int32_t* topk_idx, float* topk_w,
-                                               int lane) {
+                                               int lane, int* s_pick = nullptr) {
   float lg[8];
   bool taken[8];
 #pragma unroll
@@ -149,6 +149,7 @@ __device__ __forceinline__ void topk_one_token(const float* lg_s, int E, int k, 
   if (lane < k) {
     topk_idx[lane] = e;
     topk_w[lane] = p / den;
+    if (s_pick) s_pick[lane] = e;
   }
 }
 
@@ -391,19 +392,178 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
                                                            uint16_t* __restrict__ w3) {
   pdl_wait();
   pdl_trigger();
-  const size_t n = (size_t)E * H;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t e = i / H, h = i % H;
-    const float w = wr[i];
-    const uint32_t b1 = __float_as_uint(w) >> 16;
-    const float r1 = w - __uint_as_float(b1 << 16);
-    const uint32_t b2 = __float_as_uint(r1) >> 16;
-    const float r2 = r1 - __uint_as_float(b2 << 16);
-    uint16_t* row = w3 + e * 3 * H;
-    row[h] = (uint16_t)b1;
-    row[H + h] = (uint16_t)b2;
-    row[2 * H + h] = f32_to_bf16_bits(r2);
+  // block (x, e): columns [x * 1024, x * 1024 + 1024) of expert row e, four per thread
+  const int e = blockIdx.y, h = (blockIdx.x * 256 + threadIdx.x) * 4;
+  if (h >= H) return;
+  const float4 w4 = *reinterpret_cast<const float4*>(wr + (size_t)e * H + h);
+  const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+  uint32_t p1[2], p2[2], p3[2];
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    uint32_t b1[2], b2[2], b3[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float w = wv[i + u];
+      b1[u] = __float_as_uint(w) >> 16;
+      const float r1 = w - __uint_as_float(b1[u] << 16);
+      b2[u] = __float_as_uint(r1) >> 16;
+      const float r2 = r1 - __uint_as_float(b2[u] << 16);
+      b3[u] = f32_to_bf16_bits(r2);
+    }
+    p1[i / 2] = b1[0] | (b1[1] << 16);
+    p2[i / 2] = b2[0] | (b2[1] << 16);
+    p3[i / 2] = b3[0] | (b3[1] << 16);
   }
+  uint16_t* row = w3 + (size_t)e * 3 * H;
+  *reinterpret_cast<uint2*>(row + h) = make_uint2(p1[0], p1[1]);
+  *reinterpret_cast<uint2*>(row + H + h) = make_uint2(p2[0], p2[1]);
+  *reinterpret_cast<uint2*>(row + 2 * H + h) = make_uint2(p3[0], p3[1]);
+}
+
+// ---------------------------------------------------------------------------
+// Routing for many tokens, in three launches (no single-CTA pass over all rows):
+//  1. topk_hist_kernel: chunks of 32 tokens (k*32 rows), one warp per token:
+//     logits from the split partials (split order, + bias), the top k,
+//     then each row's stable rank among the chunk's rows of its expert and the
+//     chunk's per-expert counts;
+//  2. table_scan_kernel (one CTA): per expert, offsets and the base position of
+//     every chunk's rows (counts replaced in place), the group list;
+//  3. table_scatter_kernel: sorted_rows[pos] = r, row_pos[r] = pos with
+//     pos = base[chunk][expert] + rank.
+// Row ids r = t*k + j keep their order inside an expert (the table is the same
+// stable counting sort as build_table).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) topk_hist_kernel(const float* __restrict__ part, int nsplit,
+                                                         const float* __restrict__ bias, int T, int E, int k,
+                                                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                         int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float s_lg[kChunkTok][256];
+  __shared__ int s_pick[kChunkTok * 8];
+  __shared__ int s_wcnt[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kChunkTok;
+  const int ntok = min(kChunkTok, T - t0);
+  for (int i = threadIdx.x; i < 8 * 256; i += 1024) (&s_wcnt[0][0])[i] = 0;
+  if (warp < ntok) {
+    // warp w takes token t0 + w; lane takes experts lane + 32 i, every load before the stores
+    const int t = t0 + warp;
+    float lg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      lg[i] = e < E ? token_logit(part, nsplit, bias, T, E, t, e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < E) s_lg[warp][lane + 32 * i] = lg[i];
+    __syncwarp();
+    topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, lane, s_pick + warp * k);
+  }
+  __syncthreads();
+  // stable rank of each of the chunk's rows among its expert's rows (row order);
+  // threads 0..255 (warps 0-7) take local rows 0..255 (k * 32 <= 256)
+  const int nrow = ntok * k;
+  const int i = threadIdx.x;
+  int e = 0, rk = 0;
+  if (warp < 8) {
+    e = i < nrow ? s_pick[i] : -1 - lane;  // rows past the end match nothing
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    rk = __popc(same & ((1u << lane) - 1u));
+    if (i < nrow && rk == 0) s_wcnt[warp][e] = __popc(same);
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = s_wcnt[w][threadIdx.x];
+      s_wcnt[w][threadIdx.x] = acc;
+      acc += c;
+    }
+    chunk_cnt[(size_t)blockIdx.x * E + threadIdx.x] = acc;
+  }
+  __syncthreads();
+  if (warp < 8 && i < nrow) rank[(size_t)t0 * k + i] = s_wcnt[warp][e] + rk;
+}
+
+__global__ void __launch_bounds__(256) table_scan_kernel(int32_t* __restrict__ chunk_cnt, int nchunks, int E, int R,
+                                                         int G, int32_t* __restrict__ offsets,
+                                                         int4* __restrict__ groups, int32_t* __restrict__ n_groups) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_off[257], s_goff[257];
+  const int e = threadIdx.x, warp = e >> 5, lane = e & 31;
+  // chunk counts in batches of 8 independent loads
+  int total = 0;
+  if (e < E)
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < nchunks ? __ldcg(chunk_cnt + (size_t)(c0 + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) total += v[j];
+    }
+  const int gcnt = (total + G - 1) / G;
+  // exclusive scans over experts (256 threads: warp scans, then warp totals)
+  __shared__ int s_wr[8], s_wg[8];
+  int rx = total, gx = gcnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ry = __shfl_up_sync(0xffffffffu, rx, o), gy = __shfl_up_sync(0xffffffffu, gx, o);
+    if (lane >= o) {
+      rx += ry;
+      gx += gy;
+    }
+  }
+  if (lane == 31) {
+    s_wr[warp] = rx;
+    s_wg[warp] = gx;
+  }
+  __syncthreads();
+  int rbase = 0, gbase = 0;
+  for (int w = 0; w < warp; ++w) {
+    rbase += s_wr[w];
+    gbase += s_wg[w];
+  }
+  const int off = rbase + rx - total, goff = gbase + gx - gcnt;
+  if (e < E) {
+    offsets[e] = off;
+    int acc = off;
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < nchunks ? __ldcg(chunk_cnt + (size_t)(c0 + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < nchunks) {
+          chunk_cnt[(size_t)(c0 + j) * E + e] = acc;  // base position of chunk c's rows of expert e
+          acc += v[j];
+        }
+    }
+    int gi = goff;
+    for (int g0 = 0; g0 < total; g0 += G) groups[gi++] = make_int4(e, off + g0, min(G, total - g0), 0);
+  }
+  if (e == E - 1) {
+    offsets[E] = off + total;  // = R
+    *n_groups = goff + gcnt;
+  }
+}
+
+__global__ void __launch_bounds__(256) table_scatter_kernel(const int32_t* __restrict__ topk_idx,
+                                                            const int32_t* __restrict__ rank,
+                                                            const int32_t* __restrict__ chunk_base, int R, int E,
+                                                            int k, int32_t* __restrict__ sorted_rows,
+                                                            int32_t* __restrict__ row_pos) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x * 256 + threadIdx.x;
+  if (r >= R) return;
+  const int e = topk_idx[r], c = (r / k) / kChunkTok;
+  const int pos = chunk_base[(size_t)c * E + e] + rank[r];
+  sorted_rows[pos] = r;
+  row_pos[r] = pos;
 }
 
 }  // namespace lmoe

@@ -8,7 +8,9 @@
 // elements) and bf16 activations, fp32 accumulation.
 //
 // One work item = one group of up to 160 rows of one expert (sorted
-// positions p0 .. p0+n-1) x one 128-row tile of the expert's output features.
+// positions p0 .. p0+n-1) x output features: one 128-row tile of the gate and
+// of the up half (gate/up), or two consecutive 128-row tiles (down), so every
+// activation stage feeds two MMAs.
 // The weight tile is the MMA's A operand (M = 128), the group's activation
 // rows are B (N = n rounded up to 16), so ragged groups cost no padded rows
 // of A.  Per CTA (persistent, one per SM, 19 warps):
@@ -25,7 +27,8 @@
 //               per-32-column sums of squares for post_expert_norm (down);
 //               two warps per TMEM lane quarter take alternate 32-column chunks
 // Tensor memory (512 columns): accumulators of 160 columns (gate/up: gate at
-// 0, up at 160, so SwiGLU pairs are lane-local; down: two buffers), and from
+// 0, up at 160, so SwiGLU pairs are lane-local; down: the item's two 128-row
+// output tiles at 0 and 160, or with one tile per item two buffers), and from
 // column 320 the A stages, 32 columns (64 K of bf16) per weight matrix.
 #include <atomic>
 
@@ -55,11 +58,16 @@ struct XCfg<0> {  // gate/up: two weight matrices per item, single accumulator p
   static constexpr int NMAT = 2, RAW = 3, ST = 3, NACC = 1;
 };
 template <>
-struct XCfg<1> {  // down: one weight matrix, double-buffered accumulator
+struct XCfg<1> {  // down, one 128-row output tile per item: double-buffered accumulator
   static constexpr int NMAT = 1, RAW = 4, ST = 6, NACC = 2;
+};
+template <>
+struct XCfg<2> {  // down, two 128-row output tiles per item sharing each activation stage
+  static constexpr int NMAT = 2, RAW = 3, ST = 3, NACC = 1;
 };
 static_assert(kXACol + XCfg<0>::ST * XCfg<0>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
 static_assert(kXACol + XCfg<1>::ST * XCfg<1>::NMAT * 32 <= 512 && XCfg<1>::NACC * kXAcc <= kXACol, "TMEM columns");
+static_assert(kXACol + XCfg<2>::ST * XCfg<2>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
 
 template <int MODE>
 constexpr int xring_bytes() {
@@ -70,7 +78,8 @@ template <int MODE>
 constexpr int xsmem_bytes() {
   return xring_bytes<MODE>() + 1024 + 256;
 }
-static_assert(xsmem_bytes<0>() <= 232448 && xsmem_bytes<1>() <= 232448, "shared memory budget");
+static_assert(xsmem_bytes<0>() <= 232448 && xsmem_bytes<1>() <= 232448 && xsmem_bytes<2>() <= 232448,
+              "shared memory budget");
 
 // ---------------------------------------------------------------------------
 // MXFP4 -> bf16.  E2M1 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 have bf16 bit
@@ -224,7 +233,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int nft = (MODE == 0 ? a.inter : a.latent) / kXM;  // feature tiles per group
+  // rows of the weight matrix per item and matrix tile m: gate/up: tile ft of the gate
+  // (m = 0) and up (m = 1) halves; down: tile ft (MODE 1) or 128-row tiles 2 ft, 2 ft + 1
+  constexpr int TPI = MODE == 2 ? 2 : 1;                            // output tiles per item
+  const int nft = (MODE == 0 ? a.inter : a.latent) / (kXM * TPI);  // items per group
   const int n_items = *a.n_groups * nft;
   const int K = a.K, nks = K / 64, nkr = K / 256;
   const int rows_pe = MODE == 0 ? 2 * a.inter : a.latent;  // weight rows per expert
@@ -251,7 +263,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
 #pragma unroll
           for (int m = 0; m < C::NMAT; ++m)
             tma_load_2d(s_raw + (rs * C::NMAT + m) * kXTile, &tm_q, kr * 128,
-                        x.e * rows_pe + m * a.inter + x.ft * kXM, &raw_full[rs], pol);
+                        x.e * rows_pe + (MODE == 0 ? m * a.inter + x.ft * kXM : (x.ft * TPI + m) * kXM),
+                        &raw_full[rs], pol);
           ++issued;
           if (++rs == C::RAW) {
             rs = 0;
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(kXM, (x.n + 15) & ~15);
         if (!mbar_wait(&acc_empty[acc], cph ^ 1, a.st, 65)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
+        const uint32_t d = tmem + (MODE == 1 ? (uint32_t)acc * kXAcc : 0u);
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(&full[as], aph, a.st, 66)) {
             ok = false;
@@ -356,16 +369,17 @@ __global__ void __launch_bounds__(kXThreads, 1)
   } else if (warp < 3 + kDqWarps) {
     // ---------------- dequantisation: codes -> bf16 A stages in TMEM ----------------
     // A warp may only touch the TMEM lanes of its quarter (warp % 4): warp w
-    // handles rows 32 (w % 4) .. +31.  Gate/up: warps 3-6 the gate tile, 7-10 the
-    // up tile, both 32-blocks of each 64-K step; down: warps 3-6 the first and
-    // 7-10 the second 32-block of each step.
+    // handles rows 32 (w % 4) .. +31.  Two tiles per item (gate/up; down in
+    // MODE 2): warps 3-6 the first tile, 7-10 the second, both 32-blocks of each
+    // 64-K step; one tile (MODE 1): warps 3-6 the first and 7-10 the second
+    // 32-block of each step.
     const int dw = warp - 3, q = warp & 3;
-    const int m = MODE == 0 ? dw >> 2 : 0;
-    const int b_only = MODE == 0 ? 0 : dw >> 2;
+    const int m = C::NMAT == 2 ? dw >> 2 : 0;
+    const int b_only = C::NMAT == 2 ? 0 : dw >> 2;
     const int rr = q * 32 + lane;
     const int sw = rr & 7;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    constexpr int NB = MODE == 0 ? 2 : 1;
+    constexpr int NB = C::NMAT == 2 ? 2 : 1;
     int rs = 0, as = 0;
     uint32_t rph = 0, aph = 0;
     bool ok = true;
@@ -378,7 +392,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
       g_next = x_group(a, it + gridDim.x, nft, n_items);
       XItem x;
       if (!x_item(a, g_cur, it, nft, &x)) continue;
-      const size_t grow = (size_t)x.e * rows_pe + (size_t)m * a.inter + (size_t)x.ft * kXM + rr;
+      const size_t grow = (size_t)x.e * rows_pe +
+                          (MODE == 0 ? (size_t)m * a.inter + (size_t)x.ft * kXM : (size_t)(x.ft * TPI + m) * kXM) + rr;
       const uint8_t* srow = a.s + grow * (size_t)(K / 32);
       uint2 sc_next = __ldg(reinterpret_cast<const uint2*>(srow));
       for (int kr = 0; kr < nkr && ok; ++kr) {
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           uint32_t o[16 * NB];
 #pragma unroll
           for (int bi = 0; bi < NB; ++bi) {
-            const int b = MODE == 0 ? bi : b_only;
+            const int b = C::NMAT == 2 ? bi : b_only;
             const int kb = 2 * j + b;  // 32-block within the raw stage
             const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
             const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           }
           tc_fence_after();
           const uint32_t acol = tmem + lane_base + kXACol + (uint32_t)(as * C::NMAT + m) * 32u;
-          if (MODE == 0)
+          if (C::NMAT == 2)
             tmem_st32(acol, o);
           else
             tmem_st16(acol + 16u * b_only, o);
@@ -455,8 +470,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (!x_item(a, g_cur, it, nft, &x)) continue;
       if (!mbar_wait_sleep(&acc_full[acc], cph, a.st, 72, 256)) break;
       tc_fence_after();
-      const int f = x.ft * kXM + q * 32 + lane;  // output feature of this lane
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 0 ? 0u : (uint32_t)acc * kXAcc);
+      for (int m = 0; m < TPI; ++m) {
+      const int f = (x.ft * TPI + m) * kXM + q * 32 + lane;  // output feature of this lane
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 1 ? (uint32_t)acc * kXAcc : (uint32_t)m * kXAcc);
       for (int c0 = 32 * half; c0 < x.n; c0 += 64) {
         if (MODE == 0) {
           uint32_t g[32], u[32];
@@ -498,8 +514,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
               s[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
             }
           }
-          if (c0 + lane < x.n) a.ssq_out[(size_t)my_row * (a.latent / 32) + (x.ft * kXM + q * 32) / 32] = s[0];
+          if (c0 + lane < x.n)
+            a.ssq_out[(size_t)my_row * (a.latent / 32) + ((x.ft * TPI + m) * kXM + q * 32) / 32] = s[0];
         }
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -521,7 +539,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
 template <int MODE>
 int launch_tc_expert(const TcExpertArgs& a, const uint16_t* act, cudaStream_t s, int num_sms) {
   const int K = a.K;
-  if (K % 256 || a.inter % kXM || a.latent % kXM) return LMOE_EUNSUPPORTED;
+  if (K % 256 || a.inter % kXM || a.latent % (MODE == 2 ? 2 * kXM : kXM)) return LMOE_EUNSUPPORTED;
   constexpr int smem = xsmem_bytes<MODE>();
   static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
@@ -566,6 +584,8 @@ int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream
 }
 
 int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms) {
+  // two output tiles per item halve the activation traffic per MMA
+  if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2>(a, h, s, num_sms);
   return launch_tc_expert<1>(a, h, s, num_sms);
 }
 

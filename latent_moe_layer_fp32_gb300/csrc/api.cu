@@ -374,6 +374,8 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.K = L;
   a.h_out = at<uint16_t>(ws, w.h);
   a.early = groups_early ? 1 : 0;
+  a.groups_cap = T * k + d->n_experts + 1;
+  a.rows = T * k;
   pre_launch(s, "expert_gateup");
   CHECK(launch_gateup(a, T, G, s, di.sms));
   ++g_launches;
@@ -405,16 +407,17 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
   while (csplit < d->latent / 256 && d->T * csplit < 2 * di.sms) csplit *= 2;
   LAUNCH(dim3(d->T, csplit), dim3(256), s, combine_kernel, y, (const float*)at<float>(ws, w.ssq),
          topk_idx, topk_w, norm_g, d->latent, d->top_k, d->n_experts, d->eps, zb, st);
-  const bool dense = d->T >= t_dense_min_t;
-  pre_launch(s, dense ? "unpool_tc_gemm" : "unpool_gemv");
-  if (dense) {
-    TcGemmArgs g{out, d->T, d->hidden, d->latent, st};
-    CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
-  } else {
+  if (d->T < t_dense_min_t) {
     // the unpooler weights depend on nothing earlier: they stream while the combine finishes
+    pre_launch(s, "unpool_gemv");
     GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st, kWaitAfterWeights};
     CHECK(launch_gemv_bf16(g, s, di.sms));
+    ++g_launches;
+    return LMOE_OK;
   }
+  pre_launch(s, "unpool_tc_gemm");
+  TcGemmArgs g{out, d->T, d->hidden, d->latent, st};
+  CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
   ++g_launches;
   return LMOE_OK;
 }

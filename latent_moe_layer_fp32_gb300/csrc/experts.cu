@@ -228,6 +228,18 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     pdl_trigger();
   }
 
+  // The producer's routing reads in one round trip with the group count: group
+  // entries 0..63 and row ids 0..127 read ahead (as far as allocated); a CTA
+  // whose groups lie beyond them reads those from memory.
+  int4 sg0 = make_int4(0, 0, 0, 0), sg1 = make_int4(0, 0, 0, 0);
+  int sr[4] = {0, 0, 0, 0};
+  if (warp == Q) {
+    if (lane < a.groups_cap) sg0 = a.groups[lane];
+    if (lane + 32 < a.groups_cap) sg1 = a.groups[lane + 32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (lane + 32 * i < a.rows) sr[i] = a.sorted_rows[lane + 32 * i];
+  }
   const int n_items = *a.n_groups * tiles;
   const int it0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
   const int it1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
@@ -240,31 +252,22 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
     }
-    // The routing of this CTA's groups, read once up front (one round trip each):
-    // lane l holds the entry of group g_first + l, and, for groups of up to G
-    // rows, lane l of set s the row id of token l % G of group
-    // g_first + s * (32 / G) + l / G.  Groups past these come from memory.
-    constexpr int GPS = 32 / G;  // groups per set of row ids
-    constexpr int NSET = (G == 1) ? 1 : 2;
-    const int g_first = it0 / tiles;
-    const int g_last = nloc > 0 ? (it1 - 1) / tiles : g_first - 1;
-    int4 ent = make_int4(0, 0, 0, 0);
-    if (g_first + lane <= g_last) ent = a.groups[g_first + lane];
     const int4* groups = a.groups;
-    auto entry = [ent, g_first, groups](int grp) -> int4 {
-      const int off = grp - g_first;
-      if (off < 32) {
-        return make_int4(__shfl_sync(0xffffffffu, ent.x, off), __shfl_sync(0xffffffffu, ent.y, off),
-                         __shfl_sync(0xffffffffu, ent.z, off), 0);
+    auto entry = [sg0, sg1, groups](int grp) -> int4 {  // grp is warp-uniform
+      if (grp < 64) {
+        const int4 v = grp < 32 ? sg0 : sg1;
+        const int src = grp & 31;
+        return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                         __shfl_sync(0xffffffffu, v.z, src), 0);
       }
       return groups[grp];
     };
     int seq = 0, pseq = 0, cur = -1;
     bool ok = true;
-    // codes and scales of chunk c of local item j into the next ring slot
-    auto issue = [&](int j, int c) -> bool {
-      const int it = it0 + j, tile = it % tiles;
-      const int e = entry(it / tiles).x;
+    // codes and scales of chunk c of local item j (expert e) into the next ring
+    // slot; lane 0 waits for the slot and issues all four copies
+    auto issue = [&](int j, int c, int e) -> bool {
+      const int tile = (it0 + j) % tiles;
       // first rows of box A and box B
       int rowA, rowB;
       if (MODE == MODE_GATEUP) {
@@ -277,42 +280,34 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       const int d = seq % D;
       const uint32_t par = ((seq / D) & 1) ^ 1;
       ++seq;
-      int got = 1;
-      if (lane == 0) got = mbar_wait(&empty[d], par, a.st, 1);
-      if (!__shfl_sync(0xffffffffu, got, 0)) return false;
-      uint8_t* slot = smem + d * Lay::kSlot;
-      uint64_t* bar = &full[d];
+      int good = 1;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
-        tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
-        tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
+        good = mbar_wait(&empty[d], par, a.st, 1);
+        if (good) {
+          uint8_t* slot = smem + d * Lay::kSlot;
+          uint64_t* bar = &full[d];
+          mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
+          tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
+          tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
+          uint8_t* sdst = slot + Lay::kCodes;
+          if (nch > 1) {
+            tma_load_2d(sdst, &tm_s, c * nb, rowA, bar, pol);
+            tma_load_2d(sdst + 16 * nb, &tm_s, c * nb, rowB, bar, pol);
+          } else {  // one chunk: the 16 rows' scales are contiguous
+            bulk_g2s(sdst, a.s + (size_t)rowA * Ks, 16 * Ks, bar);
+            bulk_g2s(sdst + 16 * nb, a.s + (size_t)rowB * Ks, 16 * Ks, bar);
+          }
+        }
       }
-      __syncwarp();
-      if (lane == 1 || lane == 2) {
-        uint8_t* sdst = slot + Lay::kCodes + (lane - 1) * 16 * nb;
-        const int srow = lane == 1 ? rowA : rowB;
-        if (nch > 1)
-          tma_load_2d(sdst, &tm_s, c * nb, srow, bar, pol);
-        else  // one chunk: the 16 rows' scales are contiguous
-          bulk_g2s(sdst, a.s + (size_t)srow * Ks, 16 * Ks, bar);
-      }
-      __syncwarp();
-      return true;
+      return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
     // the ring's first D slots are free: fill them before waiting
     int issued = 0;
     const int total = nloc * nch;
     while (a.early && ok && issued < total && issued < D) {
-      ok = issue(issued / nch, issued % nch);
+      const int j = issued / nch;
+      ok = issue(j, issued % nch, entry((it0 + j) / tiles).x);
       ++issued;
-    }
-    int rowv[NSET];
-#pragma unroll
-    for (int st = 0; st < NSET; ++st) {
-      rowv[st] = 0;
-      const int off = st * GPS + lane / G;  // < 32: its entry is in lane `off`
-      const int gy = __shfl_sync(0xffffffffu, ent.y, off), gz = __shfl_sync(0xffffffffu, ent.z, off);
-      if (g_first + off <= g_last && lane % G < gz) rowv[st] = a.sorted_rows[gy + lane % G];
     }
     if (a.early) {
       pdl_wait();
@@ -320,9 +315,10 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     }
     for (int j = 0; j < nloc && ok; ++j) {
       const int it = it0 + j, grp = it / tiles;
+      const int e_item = entry(grp).x;
       for (int c = 0; c < nch && ok; ++c) {
         if (j * nch + c >= issued) {
-          ok = issue(j, c);
+          ok = issue(j, c, e_item);
           ++issued;
           if (!ok) break;
         }
@@ -341,14 +337,16 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
             ok = false;
             break;
           }
-          const int off = grp - g_first;
           int my_row = 0;
-          if (off < NSET * GPS) {
-            int v = 0;
+          if (p0 + ntok <= 128) {  // from the rows read ahead
+            const int idx = (p0 + lane) & 127;
+            int v[4];
 #pragma unroll
-            for (int st = 0; st < NSET; ++st)
-              if (st == off / GPS) v = rowv[st];
-            my_row = __shfl_sync(0xffffffffu, v, ((off % GPS) * G + lane % G) & 31);
+            for (int i = 0; i < 4; ++i) v[i] = __shfl_sync(0xffffffffu, sr[i], idx & 31);
+            my_row = v[0];
+#pragma unroll
+            for (int i = 1; i < 4; ++i)
+              if (idx >> 5 == i) my_row = v[i];
           } else if (lane < ntok) {
             my_row = a.sorted_rows[p0 + lane];
           }

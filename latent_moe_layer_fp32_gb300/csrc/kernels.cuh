@@ -46,6 +46,8 @@ struct ExpertArgs {
   float* y_out;             // down: fp32 [R][L] by original row id
   float* ssq_out;           // down: fp32 [R][L/32] sum of y^2 per 32-row tile (may be null)
   Status* st;
+  int groups_cap;           // entries allocated in groups (read ahead speculatively up to this)
+  int rows;                 // R = T * k: entries of sorted_rows
   int early;                // 1: the group list comes from a kernel before the preceding one, so the
                             // first weights stream before the programmatic-launch wait; 0: wait first
 };

@@ -313,14 +313,17 @@ __global__ void __launch_bounds__(kTableThreads) table_kernel(const int32_t* __r
 
 // ---------------------------------------------------------------------------
 // Small-T routing in one launch: the router partials of router_partial_kernel
-// (same grid), then two levels of "last CTA finishes":
-//  1. per (32-expert block, 8-token block): the last of its split CTAs sums
-//     the block's partials in split order (+ bias) into final logits, stored
-//     over split 0 of the partials (it alone reads or writes that block);
-//  2. the last block to finish level 1 selects the top k of every token (one
-//     warp per token, in turns) and builds the table.
-// tickets[0] counts level 2, tickets[1 + block] level 1; all start at zero.
-// Requires T <= 16 (at most 16 level-1 blocks).
+// (same grid), then "last CTA finishes":
+//  - T <= 2: the last CTA overall sums every (token, expert) logit from its
+//    split partials (split order, + bias) itself;
+//  - T > 2, two levels: per (32-expert block, 8-token block) the last of its
+//    split CTAs sums the block's logits and stores them over split 0 of the
+//    partials (it alone reads or writes that block), and the last block to
+//    finish reads those;
+// then it selects the top k of every token (one warp per token, in turns) and
+// builds the table from the picks it holds in shared memory.
+// tickets[0] counts the last level, tickets[1 + block] the first; all start at
+// zero.  Requires T <= 16 (at most 16 blocks).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                                                           const float* __restrict__ bias, float* __restrict__ part,
@@ -333,49 +336,60 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
                                                           Status* st) {
   router_partial_body(x, wr, part, T, H, E, split_len);
   __shared__ int s_last;
+  const bool one_level = T <= 2;
   const int blk = blockIdx.y * gridDim.x + blockIdx.x;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's partials before its ticket
-    s_last = (atomicAdd(&tickets[1 + blk], 1) == (int)gridDim.z - 1);
-    if (s_last) __threadfence();
-  }
-  __syncthreads();
-  if (!s_last) return;
-  {
+  if (!one_level) {
+    if (threadIdx.x == 0) {
+      __threadfence();  // this CTA's partials before its ticket
+      s_last = (atomicAdd(&tickets[1 + blk], 1) == (int)gridDim.z - 1);
+      if (s_last) __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
     // thread (u, el): token blockIdx.y*8 + u, expert blockIdx.x*32 + el
     const int t = blockIdx.y * kRouterTok + (threadIdx.x >> 5), e = blockIdx.x * 32 + (threadIdx.x & 31);
     if (t < T && e < E) {
       const float v = token_logit(part, gridDim.z, bias, T, E, t, e);
       __stcg(part + (size_t)t * E + e, v);
     }
+    __syncthreads();
   }
-  __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();  // this block's logits before the level-2 ticket
-    s_last = (atomicAdd(&tickets[0], 1) == (int)(gridDim.x * gridDim.y) - 1);
+    __threadfence();  // this CTA's partials (or its block's logits) before the ticket
+    s_last = (atomicAdd(&tickets[0], 1) == (int)(one_level ? gridDim.x * gridDim.y * gridDim.z
+                                                           : gridDim.x * gridDim.y) - 1);
     if (s_last) __threadfence();
   }
   __syncthreads();
   if (!s_last) return;
   __shared__ float s_lg[8][256];
+  __shared__ int s_pick[16 * 8];
   __shared__ TableSmem<256> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t0 = 0; t0 < T; t0 += 8) {
-    // thread e loads expert e's final logit of up to 8 tokens (independent loads)
+    // thread e: expert e's logit of up to 8 tokens, every load before the stores
     if (threadIdx.x < E) {
       float v[8];
+      if (one_level) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = (t0 + u < T) ? __ldcg(part + (size_t)(t0 + u) * E + threadIdx.x) : 0.f;
+        for (int u = 0; u < 2; ++u)
+          v[u] = (t0 + u < T) ? token_logit(part, gridDim.z, bias, T, E, t0 + u, threadIdx.x) : 0.f;
+      } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) s_lg[u][threadIdx.x] = v[u];
+        for (int u = 0; u < 8; ++u) v[u] = (t0 + u < T) ? __ldcg(part + (size_t)(t0 + u) * E + threadIdx.x) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (t0 + u < T && (!one_level || u < 2)) s_lg[u][threadIdx.x] = v[u];
     }
     __syncthreads();
     if (t0 + warp < T)
-      topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)(t0 + warp) * k, topk_w + (size_t)(t0 + warp) * k, lane);
+      topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)(t0 + warp) * k, topk_w + (size_t)(t0 + warp) * k, lane,
+                     s_pick + (t0 + warp) * k);
     __syncthreads();
   }
-  build_table<256>(topk_idx, T * k, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm);
+  build_table<256>(s_pick, T * k, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm);
 }
 
 // ---------------------------------------------------------------------------

@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       ++seq;
       int good = 1;
       if (lane == 0) {
-        good = mbar_wait(&empty[d], par, a.st, 1);
+        good = seq <= D || mbar_wait(&empty[d], par, a.st, 1);  // the first D slots start free
         if (good) {
           uint8_t* slot = smem + d * Lay::kSlot;
           uint64_t* bar = &full[d];
@@ -301,10 +301,11 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       }
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    // the ring's first D slots are free: fill them before waiting
+    // two of the ring's free slots before waiting (the activation panel, issued
+    // right after the wait, gates the first MMAs; the rest of the ring follows it)
     int issued = 0;
     const int total = nloc * nch;
-    while (a.early && ok && issued < total && issued < D) {
+    while (a.early && ok && issued < total && issued < 2) {
       const int j = issued / nch;
       ok = issue(j, issued % nch, entry((it0 + j) / tiles).x);
       ++issued;

@@ -318,6 +318,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_t1", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--routed", action="store_true",
+                    help="time lmoe_forward_routed on a seeded caller-supplied routing (uniform expert ids, "
+                         "weights summing to 1) instead of lmoe_forward")
     ap.add_argument("--stage", choices=["pool", "unpool"], default=None,
                     help="time one dense projection call alone (for profiling); prints a stage line")
     args = ap.parse_args()
@@ -356,6 +359,18 @@ def main():
     ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
     x_dev = to_dev(x)
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
+    if args.routed:
+        rng = np.random.default_rng(1234)
+        r_idx = rng.integers(0, d.E, size=(d.T, d.k), dtype=np.int32)
+        r_w = rng.uniform(0.05, 1.0, size=(d.T, d.k)).astype(np.float32)
+        r_w /= r_w.sum(1, keepdims=True)
+        r_idx_dev, r_w_dev = to_dev(r_idx), to_dev(r_w.astype(np.float32))
+
+        def forward(xd, o):
+            lm.lmoe_forward_routed(dims, wts, xd, r_idx_dev, r_w_dev, o, ws)
+    else:
+        def forward(xd, o):
+            lm.lmoe_forward(dims, wts, xd, o, ws)
     x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     out_host = torch.empty(d.T, d.H, dtype=torch.bfloat16).pin_memory()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -363,7 +378,7 @@ def main():
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+            forward(x_dev, out)
         rc = lm.lmoe_status_check(ws)
         if rc != 0:
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
@@ -384,7 +399,7 @@ def main():
             for i in range(args.steps):
                 flush.zero_()
                 e0[i].record()
-                lm.lmoe_forward(dims, wts, x_dev, out, ws)
+                forward(x_dev, out)
                 e1[i].record()
             torch.cuda.synchronize()
         finally:
@@ -397,7 +412,7 @@ def main():
         # ---- end to end: host input upload and output download inside the timed region ----
         for _ in range(2):
             x_dev.copy_(x_host, non_blocking=True)
-            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+            forward(x_dev, out)
             out_host.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         barrier(world)
@@ -405,7 +420,7 @@ def main():
             flush.zero_()
             e0[i].record()
             x_dev.copy_(x_host, non_blocking=True)
-            lm.lmoe_forward(dims, wts, x_dev, out, ws)
+            forward(x_dev, out)
             out_host.copy_(out, non_blocking=True)
             e1[i].record()
         torch.cuda.synchronize()
@@ -420,7 +435,7 @@ def main():
         try:
             for i in range(max(5, min(args.steps, 20))):
                 flush.zero_()
-                lm.lmoe_forward(dims, wts, x_dev, out, ws)
+                forward(x_dev, out)
                 torch.cuda.synchronize()
                 for j in range(launches_per_step):
                     per_launch[j].append(evs[j].elapsed_time(evs[j + 1]))
@@ -463,7 +478,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random weights of the layer's shape)",
-        "config": {"workload": workload_name(d, name), "T": d.T, "touched_experts": touched,
+        "config": {"workload": workload_name(d, name) + (" (caller-supplied routing: seeded uniform ids, "
+                                                          "lmoe_forward_routed)" if args.routed else ""),
+                   "T": d.T, "touched_experts": touched,
                    "l2": "flushed between steps (512 MB device write outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_gbs / pk["hbm_gbs"],

@@ -170,6 +170,23 @@ LMOE_API int lmoe_norm_combine_unpool(const lmoe_dims* dims, const float* y, con
 LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x, uint16_t* out,
                  void* ws, size_t ws_bytes, lmoe_stream_t stream);
 
+/* The whole layer with caller-supplied routing ("Muse Spark Open on Gaudi 2",
+ * "The latent MoE: A' with a per-expert norm": the experts, the per-route
+ * post_expert_norm, the fp32 weighted sum and the unpooler all take the
+ * routing as given).  The router is not run: the routing table is built from
+ * topk_idx, the weighted sum uses topk_w as they are.  For replaying a
+ * recorded routing, or forcing an expert choice.
+ *   topk_idx in  int32 [T][k], device; expert ids in [0, E) (a token may name
+ *                an expert more than once: each route row stays separate)
+ *   topk_w   in  fp32 [T][k], device; the weights of the sum, used as given
+ *   out      out bf16 [T][H]
+ * weights->router_w and router_bias are ignored.  An id outside [0, E) is
+ * reported on the device (LMOE_EDEVICE_CHECK through lmoe_status_check) and
+ * counted as expert 0.  Workspace, streams and errors as for lmoe_forward. */
+LMOE_API int lmoe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x,
+                                 const int32_t* topk_idx, const float* topk_w, uint16_t* out, void* ws,
+                                 size_t ws_bytes, lmoe_stream_t stream);
+
 /* Synchronises `stream`, reads the device status word of `ws` and returns it
  * (LMOE_OK, LMOE_ETIMEOUT or LMOE_EDEVICE_CHECK), or LMOE_ECUDA if the
  * stream itself reports an error.  `ws` is a device pointer. */

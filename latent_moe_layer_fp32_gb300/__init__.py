@@ -19,7 +19,7 @@ from ._build import build, up_to_date
 __all__ = [
     "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
     "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_route_noalloc", "lmoe_pool", "lmoe_experts_mxfp4",
-    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_status_check", "lmoe_error_string",
+    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_status_check", "lmoe_error_string",
     "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
 ]
 
@@ -72,6 +72,7 @@ def load(path: str | None = None):
     lib.lmoe_experts_mxfp4.argtypes = [dp] + [vp] * 8 + [vp, sz, vp]
     lib.lmoe_norm_combine_unpool.argtypes = [dp] + [vp] * 6 + [vp, sz, vp]
     lib.lmoe_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
+    lib.lmoe_forward_routed.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, vp, vp, sz, vp]
     lib.lmoe_status_check.argtypes = [vp, vp]
     lib.lmoe_error_string.argtypes = [i32]
     lib.lmoe_error_string.restype = ctypes.c_char_p
@@ -195,6 +196,14 @@ def lmoe_norm_combine_unpool(dims, y, topk_idx, topk_w, norm_g, unpooler_w, out,
 def lmoe_forward(dims, weights: LmoeWeights, x, out, ws, stream=None):
     _check(load().lmoe_forward(ctypes.byref(dims), ctypes.byref(weights), _ptr(x, _BF16), _ptr(out, _BF16),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "lmoe_forward")
+
+
+def lmoe_forward_routed(dims, weights: LmoeWeights, x, topk_idx, topk_w, out, ws, stream=None):
+    """The layer with caller-supplied routing: topk_idx int32 [T][k], topk_w fp32 [T][k]."""
+    _check(load().lmoe_forward_routed(ctypes.byref(dims), ctypes.byref(weights), _ptr(x, _BF16),
+                                      _ptr(topk_idx, (torch.int32,)), _ptr(topk_w, (torch.float32,)),
+                                      _ptr(out, _BF16), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "lmoe_forward_routed")
 
 
 def lmoe_status_check(ws, stream=None) -> int:

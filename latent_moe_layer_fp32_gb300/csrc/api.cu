@@ -111,7 +111,7 @@ int set_carveouts() {
       reinterpret_cast<const void*>(route_small_kernel), reinterpret_cast<const void*>(router_partial_kernel),
       reinterpret_cast<const void*>(topk_kernel),        reinterpret_cast<const void*>(table_kernel),
       reinterpret_cast<const void*>(topk_hist_kernel),   reinterpret_cast<const void*>(table_scan_kernel),
-      reinterpret_cast<const void*>(table_scatter_kernel),
+      reinterpret_cast<const void*>(table_scatter_kernel), reinterpret_cast<const void*>(table_hist_kernel),
       reinterpret_cast<const void*>(combine_kernel),     reinterpret_cast<const void*>(ssq_kernel),
       reinterpret_cast<const void*>(groups_from_offsets_kernel),
       reinterpret_cast<const void*>(gather_rows_kernel), reinterpret_cast<const void*>(router_split_kernel)};
@@ -538,6 +538,52 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
   CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
+  return post_call(s, LMOE_OK);
+}
+
+int lmoe_forward_routed(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, const int32_t* topk_idx,
+                        const float* topk_w, uint16_t* out, void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  if (!wt || !x || !out || !topk_idx || !topk_w || !aligned16(x) || !aligned16(out) || !aligned16(topk_idx) ||
+      !aligned16(topk_w))
+    return LMOE_EINVAL;
+  const void* ptrs[] = {wt->pooler_w, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, wt->norm_g, wt->unpooler_w};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  const int T = d->T, E = d->n_experts, k = d->top_k, R = T * k, nchunks = (T + kChunkTok - 1) / kChunkTok;
+  int32_t* srows = at<int32_t>(ws, w.pub.sorted_rows);
+  uint16_t* x_lat = at<uint16_t>(ws, w.pub.x_lat);
+  float* y = at<float>(ws, w.pub.y);
+  Status* st = at<Status>(ws, w.pub.status);
+  int32_t* rank = at<int32_t>(ws, w.rank);
+  int32_t* chunk = at<int32_t>(ws, w.chunk);
+  // the table from the given ids (the router is not run), next to the pooler for many tokens
+  const bool fork = T > 16;
+  SideStream* ss = nullptr;
+  cudaStream_t st_table = s;
+  if (fork) {
+    CHECK(side_stream(&ss));
+    if (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+      return LMOE_ECUDA;
+    st_table = ss->s;
+  }
+  LAUNCH(dim3(nchunks), dim3(256), st_table, table_hist_kernel, topk_idx, T, E, k, rank, chunk, st);
+  LAUNCH(dim3(1), dim3(256), st_table, table_scan_kernel, chunk, nchunks, E, R, group_rows(T),
+         at<int32_t>(ws, w.pub.expert_offsets), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups));
+  LAUNCH(dim3((R + 255) / 256), dim3(256), st_table, table_scatter_kernel, topk_idx, (const int32_t*)rank,
+         (const int32_t*)chunk, R, E, k, srows, at<int32_t>(ws, w.pub.row_pos));
+  if (fork) {
+    if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return LMOE_ECUDA;
+    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
+    if (cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) return LMOE_ECUDA;
+  } else {
+    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
+  }
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
+  CHECK(run_combine_unpool(d, w, di, y, topk_idx, topk_w, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return post_call(s, LMOE_OK);
 }
 

@@ -19,6 +19,8 @@ __global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3)
 constexpr int kChunkTok = 32;  // tokens per chunk of the many-token routing table
 __global__ void topk_hist_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,
                                  int32_t* topk_idx, float* topk_w, int32_t* rank, int32_t* chunk_cnt);
+__global__ void table_hist_kernel(const int32_t* topk_idx, int T, int E, int k, int32_t* rank, int32_t* chunk_cnt,
+                                  Status* st);
 __global__ void table_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int R, int G, int32_t* offsets,
                                   int4* groups, int32_t* n_groups);
 __global__ void table_scatter_kernel(const int32_t* topk_idx, const int32_t* rank, const int32_t* chunk_base, int R,

@@ -447,6 +447,36 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
 // Row ids r = t*k + j keep their order inside an expert (the table is the same
 // stable counting sort as build_table).
 // ---------------------------------------------------------------------------
+// Stable rank of each of a chunk's rows among the chunk's rows of its expert
+// (row order), and the chunk's per-expert counts.  Threads 0..255 (warps 0-7)
+// take local rows 0..255; picks[i] is local row i's expert, rows from
+// `row0`; s_wcnt is zeroed shared scratch.  Every thread of the block calls it.
+__device__ __forceinline__ void chunk_ranks(const int* picks, int nrow, int E, int row0, int chunk,
+                                            int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt,
+                                            int (&s_wcnt)[8][256]) {
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  int e = 0, rk = 0;
+  if (warp < 8) {
+    e = i < nrow ? picks[i] : -1 - lane;  // rows past the end match nothing
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    rk = __popc(same & ((1u << lane) - 1u));
+    if (i < nrow && rk == 0) s_wcnt[warp][e] = __popc(same);
+  }
+  __syncthreads();
+  if (i < E) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = s_wcnt[w][i];
+      s_wcnt[w][i] = acc;
+      acc += c;
+    }
+    chunk_cnt[(size_t)chunk * E + i] = acc;
+  }
+  __syncthreads();
+  if (warp < 8 && i < nrow) rank[(size_t)row0 + i] = s_wcnt[warp][e] + rk;
+}
+
 __global__ void __launch_bounds__(1024) topk_hist_kernel(const float* __restrict__ part, int nsplit,
                                                          const float* __restrict__ bias, int T, int E, int k,
                                                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
@@ -476,30 +506,33 @@ __global__ void __launch_bounds__(1024) topk_hist_kernel(const float* __restrict
     topk_one_token(s_lg[warp], E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, lane, s_pick + warp * k);
   }
   __syncthreads();
-  // stable rank of each of the chunk's rows among its expert's rows (row order);
-  // threads 0..255 (warps 0-7) take local rows 0..255 (k * 32 <= 256)
-  const int nrow = ntok * k;
-  const int i = threadIdx.x;
-  int e = 0, rk = 0;
-  if (warp < 8) {
-    e = i < nrow ? s_pick[i] : -1 - lane;  // rows past the end match nothing
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    rk = __popc(same & ((1u << lane) - 1u));
-    if (i < nrow && rk == 0) s_wcnt[warp][e] = __popc(same);
-  }
-  __syncthreads();
-  if (threadIdx.x < E) {
-    int acc = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const int c = s_wcnt[w][threadIdx.x];
-      s_wcnt[w][threadIdx.x] = acc;
-      acc += c;
+  chunk_ranks(s_pick, ntok * k, E, t0 * k, blockIdx.x, rank, chunk_cnt, s_wcnt);
+}
+
+// Routing table from caller-supplied expert ids, first pass: chunks of 32
+// tokens as in topk_hist_kernel.  Ids outside [0, E) are reported on the
+// device (LMOE_EDEVICE_CHECK) and counted as expert 0 so every index stays in
+// range.
+__global__ void __launch_bounds__(256) table_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                                                         int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt,
+                                                         Status* st) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_pick[kChunkTok * 8];
+  __shared__ int s_wcnt[8][256];
+  const int t0 = blockIdx.x * kChunkTok;
+  const int nrow = min(kChunkTok, T - t0) * k;
+  for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+  if ((int)threadIdx.x < nrow) {
+    int e = topk_idx[(size_t)t0 * k + threadIdx.x];
+    if (e < 0 || e >= E) {
+      set_error(st, LMOE_EDEVICE_CHECK, 104);
+      e = 0;
     }
-    chunk_cnt[(size_t)blockIdx.x * E + threadIdx.x] = acc;
+    s_pick[threadIdx.x] = e;
   }
   __syncthreads();
-  if (warp < 8 && i < nrow) rank[(size_t)t0 * k + i] = s_wcnt[warp][e] + rk;
+  chunk_ranks(s_pick, nrow, E, t0 * k, blockIdx.x, rank, chunk_cnt, s_wcnt);
 }
 
 __global__ void __launch_bounds__(256) table_scan_kernel(int32_t* __restrict__ chunk_cnt, int nchunks, int E, int R,
@@ -574,7 +607,9 @@ __global__ void __launch_bounds__(256) table_scatter_kernel(const int32_t* __res
   pdl_trigger();
   const int r = blockIdx.x * 256 + threadIdx.x;
   if (r >= R) return;
-  const int e = topk_idx[r], c = (r / k) / kChunkTok;
+  int e = topk_idx[r];
+  if (e < 0 || e >= E) e = 0;  // as the first pass counted it (caller-supplied ids are checked there)
+  const int c = (r / k) / kChunkTok;
   const int pos = chunk_base[(size_t)c * E + e] + rank[r];
   sorted_rows[pos] = r;
   row_pos[r] = pos;

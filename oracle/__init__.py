@@ -144,6 +144,14 @@ class Oracle:
         self.lib.oracle_unpool(ctypes.byref(od), _p(z), _p(unpooler_w), _p(out))
         return out
 
+    def forward_routed(self, d, x, w, topk_idx, topk_w):
+        """Whole layer with the given routing: the pooler, expert, norm-and-sum and
+        unpooler stages composed as in forward(), the router and top-k skipped."""
+        x_lat = self.pool(d, x, w["pooler_w"])
+        y = self.experts(d, x_lat, topk_idx, w)
+        z = self.norm_combine(d, y, topk_idx, topk_w, w["norm_g"])
+        return {"out": self.unpool(d, z, w["unpooler_w"]), "x_lat": x_lat, "y": y, "z": z}
+
     def forward(self, d, x, w):
         """Whole layer; returns a dict of the output and every intermediate."""
         T = x.shape[0]

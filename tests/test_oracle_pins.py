@@ -49,6 +49,33 @@ def test_forward_is_stage_composition(o, case):
     assert np.array_equal(r["out"], case.out)
 
 
+def test_forward_routed_with_its_own_routing_is_forward(o, case):
+    d = case.d
+    r = o.forward_routed(d, case.x, case.w, case.idx, case.tw)
+    for key in ("x_lat", "y", "z", "out"):
+        assert np.array_equal(r[key], getattr(case, key)), key
+
+
+def test_forward_routed_duplicate_route_sums_its_weights(o, case):
+    # a token naming one expert twice with weights a, b gives the sum of a route
+    # with weight a + b plus a route of weight 0 (0.25 + 0.25 = 0.5 and 0 * y are exact)
+    d = case.d
+    idx = case.idx.copy()
+    w = np.full(idx.shape, 1.0 / d.k, np.float32)
+    w[:, :2] = 0.25 if d.k == 4 else w[:, :2]
+    w[:, 2:] = (1.0 - w[:, :2].sum(1, keepdims=True)) / (d.k - 2)
+    dup = idx.copy()
+    dup[:, 1] = dup[:, 0]
+    single = idx.copy()
+    ws = w.copy()
+    ws[:, 0] = w[:, 0] + w[:, 1]
+    ws[:, 1] = 0.0
+    a = o.forward_routed(d, case.x, case.w, dup, w)
+    b = o.forward_routed(d, case.x, case.w, single, ws)
+    assert np.array_equal(a["z"], b["z"])
+    assert np.array_equal(a["out"], b["out"])
+
+
 def test_thread_count_invariance(case):
     d = case.d
     a = oracle.Oracle(0, threads=1).forward(d, case.x, case.w)

@@ -321,6 +321,10 @@ def main():
     ap.add_argument("--routed", action="store_true",
                     help="time lmoe_forward_routed on a seeded caller-supplied routing (uniform expert ids, "
                          "weights summing to 1) instead of lmoe_forward")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="a step runs this many layers back to back, each layer's output the next one's input "
+                         "and each layer with its own device copy of the weights")
+    ap.add_argument("--graph", action="store_true", help="capture one step in a CUDA graph and replay it")
     ap.add_argument("--stage", choices=["pool", "unpool"], default=None,
                     help="time one dense projection call alone (for profiling); prints a stage line")
     args = ap.parse_args()
@@ -354,7 +358,11 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     w = {k: to_dev(v) for k, v in hw.items()}
-    wts = lm.weights_of(w)
+    n_layers = max(1, args.layers)
+    # each layer gets its own copy of the weights, so no layer finds another's in L2
+    w_layers = [w] + [{k: (None if v is None else v.clone()) for k, v in w.items()} for _ in range(n_layers - 1)]
+    wts_layers = [lm.weights_of(wl) for wl in w_layers]
+    wts = wts_layers[0]
     dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
     ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
     x_dev = to_dev(x)
@@ -366,11 +374,37 @@ def main():
         r_w /= r_w.sum(1, keepdims=True)
         r_idx_dev, r_w_dev = to_dev(r_idx), to_dev(r_w.astype(np.float32))
 
-        def forward(xd, o):
-            lm.lmoe_forward_routed(dims, wts, xd, r_idx_dev, r_w_dev, o, ws)
+        def forward(xd, o, layer=0):
+            lm.lmoe_forward_routed(dims, wts_layers[layer], xd, r_idx_dev, r_w_dev, o, ws)
     else:
-        def forward(xd, o):
-            lm.lmoe_forward(dims, wts, xd, o, ws)
+        def forward(xd, o, layer=0):
+            lm.lmoe_forward(dims, wts_layers[layer], xd, o, ws)
+    mid = torch.empty_like(out)
+
+    def layers(xd, o):
+        # layer i reads the previous layer's output; the last one writes o
+        cur = xd
+        for i in range(n_layers):
+            dst = o if (n_layers - 1 - i) % 2 == 0 else mid
+            forward(cur, dst, i)
+            cur = dst
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            layers(x_dev, out)  # first-use setup happens outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layers(x_dev, out)
+
+    def step(xd, o):
+        if graph is not None:
+            graph.replay()  # captured on x_dev and out
+        else:
+            layers(xd, o)
     x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     out_host = torch.empty(d.T, d.H, dtype=torch.bfloat16).pin_memory()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -378,7 +412,7 @@ def main():
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            forward(x_dev, out)
+            step(x_dev, out)
         rc = lm.lmoe_status_check(ws)
         if rc != 0:
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
@@ -399,7 +433,7 @@ def main():
             for i in range(args.steps):
                 flush.zero_()
                 e0[i].record()
-                forward(x_dev, out)
+                step(x_dev, out)
                 e1[i].record()
             torch.cuda.synchronize()
         finally:
@@ -412,7 +446,7 @@ def main():
         # ---- end to end: host input upload and output download inside the timed region ----
         for _ in range(2):
             x_dev.copy_(x_host, non_blocking=True)
-            forward(x_dev, out)
+            step(x_dev, out)
             out_host.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         barrier(world)
@@ -420,7 +454,7 @@ def main():
             flush.zero_()
             e0[i].record()
             x_dev.copy_(x_host, non_blocking=True)
-            forward(x_dev, out)
+            step(x_dev, out)
             out_host.copy_(out, non_blocking=True)
             e1[i].record()
         torch.cuda.synchronize()
@@ -446,10 +480,13 @@ def main():
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
 
     pk = peaks()
-    tokens = d.T * args.steps * world
+    # a step of n_layers layers moves each of its T tokens through n_layers layers:
+    # the metric counts token-layers, so one- and many-layer steps compare directly
+    tokens = d.T * n_layers * args.steps * world
     value = tokens / total_s
     layer_bytes = touched * EXPERT_BYTES + PROJ_BYTES
-    layer_gbs = layer_bytes * args.steps / total_s / 1e9
+    # every layer of a step streams about the same bytes (its own touched experts)
+    layer_gbs = layer_bytes * n_layers * args.steps / total_s / 1e9
 
     # dominant kernel: the modelled launch with the largest mean device time
     kern_ms = {names[j]: statistics.mean(v) for j, v in enumerate(per_launch)}
@@ -479,17 +516,19 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random weights of the layer's shape)",
         "config": {"workload": workload_name(d, name) + (" (caller-supplied routing: seeded uniform ids, "
-                                                          "lmoe_forward_routed)" if args.routed else ""),
-                   "T": d.T, "touched_experts": touched,
+                                                          "lmoe_forward_routed)" if args.routed else "") +
+                   (f", {n_layers} layers per step" if n_layers > 1 else "") + (", CUDA graph" if args.graph else ""),
+                   "T": d.T, "touched_experts": touched, "layers_per_step": n_layers,
                    "l2": "flushed between steps (512 MB device write outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ms_per_layer": 1e3 * total_s / args.steps / n_layers,
         "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_gbs / pk["hbm_gbs"],
         "layer_bytes_per_step": layer_bytes,
         "roofline": roof,
         "kernels_ms": kern_ms,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
                 "d2h_bytes_per_step": d.T * d.H * 2},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * n_layers * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

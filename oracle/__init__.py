@@ -66,8 +66,14 @@ class Oracle:
         L.oracle_norm_combine.argtypes = [dp, vp, vp, vp, vp, vp, vp]
         L.oracle_unpool.argtypes = [dp, vp, vp, vp]
         L.oracle_forward.argtypes = [dp] + [vp] * 16
+        L.oracle_router_logits_f32.argtypes = [dp, vp, vp, vp, vp, vp]
+        i64 = ctypes.c_int64
+        L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, vp, ctypes.c_float, vp]
+        L.oracle_bf16_round.argtypes = [i64, vp, vp]
+        L.oracle_residual_add.argtypes = [i64, vp, vp, vp]
         for f in ("oracle_router_logits", "oracle_topk", "oracle_table", "oracle_pool", "oracle_experts",
-                  "oracle_norm_combine", "oracle_unpool", "oracle_forward", "oracle_set_threads"):
+                  "oracle_norm_combine", "oracle_unpool", "oracle_forward", "oracle_set_threads",
+                  "oracle_router_logits_f32", "oracle_rmsnorm_rows", "oracle_bf16_round", "oracle_residual_add"):
             getattr(L, f).restype = None
         self.set_threads(threads if threads else max(1, min(64, os.cpu_count() or 1)))
 
@@ -143,6 +149,52 @@ class Oracle:
         out = np.empty((od.T, d.H), np.uint16)
         self.lib.oracle_unpool(ctypes.byref(od), _p(z), _p(unpooler_w), _p(out))
         return out
+
+    # -- the sandwich block around the layer ----------------------------------------------
+    def rmsnorm(self, x, g, eps):
+        """Row RMSNorm of bf16 rows x [rows][W] with the bf16 gain g [W] -> fp32."""
+        x = np.ascontiguousarray(x)
+        out = np.empty(x.shape, np.float32)
+        self.lib.oracle_rmsnorm_rows(x.shape[0], x.shape[1], _p(x), _p(np.ascontiguousarray(g)), float(eps), _p(out))
+        return out
+
+    def router_logits_f32(self, d, x, router_w, router_bias=None, want_absdot=False):
+        """Router logits of fp32 input rows x [T][H] (the pre-norm's output)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        od = self.dims(d, x.shape[0])
+        logits = np.empty((od.T, d.E), np.float32)
+        absdot = np.empty((od.T, d.E), np.float64) if want_absdot else None
+        self.lib.oracle_router_logits_f32(ctypes.byref(od), _p(x), _p(router_w), _p(router_bias), _p(logits),
+                                          _p(absdot))
+        return (logits, absdot) if want_absdot else logits
+
+    def bf16_round(self, a):
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        out = np.empty(a.shape, np.uint16)
+        self.lib.oracle_bf16_round(a.size, _p(a), _p(out))
+        return out
+
+    def residual_add(self, x, p):
+        x = np.ascontiguousarray(x)
+        p = np.ascontiguousarray(p, dtype=np.float32)
+        out = np.empty(x.shape, np.uint16)
+        self.lib.oracle_residual_add(x.size, _p(x), _p(p), _p(out))
+        return out
+
+    def block_forward(self, d, x, w, nw, eps=None):
+        """y = x + post_norm(F(pre_norm(x))) with F the layer; the router reads the
+        pre-norm's fp32 output, the pooler that output rounded to bf16.  nw holds
+        the bf16 gains "pre_g" and "post_g" [H]; eps defaults to the layer's."""
+        eps = d.eps if eps is None else eps
+        n = self.rmsnorm(x, nw["pre_g"], eps)
+        logits, absdot = self.router_logits_f32(d, n, w["router_w"], w.get("router_bias"), want_absdot=True)
+        idx, tw = self.topk(d, logits)
+        nb = self.bf16_round(n)
+        r = self.forward_routed(d, nb, w, idx, tw)
+        p = self.rmsnorm(r["out"], nw["post_g"], eps)
+        r.update({"y": self.residual_add(x, p), "n": n, "nb": nb, "logits": logits, "absdot": absdot,
+                  "topk_idx": idx, "topk_w": tw})
+        return r
 
     def forward_routed(self, d, x, w, topk_idx, topk_w):
         """Whole layer with the given routing: the pooler, expert, norm-and-sum and

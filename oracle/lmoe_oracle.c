@@ -48,6 +48,19 @@
  *   3 W2 read transposed            4 block scale off by one
  *   5 weights not renormalised      6 ties go to the higher index
  *   7 norm applied to the sum       8 norm gain dropped
+ *   9 row RMSNorm drops its gain    10 block drops the residual
+ *
+ * The transformer block around the layer ("Soporte de dia 0 para Muse Spark
+ * Open en vLLM", section "Normalizacion en sandwich": one norm before the
+ * block and one after it, y = x + post_norm(F(norm(x)))), with the router fed
+ * by the fp32 output of the pre-norm (same page, section "Nvidia"):
+ *  - each norm is an RMSNorm over the hidden width, eps inside the square
+ *    root, a bf16 gain per column, multiply order (x * rinv) * g, as for
+ *    post_expert_norm;
+ *  - the router reads the pre-norm's fp32 output; the pooler reads it
+ *    rounded to bf16 (the layer's activations are bf16);
+ *  - the residual sum x + post_norm(out) is formed in fp32 and rounded once
+ *    to bf16.
  */
 #ifndef LMOE_ORACLE_PLANT
 #define LMOE_ORACLE_PLANT 0
@@ -197,6 +210,39 @@ void oracle_router_logits(const or_dims* d, const uint16_t* x, const float* rout
                           const float* router_bias, float* logits, double* absdot) {
   router_ctx c = {d, x, router_w, router_bias, logits, absdot};
   parallel_for((int64_t)d->T * d->E, router_body, &c);
+}
+
+/* The same logits for an fp32 input row (the sandwich block's pre-norm
+ * output): every product of two fp32 values is exact in fp64, so the fp64 sum
+ * rounded once is again the correctly rounded fp32 logit. */
+typedef struct {
+  const or_dims* d;
+  const float* x;
+  const float* wr;
+  const float* bias;
+  float* logits;
+  double* absdot;
+} router_f32_ctx;
+
+static void router_f32_body(void* p, int64_t i) {
+  router_f32_ctx* c = (router_f32_ctx*)p;
+  int64_t t = i / c->d->E, e = i % c->d->E, H = c->d->H;
+  double acc = 0.0, mag = 0.0;
+  for (int64_t h = 0; h < H; ++h) {
+    double prod = (double)c->x[t * H + h] * (double)c->wr[e * H + h];
+    acc += prod;
+    mag += fabs(prod);
+  }
+  float lg = (float)acc;
+  if (c->bias) lg = lg + c->bias[e];
+  c->logits[t * c->d->E + e] = lg;
+  if (c->absdot) c->absdot[t * c->d->E + e] = mag;
+}
+
+void oracle_router_logits_f32(const or_dims* d, const float* x, const float* router_w, const float* router_bias,
+                              float* logits, double* absdot) {
+  router_f32_ctx c = {d, x, router_w, router_bias, logits, absdot};
+  parallel_for((int64_t)d->T * d->E, router_f32_body, &c);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -462,4 +508,42 @@ void oracle_forward(const or_dims* d, const uint16_t* x, const float* router_w,
   if (!x_lat_out) free(x_lat);
   if (!y_out) free(y);
   if (!z_out) free(z);
+}
+
+/* ------------------------------------------------------------------------ */
+/* sandwich block around the layer                                          */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm of each of `rows` bf16 rows of width W: ss = sum x^2 (fp32,
+ * sequential), rinv = 1/sqrt(ss/W + eps), out = (x * rinv) * g in fp32. */
+void oracle_rmsnorm_rows(int64_t rows, int64_t W, const uint16_t* x, const uint16_t* g, float eps, float* out) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * W;
+    float ss = 0.0f;
+    for (int64_t c = 0; c < W; ++c) ss += bf16_val(xr[c]) * bf16_val(xr[c]);
+    float rinv = 1.0f / sqrtf(ss / (float)W + eps);
+    for (int64_t c = 0; c < W; ++c) {
+#if LMOE_ORACLE_PLANT == 9
+      out[r * W + c] = bf16_val(xr[c]) * rinv;
+#else
+      out[r * W + c] = (bf16_val(xr[c]) * rinv) * bf16_val(g[c]);
+#endif
+    }
+  }
+}
+
+/* bf16 round-to-nearest-even of n fp32 values. */
+void oracle_bf16_round(int64_t n, const float* a, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(a[i]);
+}
+
+/* out = bf16(x + p): the residual sum in fp32, rounded once. */
+void oracle_residual_add(int64_t n, const uint16_t* x, const float* p, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+#if LMOE_ORACLE_PLANT == 10
+    out[i] = oracle_bf16_rne(p[i]);
+#else
+    out[i] = oracle_bf16_rne(bf16_val(x[i]) + p[i]);
+#endif
+  }
 }

@@ -21,6 +21,16 @@ What pins what:
     the per-route norm, an fp32 re-summation in route order, the
     "norm of a partial sum is wrong" control and "non-local rows are exact
     zeros" ("Muse Spark Open on Gaudi 2", "EP and TP layout")
+
+The sandwich block around the layer ("Soporte de dia 0 ...", "Normalizacion
+en sandwich") is pinned by BLOCK_PINS:
+  * row RMSNorm         -> with eps = 0: bitwise invariance under a power-of-two
+    scale of the row, and RMS(out / g) = 1 for every row
+  * fp32-input router   -> bitwise equal to the pinned bf16-input router on
+    bf16-representable input; fp64 numpy logits on arbitrary fp32 input
+  * block               -> a zero post-norm gain or a zero unpooler gives y = x
+    exactly; with eps = 0 the layer output does not change when x is scaled by
+    a power of two (the norm comes first); token independence
 """
 from __future__ import annotations
 
@@ -326,3 +336,84 @@ def pin_identical_experts(o, c):
 PINS = [pin_e2m1_golden, pin_mxfp4_closed_form, pin_bf16_rne, pin_router_fp64, pin_topk_bruteforce,
         pin_table, pin_pool_textbook, pin_experts_dense, pin_norm_per_route, pin_sharded_invariants,
         pin_unpool_textbook, pin_w2_scale_invariance, pin_identical_experts]
+
+
+# --------------------------------------------------------------------------------------
+# the sandwich block
+# --------------------------------------------------------------------------------------
+
+class BlockCase:
+    def __init__(self, o, d, x, w, nw):
+        self.d, self.x, self.w, self.nw = d, x, w, nw
+        self.r = o.block_forward(d, x, w, nw)
+
+
+def make_block_case(o, T=12, seed=0):
+    d = synth.with_tokens(synth.CONFIGS["tiny"], T)
+    return BlockCase(o, d, synth.make_x(d, seed), synth.make_weights(d, seed), synth.make_block_norms(d, seed))
+
+
+def pin_rmsnorm_invariants(o, c):
+    x, g = c.x, c.nw["pre_g"]
+    a = o.rmsnorm(x, g, 0.0)
+    # a power-of-two scale of a row is exact in bf16 and cancels exactly in the norm
+    for k in (-3, 5):
+        xs = f32_to_bf16_torch(np.ldexp(bf16_to_f64(x), k).astype(np.float32))
+        assert np.array_equal(bf16_to_f64(xs), np.ldexp(bf16_to_f64(x), k))
+        assert np.array_equal(o.rmsnorm(xs, g, 0.0), a), k
+    # RMS over the row of out / g is one (mean over the W columns, the gain applied per column)
+    ratio = a.astype(np.float64) / bf16_to_f64(g)[None, :]
+    rms = np.sqrt((ratio * ratio).mean(1))
+    assert np.all(np.abs(rms - 1.0) <= (x.shape[1] + 16) * EPS32), np.abs(rms - 1.0).max()
+    # eps enters inside the square root
+    e = 0.25
+    b = o.rmsnorm(x, g, e).astype(np.float64) / bf16_to_f64(g)[None, :]
+    x64 = bf16_to_f64(x)
+    want = x64 / np.sqrt((x64 * x64).mean(1, keepdims=True) + e)
+    assert np.allclose(b, want, rtol=(x.shape[1] + 16) * EPS32, atol=0), np.abs(b - want).max()
+
+
+def pin_router_f32_input(o, c):
+    d, w = c.d, c.w
+    # bf16-representable fp32 input: the fp32-input router equals the bf16-input one
+    xf = synth.bf16_to_f32(c.x)
+    la, aa = o.router_logits(d, c.x, w["router_w"], w["router_bias"], want_absdot=True)
+    lb, ab = o.router_logits_f32(d, xf, w["router_w"], w["router_bias"], want_absdot=True)
+    assert np.array_equal(la, lb) and np.array_equal(aa, ab)
+    # arbitrary fp32 input (the block's pre-norm output): fp64 numpy logits
+    n = c.r["n"]
+    ref = (n.astype(np.float64) @ w["router_w"].astype(np.float64).T).astype(np.float32)
+    if w["router_bias"] is not None:
+        ref = ref + w["router_bias"]
+    assert np.array_equal(ref, c.r["logits"]), np.abs(ref - c.r["logits"]).max()
+
+
+def pin_block_identity_paths(o, c):
+    d = c.d
+    zero_post = dict(c.nw, post_g=np.zeros_like(c.nw["post_g"]))
+    r = o.block_forward(d, c.x, c.w, zero_post)
+    assert np.array_equal(r["y"], c.x), "post-norm gain 0 must leave the residual stream unchanged"
+    w0 = dict(c.w, unpooler_w=np.zeros_like(c.w["unpooler_w"]))
+    r = o.block_forward(d, c.x, w0, c.nw)
+    assert np.all(r["out"] == 0) and np.array_equal(r["y"], c.x), "a zero layer output must give y = x"
+    # the residual is added to the block input, not to the normalised input
+    assert not np.array_equal(c.r["y"], o.residual_add(c.r["nb"], np.zeros(c.x.shape, np.float32)))
+
+
+def pin_block_norm_first(o, c):
+    d = c.d
+    a = o.block_forward(d, c.x, c.w, c.nw, eps=0.0)
+    xs = f32_to_bf16_torch(np.ldexp(bf16_to_f64(c.x), 4).astype(np.float32))
+    b = o.block_forward(d, xs, c.w, c.nw, eps=0.0)
+    assert np.array_equal(a["n"], b["n"]) and np.array_equal(a["out"], b["out"])
+    assert not np.array_equal(a["y"], b["y"])
+
+
+def pin_block_token_independence(o, c):
+    d3 = synth.with_tokens(c.d, 3)
+    r = o.block_forward(d3, c.x[:3].copy(), c.w, c.nw)
+    assert np.array_equal(r["y"], c.r["y"][:3])
+
+
+BLOCK_PINS = [pin_rmsnorm_invariants, pin_router_f32_input, pin_block_identity_paths, pin_block_norm_first,
+              pin_block_token_independence]

@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from oracle_pins import PINS, make_case
+from oracle_pins import BLOCK_PINS, PINS, make_block_case, make_case
 
 
 @pytest.fixture(scope="module")
@@ -104,8 +104,19 @@ def test_top1_reduces_to_one_dense_expert(o, case):
     assert np.array_equal(z, yhat)
 
 
+@pytest.fixture(scope="module")
+def block_case(o):
+    return make_block_case(o)
+
+
+@pytest.mark.parametrize("pin", BLOCK_PINS, ids=[p.__name__ for p in BLOCK_PINS])
+def test_block_pin(pin, o, block_case):
+    pin(o, block_case)
+
+
 PLANTS = {1: "nibble order", 2: "gate/up swapped", 3: "W2 transposed", 4: "scale off by one",
-          5: "no renormalisation", 6: "ties to higher index", 7: "norm on the sum", 8: "gain dropped"}
+          5: "no renormalisation", 6: "ties to higher index", 7: "norm on the sum", 8: "gain dropped",
+          9: "row RMSNorm gain dropped", 10: "block residual dropped"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=[PLANTS[k] for k in sorted(PLANTS)])
@@ -119,6 +130,12 @@ def test_planted_mistake_is_caught(plant):
     for pin in PINS:
         try:
             pin(bad, c)
+        except AssertionError:
+            failed.append(pin.__name__)
+    bc = make_block_case(bad)
+    for pin in BLOCK_PINS:
+        try:
+            pin(bad, bc)
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake '{PLANTS[plant]}' passed every pin"

@@ -202,13 +202,16 @@ def allreduce_max(world, v: float) -> float:
     return float(t.item())
 
 
-def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000):
-    """Tokens/s of the CPU oracle on repeated whole-layer evaluations of `x`."""
+def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000, block_norms=None):
+    """Tokens/s of the CPU oracle on repeated whole-layer (or whole-block) evaluations of `x`."""
     import oracle
     o = oracle.get()
     reps, t0 = 0, time.perf_counter()
     while reps < max_reps:
-        o.forward(d, x, hw)
+        if block_norms is not None:
+            o.block_forward(d, x, hw, block_norms)
+        else:
+            o.forward(d, x, hw)
         reps += 1
         if time.perf_counter() - t0 >= min_seconds:
             break
@@ -325,6 +328,9 @@ def main():
                     help="a step runs this many layers back to back, each layer's output the next one's input "
                          "and each layer with its own device copy of the weights")
     ap.add_argument("--graph", action="store_true", help="capture one step in a CUDA graph and replay it")
+    ap.add_argument("--block", action="store_true",
+                    help="time the sandwich block around the layer (lmoe_block_forward: pre-norm, layer, "
+                         "post-norm and residual) instead of the layer alone")
     ap.add_argument("--stage", choices=["pool", "unpool"], default=None,
                     help="time one dense projection call alone (for profiling); prints a stage line")
     args = ap.parse_args()
@@ -364,10 +370,20 @@ def main():
     wts_layers = [lm.weights_of(wl) for wl in w_layers]
     wts = wts_layers[0]
     dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
-    ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    ws_bytes = lm.lmoe_block_workspace_bytes(dims) if args.block else lm.lmoe_workspace_bytes(dims)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     x_dev = to_dev(x)
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
-    if args.routed:
+    block_norms = synth.make_block_norms(d) if args.block else None
+    if args.block and args.routed:
+        raise SystemExit("--block runs the block's own router; it does not combine with --routed")
+    if args.block:
+        nw_dev = {k: to_dev(v) for k, v in block_norms.items()}
+        norms = lm.norms_of(nw_dev, d.eps)
+
+        def forward(xd, o, layer=0):
+            lm.lmoe_block_forward(dims, wts_layers[layer], norms, xd, o, ws)
+    elif args.routed:
         rng = np.random.default_rng(1234)
         r_idx = rng.integers(0, d.E, size=(d.T, d.k), dtype=np.int32)
         r_w = rng.uniform(0.05, 1.0, size=(d.T, d.k)).astype(np.float32)
@@ -517,6 +533,8 @@ def main():
         "data": "synthetic (seeded counter-based generator; random weights of the layer's shape)",
         "config": {"workload": workload_name(d, name) + (" (caller-supplied routing: seeded uniform ids, "
                                                           "lmoe_forward_routed)" if args.routed else "") +
+                   (" inside the sandwich block (pre-norm, fp32 router input, post-norm, residual; "
+                    "lmoe_block_forward)" if args.block else "") +
                    (f", {n_layers} layers per step" if n_layers > 1 else "") + (", CUDA graph" if args.graph else ""),
                    "T": d.T, "touched_experts": touched, "layers_per_step": n_layers,
                    "l2": "flushed between steps (512 MB device write outside the timed events)",
@@ -532,9 +550,9 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, reps, dt = cpu_oracle_rate(d, hw, x)
+        rate, cores, reps, dt = cpu_oracle_rate(d, hw, x, block_norms=block_norms)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{reps} whole-layer evaluations of the T={d.T} workload ({dt:.1f} s)"}
+                                "sample": f"{reps} whole-{'block' if args.block else 'layer'} evaluations of the T={d.T} workload ({dt:.1f} s)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

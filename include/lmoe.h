@@ -187,6 +187,36 @@ LMOE_API int lmoe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weig
                                  const int32_t* topk_idx, const float* topk_w, uint16_t* out, void* ws,
                                  size_t ws_bytes, lmoe_stream_t stream);
 
+/* The transformer block around the layer, with sandwich normalisation
+ * ("Soporte de dia 0 para Muse Spark Open en vLLM", section "Normalizacion en
+ * sandwich": y = x + post_norm(F(pre_norm(x)))), and the router fed by the
+ * pre-norm's fp32 output (same page, section "Nvidia").
+ *   pre_norm, post_norm: RMSNorm over H, n = (x * rinv) * g with
+ *     rinv = 1/sqrt(sum(x^2)/H + eps) and a bf16 gain g per column
+ *   F: the layer of lmoe_forward; its router takes the pre-norm output in
+ *     fp32, its pooler that output rounded to bf16
+ *   y = bf16(x + post_norm(F(...))), the residual sum in fp32
+ * Each norm gain is a bf16 [H] device array; eps applies to both norms. */
+typedef struct {
+  const uint16_t* pre_g;  /* bf16 [H], gain of the norm before the layer */
+  const uint16_t* post_g; /* bf16 [H], gain of the norm after the layer */
+  float eps;              /* both norms' epsilon (inside the square root), >= 0 */
+} lmoe_block_norms;
+
+/* Workspace size in bytes for lmoe_block_forward (0 if dims are invalid):
+ * lmoe_workspace_bytes plus the pre-norm output, its per-token scale, the
+ * router's split input and the layer's output.  Same alignment rule. */
+LMOE_API size_t lmoe_block_workspace_bytes(const lmoe_dims* dims);
+
+/* The block above.
+ *   x   bf16 [T][H], the residual stream;  y out bf16 [T][H] (may be x itself,
+ *       for an in-place update)
+ * The layer's intermediates stay in the workspace at the offsets of
+ * lmoe_workspace_layout.  Streams and errors as for lmoe_forward; the
+ * workspace must hold lmoe_block_workspace_bytes (LMOE_EWORKSPACE if not). */
+LMOE_API int lmoe_block_forward(const lmoe_dims* dims, const lmoe_weights* weights, const lmoe_block_norms* norms,
+                                const uint16_t* x, uint16_t* y, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
 /* Synchronises `stream`, reads the device status word of `ws` and returns it
  * (LMOE_OK, LMOE_ETIMEOUT or LMOE_EDEVICE_CHECK), or LMOE_ECUDA if the
  * stream itself reports an error.  `ws` is a device pointer. */

@@ -19,7 +19,8 @@ from ._build import build, up_to_date
 __all__ = [
     "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
     "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_route_noalloc", "lmoe_pool", "lmoe_experts_mxfp4",
-    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_status_check", "lmoe_error_string",
+    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_block_workspace_bytes",
+    "lmoe_block_forward", "norms_of", "lmoe_status_check", "lmoe_error_string",
     "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
 ]
 
@@ -37,6 +38,10 @@ class LmoeDims(ctypes.Structure):
 class LmoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("router_w", "router_bias", "pooler_w", "w13_q", "w13_s", "w2_q",
                                                "w2_s", "norm_g", "unpooler_w")]
+
+
+class LmoeBlockNorms(ctypes.Structure):
+    _fields_ = [("pre_g", ctypes.c_void_p), ("post_g", ctypes.c_void_p), ("eps", ctypes.c_float)]
 
 
 class LmoeWsLayout(ctypes.Structure):
@@ -73,6 +78,10 @@ def load(path: str | None = None):
     lib.lmoe_norm_combine_unpool.argtypes = [dp] + [vp] * 6 + [vp, sz, vp]
     lib.lmoe_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
     lib.lmoe_forward_routed.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, vp, vp, sz, vp]
+    lib.lmoe_block_workspace_bytes.argtypes = [dp]
+    lib.lmoe_block_workspace_bytes.restype = sz
+    lib.lmoe_block_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), ctypes.POINTER(LmoeBlockNorms), vp, vp, vp,
+                                       sz, vp]
     lib.lmoe_status_check.argtypes = [vp, vp]
     lib.lmoe_error_string.argtypes = [i32]
     lib.lmoe_error_string.restype = ctypes.c_char_p
@@ -85,7 +94,7 @@ def load(path: str | None = None):
     lib.lmoe_last_launch_name.argtypes = [i32]
     lib.lmoe_last_launch_name.restype = ctypes.c_char_p
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
-              "lmoe_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
+              "lmoe_forward", "lmoe_forward_routed", "lmoe_block_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
               "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option", "lmoe_selftest_dequant_bf16"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -204,6 +213,22 @@ def lmoe_forward_routed(dims, weights: LmoeWeights, x, topk_idx, topk_w, out, ws
                                       _ptr(topk_idx, (torch.int32,)), _ptr(topk_w, (torch.float32,)),
                                       _ptr(out, _BF16), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "lmoe_forward_routed")
+
+
+def norms_of(nw: dict, eps: float) -> LmoeBlockNorms:
+    """LmoeBlockNorms from device tensors {"pre_g", "post_g"} (bf16 [H]) and the norms' epsilon."""
+    return LmoeBlockNorms(_ptr(nw["pre_g"], _BF16), _ptr(nw["post_g"], _BF16), float(eps))
+
+
+def lmoe_block_workspace_bytes(dims: LmoeDims) -> int:
+    return int(load().lmoe_block_workspace_bytes(ctypes.byref(dims)))
+
+
+def lmoe_block_forward(dims, weights: LmoeWeights, norms: LmoeBlockNorms, x, y, ws, stream=None):
+    """The sandwich block y = x + post_norm(layer(pre_norm(x))); y may be x."""
+    _check(load().lmoe_block_forward(ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(norms),
+                                     _ptr(x, _BF16), _ptr(y, _BF16), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "lmoe_block_forward")
 
 
 def lmoe_status_check(ws, stream=None) -> int:

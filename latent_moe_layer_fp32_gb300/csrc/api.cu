@@ -114,7 +114,8 @@ int set_carveouts() {
       reinterpret_cast<const void*>(table_scatter_kernel), reinterpret_cast<const void*>(table_hist_kernel),
       reinterpret_cast<const void*>(combine_kernel),     reinterpret_cast<const void*>(ssq_kernel),
       reinterpret_cast<const void*>(groups_from_offsets_kernel),
-      reinterpret_cast<const void*>(gather_rows_kernel), reinterpret_cast<const void*>(router_split_kernel)};
+      reinterpret_cast<const void*>(gather_rows_kernel), reinterpret_cast<const void*>(router_split_kernel),
+      reinterpret_cast<const void*>(prenorm_kernel),     reinterpret_cast<const void*>(postnorm_residual_kernel)};
   for (const void* f : fns)
     if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
         cudaSuccess)
@@ -150,10 +151,14 @@ int router_splits(const lmoe_dims* d, int sms) {
 struct WsLayout {
   lmoe_ws_layout pub;
   size_t n_groups, route_count, zero_bytes, groups, part, h, ssq, xs, wr3, rank, chunk;
+  // the sandwich block: pre-norm output (bf16), its per-token rinv, the router
+  // input split in two bf16 parts (tensor-core router), the layer's output
+  size_t nb = 0, rinv = 0, usplit = 0, lout = 0;
   int nsplit;
 };
 
-int layout(const lmoe_dims* d, int sms, WsLayout* w) {
+// block: also the sandwich block's buffers (lmoe_block_forward)
+int layout(const lmoe_dims* d, int sms, WsLayout* w, bool block = false) {
   int rc = check_dims(d);
   if (rc) return rc;
   const size_t T = d->T, E = d->n_experts, k = d->top_k, R = T * k, L = d->latent, I = d->inter;
@@ -185,7 +190,16 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w) {
   w->ssq = take(4 * R * (L / 32));
   w->pub.z = take(2 * T * L);
   w->xs = take(2 * R * L);  // x_lat rows in sorted order (grouped tensor-core experts)
-  w->wr3 = take(2 * E * 3 * (size_t)d->hidden);  // router weights as three bf16 parts (tensor-core router)
+  // router weights as three bf16 parts (tensor-core router); the block's router
+  // takes each part twice
+  w->wr3 = take(2 * E * 3 * (size_t)d->hidden * (block ? 2 : 1));
+  if (block) {
+    const size_t H = d->hidden;
+    w->nb = take(2 * T * H);
+    w->rinv = take(4 * T);
+    w->usplit = take(2 * T * 2 * H);
+    w->lout = take(2 * T * H);
+  }
   w->pub.total = o;
   return LMOE_OK;
 }
@@ -224,13 +238,13 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttr
   } while (0)
 
 int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayout* w, cudaStream_t s,
-             bool need_ws = true) {
+             bool need_ws = true, bool block = false) {
   g_launches = 0;
   snapshot_options();
   CHECK(check_dims(d));
   CHECK(dev_info(di));
   CHECK(set_carveouts());
-  CHECK(layout(d, di->sms, w));
+  CHECK(layout(d, di->sms, w, block));
   if (need_ws) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
     if (ws_bytes < w->pub.total) return LMOE_EWORKSPACE;
@@ -239,9 +253,13 @@ int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayou
   return LMOE_OK;
 }
 
+// pre_g, rinv, usplit (the sandwich block, else null): the router's input is
+// x * pre_g with its dot products scaled by rinv per token; usplit holds
+// x * pre_g as two bf16 parts for the tensor-core router
 int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x, const float* router_w,
               const float* router_bias, int32_t* topk_idx, float* topk_w, int32_t* offsets, int32_t* sorted_rows,
-              int32_t* row_pos, void* ws, cudaStream_t s) {
+              int32_t* row_pos, void* ws, cudaStream_t s, const uint16_t* pre_g = nullptr,
+              const float* rinv = nullptr, const uint16_t* usplit = nullptr) {
   const int T = d->T, E = d->n_experts, k = d->top_k, H = d->hidden;
   Status* st = at<Status>(ws, w.pub.status);
   float* part = at<float>(ws, w.part);
@@ -249,15 +267,17 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
     // one launch: router partials, then the last CTAs finish the routing
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, route_small_kernel, x, router_w, router_bias,
            part, T, H, E, k, H / w.nsplit, group_rows(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
-           at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st);
+           at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st, pre_g, rinv);
     return LMOE_OK;
   }
   int nsplit = w.nsplit;
   if (router_tc(d)) {
-    // logits on the tensor cores: x (bf16) against the three bf16 parts of Wr, split-K partials
+    // logits on the tensor cores: x (bf16) against the three bf16 parts of Wr, split-K
+    // partials; the block's input x * g is itself two bf16 parts, against each part of Wr
     uint16_t* w3 = at<uint16_t>(ws, w.wr3);
-    LAUNCH(dim3((H + 1023) / 1024, E), dim3(256), s, router_split_kernel, router_w, E, H, w3);
-    const int kblocks = 3 * H / 64, tiles_m = (T + 127) / 128;
+    const int dup = usplit ? 2 : 1;
+    LAUNCH(dim3((H + 1023) / 1024, E), dim3(256), s, router_split_kernel, router_w, E, H, w3, dup);
+    const int kblocks = 3 * dup * H / 64, tiles_m = (T + 127) / 128;
     nsplit = 1;
     for (int c = 16; c >= 2; --c)
       if (kblocks % c == 0 && tiles_m * c <= di.sms) {
@@ -267,24 +287,24 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
     TcGemmArgs g{};
     g.M = T;
     g.N = E;
-    g.K = 3 * H;
+    g.K = 3 * dup * H;
     g.st = st;
     g.out_f32 = part;
-    g.a_kblocks = H / 64;
+    g.a_kblocks = dup * H / 64;
     g.n_tile = E;
     g.nsplit = nsplit;
     pre_launch(s, "router_tc_gemm");
-    CHECK(launch_tc_gemm_bf16(g, x, w3, s, di.sms));
+    CHECK(launch_tc_gemm_bf16(g, usplit ? usplit : x, w3, s, di.sms));
     ++g_launches;
   } else {
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T,
-           H, E, H / w.nsplit);
+           H, E, H / w.nsplit, pre_g);
   }
   const int R = T * k, nchunks = (T + kChunkTok - 1) / kChunkTok;
   int32_t* rank = at<int32_t>(ws, w.rank);
   int32_t* chunk = at<int32_t>(ws, w.chunk);
   LAUNCH(dim3(nchunks), dim3(1024), s, topk_hist_kernel, (const float*)part, nsplit, router_bias, T, E, k, topk_idx,
-         topk_w, rank, chunk);
+         topk_w, rank, chunk, rinv);
   LAUNCH(dim3(1), dim3(256), s, table_scan_kernel, chunk, nchunks, E, R, group_rows(T), offsets,
          at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups));
   LAUNCH(dim3((R + 255) / 256), dim3(256), s, table_scatter_kernel, (const int32_t*)topk_idx, (const int32_t*)rank,
@@ -422,6 +442,54 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
   return LMOE_OK;
 }
 
+int check_weights(const lmoe_weights* wt) {
+  if (!wt) return LMOE_EINVAL;
+  const void* ptrs[] = {wt->router_w, wt->pooler_w, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, wt->norm_g,
+                        wt->unpooler_w};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  if (wt->router_bias && !aligned16(wt->router_bias)) return LMOE_EINVAL;
+  return LMOE_OK;
+}
+
+// The layer, routed by its own router.  x_route feeds the router (times pre_g
+// and rinv when given), x_pool the pooler; in lmoe_forward both are x.
+int run_layer(const lmoe_dims* d, const lmoe_weights* wt, const WsLayout& w, const DevInfo& di,
+              const uint16_t* x_route, const uint16_t* x_pool, const uint16_t* pre_g, const float* rinv,
+              const uint16_t* usplit, uint16_t* out, void* ws, cudaStream_t s) {
+  int32_t* idx = at<int32_t>(ws, w.pub.topk_idx);
+  float* tw = at<float>(ws, w.pub.topk_w);
+  int32_t* srows = at<int32_t>(ws, w.pub.sorted_rows);
+  uint16_t* x_lat = at<uint16_t>(ws, w.pub.x_lat);
+  float* y = at<float>(ws, w.pub.y);
+  Status* st = at<Status>(ws, w.pub.status);
+  // The pooler depends only on its input and weights.  Small T: it runs alongside the
+  // one-launch routing and waits for it only at its end (programmatic launch).
+  // Many tokens: the routing kernels run on a side stream next to it.
+  const bool fork = d->T > 16;
+  if (fork) {
+    SideStream* ss = nullptr;
+    CHECK(side_stream(&ss));
+    if (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+      return LMOE_ECUDA;
+    CHECK(run_route(d, w, di, x_route, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
+                    srows, at<int32_t>(ws, w.pub.row_pos), ws, ss->s, pre_g, rinv, usplit));
+    if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return LMOE_ECUDA;
+    CHECK(run_pool(d, di, x_pool, wt->pooler_w, x_lat, st, s));
+    if (cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) return LMOE_ECUDA;
+  } else {
+    // the pooler's input was written before the routing kernel (or is the call's input):
+    // it may read it before its wait
+    CHECK(run_route(d, w, di, x_route, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
+                    srows, at<int32_t>(ws, w.pub.row_pos), ws, s, pre_g, rinv, usplit));
+    CHECK(run_pool(d, di, x_pool, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
+  }
+  // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
+  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
+  return LMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -504,40 +572,40 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   DevInfo di;
   WsLayout w;
   CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
-  if (!wt || !x || !out || !aligned16(x) || !aligned16(out)) return LMOE_EINVAL;
-  const void* ptrs[] = {wt->router_w, wt->pooler_w, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, wt->norm_g,
-                        wt->unpooler_w};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return LMOE_EINVAL;
-  if (wt->router_bias && !aligned16(wt->router_bias)) return LMOE_EINVAL;
-  int32_t* idx = at<int32_t>(ws, w.pub.topk_idx);
-  float* tw = at<float>(ws, w.pub.topk_w);
-  int32_t* srows = at<int32_t>(ws, w.pub.sorted_rows);
-  uint16_t* x_lat = at<uint16_t>(ws, w.pub.x_lat);
-  float* y = at<float>(ws, w.pub.y);
-  Status* st = at<Status>(ws, w.pub.status);
-  // The pooler depends only on x and its weights.  Small T: it runs alongside the
-  // one-launch routing and waits for it only at its end (programmatic launch).
-  // Many tokens: the routing kernels run on a side stream next to it.
-  const bool fork = d->T > 16;
-  if (fork) {
-    SideStream* ss = nullptr;
-    CHECK(side_stream(&ss));
-    if (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
-      return LMOE_ECUDA;
-    CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
-                    srows, at<int32_t>(ws, w.pub.row_pos), ws, ss->s));
-    if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return LMOE_ECUDA;
-    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s));
-    if (cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) return LMOE_ECUDA;
-  } else {
-    CHECK(run_route(d, w, di, x, wt->router_w, wt->router_bias, idx, tw, at<int32_t>(ws, w.pub.expert_offsets),
-                    srows, at<int32_t>(ws, w.pub.row_pos), ws, s));
-    CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
-  }
-  // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
-  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return LMOE_EINVAL;
+  CHECK(check_weights(wt));
+  CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s));
+  return post_call(s, LMOE_OK);
+}
+
+size_t lmoe_block_workspace_bytes(const lmoe_dims* d) {
+  DevInfo di;
+  int sms = (dev_info(&di) == LMOE_OK) ? di.sms : 148;
+  WsLayout w;
+  if (layout(d, sms, &w, true) != LMOE_OK) return 0;
+  return w.pub.total;
+}
+
+int lmoe_block_forward(const lmoe_dims* d, const lmoe_weights* wt, const lmoe_block_norms* nm, const uint16_t* x,
+                       uint16_t* y, void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s, true, true));
+  if (!x || !y || !aligned16(x) || !aligned16(y) || !nm || !nm->pre_g || !nm->post_g || !aligned16(nm->pre_g) ||
+      !aligned16(nm->post_g) || !(nm->eps >= 0.f))
+    return LMOE_EINVAL;
+  CHECK(check_weights(wt));
+  const int T = d->T, H = d->hidden;
+  uint16_t* nb = at<uint16_t>(ws, w.nb);
+  float* rinv = at<float>(ws, w.rinv);
+  uint16_t* usplit = router_tc(d) ? at<uint16_t>(ws, w.usplit) : nullptr;
+  uint16_t* lout = at<uint16_t>(ws, w.lout);
+  // pre-norm: the pooler's bf16 input, the router's per-token scale (and split input)
+  LAUNCH(dim3(T), dim3(256), s, prenorm_kernel, x, nm->pre_g, nm->eps, H, nb, rinv, usplit);
+  CHECK(run_layer(d, wt, w, di, x, nb, nm->pre_g, rinv, usplit, lout, ws, s));
+  // post-norm of the layer's output and the residual
+  LAUNCH(dim3(T), dim3(256), s, postnorm_residual_kernel, (const uint16_t*)lout, x, nm->post_g, nm->eps, H, y);
   return post_call(s, LMOE_OK);
 }
 

@@ -7,18 +7,22 @@
 namespace lmoe {
 
 // ---- route.cu -------------------------------------------------------------
+// g (optional): the sandwich block's pre-norm gain, the router input becomes x * g;
+// rinv (optional): per-token scale of the summed dot products (before the bias)
 __global__ void router_partial_kernel(const uint16_t* x, const float* wr, float* part, int T, int H, int E,
-                                      int split_len);
+                                      int split_len, const uint16_t* g);
 __global__ void topk_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,
-                            int32_t* topk_idx, float* topk_w);
+                            int32_t* topk_idx, float* topk_w, const float* rinv);
 __global__ void route_small_kernel(const uint16_t* x, const float* wr, const float* bias, float* part, int T, int H,
                                    int E, int k, int split_len, int G, int32_t* topk_idx, float* topk_w,
                                    int32_t* offsets, int32_t* sorted_rows, int32_t* row_pos, int4* groups,
-                                   int32_t* n_groups, int32_t* tickets, Status* st);
-__global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3);
+                                   int32_t* n_groups, int32_t* tickets, Status* st, const uint16_t* g,
+                                   const float* rinv);
+__global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3, int dup);
 constexpr int kChunkTok = 32;  // tokens per chunk of the many-token routing table
 __global__ void topk_hist_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,
-                                 int32_t* topk_idx, float* topk_w, int32_t* rank, int32_t* chunk_cnt);
+                                 int32_t* topk_idx, float* topk_w, int32_t* rank, int32_t* chunk_cnt,
+                                 const float* rinv);
 __global__ void table_hist_kernel(const int32_t* topk_idx, int T, int E, int k, int32_t* rank, int32_t* chunk_cnt,
                                   Status* st);
 __global__ void table_scan_kernel(int32_t* chunk_cnt, int nchunks, int E, int R, int G, int32_t* offsets,
@@ -122,6 +126,12 @@ __global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* sca
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
                                            int4* groups, int32_t* n_groups, Status* st);
 __global__ void ssq_kernel(const float* y, int R, int L, float* ssq);
+// ---- block.cu -------------------------------------------------------------
+__global__ void prenorm_kernel(const uint16_t* x, const uint16_t* g, float eps, int H, uint16_t* n_bf16, float* rinv,
+                               uint16_t* u_split);
+__global__ void postnorm_residual_kernel(const uint16_t* out, const uint16_t* x, const uint16_t* g, float eps, int H,
+                                         uint16_t* y);
+
 __global__ void combine_kernel(const float* y, const float* ssq, const int32_t* topk_idx, const float* topk_w,
                                const uint16_t* norm_g, int L, int k, int E, float eps, uint16_t* zb, Status* st);
 __global__ void e2m1_selftest_kernel(float* out);

@@ -94,8 +94,8 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
   const int tiles = ((E + 31) / 32) * ((T + 7) / 8);
   int ns = 1;
   while (tiles * ns < 2 * sms && ns < kNoAllocMaxSplit && H % (128 * ns * 2) == 0) ns *= 2;
-  router_partial_kernel<<<dim3((E + 31) / 32, (T + 7) / 8, ns), 256, 0, s>>>(x, router_w, part, T, H, E, H / ns);
-  topk_kernel<<<dim3(T), 256, 0, s>>>(part, ns, router_bias, T, E, k, topk_idx, topk_w);
+  router_partial_kernel<<<dim3((E + 31) / 32, (T + 7) / 8, ns), 256, 0, s>>>(x, router_w, part, T, H, E, H / ns, nullptr);
+  topk_kernel<<<dim3(T), 256, 0, s>>>(part, ns, router_bias, T, E, k, topk_idx, topk_w, nullptr);
   table_kernel<<<1, 1024, 0, s>>>(topk_idx, T * k, E, expert_max_group(T), expert_offsets, sorted_rows, row_pos,
                                   groups, n_groups, st);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;

@@ -14,11 +14,15 @@ namespace lmoe {
 // logits partials: part[s][t][e] = sum_{h in split s} x[t][h] * Wr[e][h]
 // grid (E/32, ceil(T/8), nsplit), 256 threads: warp w owns 4 experts of the
 // CTA's 32, lanes walk h in float4 steps.  fp32 FMA (not TF32).
+// With a gain g (the sandwich block's pre-norm), the input is u = x * g, a
+// product of two bf16 values and exact in fp32; the reduction then scales the
+// dot product by the token's rinv.
 // ---------------------------------------------------------------------------
 constexpr int kRouterTok = 8;
 
 __device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__ x, const float* __restrict__ wr,
-                                                    float* __restrict__ part, int T, int H, int E, int split_len) {
+                                                    float* __restrict__ part, int T, int H, int E, int split_len,
+                                                    const uint16_t* __restrict__ g) {
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -38,12 +42,26 @@ __device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__
       w[i] = (e0 + i < E) ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + i) * H + h))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float g0 = 1.f, g1 = 1.f, g2 = 1.f, g3 = 1.f;
+    if (g) {
+      const uint2 gv = __ldg(reinterpret_cast<const uint2*>(g + h));
+      g0 = bf16_bits_to_f32(gv.x & 0xffffu);
+      g1 = bf16_bits_to_f32(gv.x >> 16);
+      g2 = bf16_bits_to_f32(gv.y & 0xffffu);
+      g3 = bf16_bits_to_f32(gv.y >> 16);
+    }
 #pragma unroll
     for (int j = 0; j < kRouterTok; ++j) {
       if (j < ntok) {
         uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + j) * H + h));
         float x0 = bf16_bits_to_f32(xv.x & 0xffffu), x1 = bf16_bits_to_f32(xv.x >> 16);
         float x2 = bf16_bits_to_f32(xv.y & 0xffffu), x3 = bf16_bits_to_f32(xv.y >> 16);
+        if (g) {  // exact products
+          x0 = __fmul_rn(x0, g0);
+          x1 = __fmul_rn(x1, g1);
+          x2 = __fmul_rn(x2, g2);
+          x3 = __fmul_rn(x3, g3);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float a = acc[i][j];
@@ -72,8 +90,8 @@ __device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__
 __global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __restrict__ x,
                                                              const float* __restrict__ wr,
                                                              float* __restrict__ part, int T, int H, int E,
-                                                             int split_len) {
-  router_partial_body(x, wr, part, T, H, E, split_len);
+                                                             int split_len, const uint16_t* __restrict__ g) {
+  router_partial_body(x, wr, part, T, H, E, split_len, g);
 }
 
 // ---------------------------------------------------------------------------
@@ -153,9 +171,9 @@ __device__ __forceinline__ void topk_one_token(const float* lg_s, int E, int k, 
   }
 }
 
-// logit[e] of token t = sum over splits in split order (+ bias)
+// logit[e] of token t = sum over splits in split order (times rinv[t]) (+ bias)
 __device__ __forceinline__ float token_logit(const float* part, int nsplit, const float* bias, int T, int E, int t,
-                                             int e) {
+                                             int e, const float* rinv) {
   float v[16];
 #pragma unroll
   for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? __ldcg(part + ((size_t)sp * T + t) * E + e) : 0.f;
@@ -163,19 +181,21 @@ __device__ __forceinline__ float token_logit(const float* part, int nsplit, cons
 #pragma unroll
   for (int sp = 1; sp < 16; ++sp)
     if (sp < nsplit) acc += v[sp];
+  if (rinv) acc = __fmul_rn(acc, rinv[t]);
   if (bias) acc = acc + bias[e];
   return acc;
 }
 
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int nsplit,
                                                    const float* __restrict__ bias, int T, int E, int k,
-                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                   const float* __restrict__ rinv) {
   pdl_wait();
   pdl_trigger();
   // one CTA per token: thread e sums its partials, warp 0 selects the top k
   __shared__ float s_lg[256];
   const int t = blockIdx.x, tid = threadIdx.x;
-  if (tid < E) s_lg[tid] = token_logit(part, nsplit, bias, T, E, t, tid);
+  if (tid < E) s_lg[tid] = token_logit(part, nsplit, bias, T, E, t, tid, rinv);
   __syncthreads();
   if (tid < 32) topk_one_token(s_lg, E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, tid);
 }
@@ -333,8 +353,9 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
                                                           int32_t* __restrict__ sorted_rows,
                                                           int32_t* __restrict__ row_pos, int4* __restrict__ groups,
                                                           int32_t* __restrict__ n_groups, int32_t* tickets,
-                                                          Status* st) {
-  router_partial_body(x, wr, part, T, H, E, split_len);
+                                                          Status* st, const uint16_t* __restrict__ g,
+                                                          const float* __restrict__ rinv) {
+  router_partial_body(x, wr, part, T, H, E, split_len, g);
   __shared__ int s_last;
   const bool one_level = T <= 2;
   const int blk = blockIdx.y * gridDim.x + blockIdx.x;
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
     // thread (u, el): token blockIdx.y*8 + u, expert blockIdx.x*32 + el
     const int t = blockIdx.y * kRouterTok + (threadIdx.x >> 5), e = blockIdx.x * 32 + (threadIdx.x & 31);
     if (t < T && e < E) {
-      const float v = token_logit(part, gridDim.z, bias, T, E, t, e);
+      const float v = token_logit(part, gridDim.z, bias, T, E, t, e, rinv);
       __stcg(part + (size_t)t * E + e, v);
     }
     __syncthreads();
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
       if (one_level) {
 #pragma unroll
         for (int u = 0; u < 2; ++u)
-          v[u] = (t0 + u < T) ? token_logit(part, gridDim.z, bias, T, E, t0 + u, threadIdx.x) : 0.f;
+          v[u] = (t0 + u < T) ? token_logit(part, gridDim.z, bias, T, E, t0 + u, threadIdx.x, rinv) : 0.f;
       } else {
 #pragma unroll
         for (int u = 0; u < 8; ++u) v[u] = (t0 + u < T) ? __ldcg(part + (size_t)(t0 + u) * E + threadIdx.x) : 0.f;
@@ -401,9 +422,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
 // is one GEMM over K = 3H against x repeated three times.  Products of the bf16
 // x with each part are exact in fp32, so the tensor core reproduces an fp32
 // dot product up to the order of the fp32 sum.  Finite weights required.
+// dup = 2 lays the parts out [E][6H] as (w1 | w1 | w2 | w2 | w3 | w3) for an
+// input split in two bf16 parts (u1 | u2) repeated three times:
+//   u . w = sum over parts b of (u1 . wb + u2 . wb).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ wr, int E, int H,
-                                                           uint16_t* __restrict__ w3) {
+                                                           uint16_t* __restrict__ w3, int dup) {
   pdl_wait();
   pdl_trigger();
   // block (x, e): columns [x * 1024, x * 1024 + 1024) of expert row e, four per thread
@@ -428,10 +452,12 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
     p2[i / 2] = b2[0] | (b2[1] << 16);
     p3[i / 2] = b3[0] | (b3[1] << 16);
   }
-  uint16_t* row = w3 + (size_t)e * 3 * H;
-  *reinterpret_cast<uint2*>(row + h) = make_uint2(p1[0], p1[1]);
-  *reinterpret_cast<uint2*>(row + H + h) = make_uint2(p2[0], p2[1]);
-  *reinterpret_cast<uint2*>(row + 2 * H + h) = make_uint2(p3[0], p3[1]);
+  uint16_t* row = w3 + (size_t)e * 3 * dup * H;
+  for (int r = 0; r < dup; ++r) {
+    *reinterpret_cast<uint2*>(row + (size_t)(0 * dup + r) * H + h) = make_uint2(p1[0], p1[1]);
+    *reinterpret_cast<uint2*>(row + (size_t)(1 * dup + r) * H + h) = make_uint2(p2[0], p2[1]);
+    *reinterpret_cast<uint2*>(row + (size_t)(2 * dup + r) * H + h) = make_uint2(p3[0], p3[1]);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -480,7 +506,8 @@ __device__ __forceinline__ void chunk_ranks(const int* picks, int nrow, int E, i
 __global__ void __launch_bounds__(1024) topk_hist_kernel(const float* __restrict__ part, int nsplit,
                                                          const float* __restrict__ bias, int T, int E, int k,
                                                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                                         int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt) {
+                                                         int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt,
+                                                         const float* __restrict__ rinv) {
   pdl_wait();
   pdl_trigger();
   __shared__ float s_lg[kChunkTok][256];
@@ -497,7 +524,7 @@ __global__ void __launch_bounds__(1024) topk_hist_kernel(const float* __restrict
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      lg[i] = e < E ? token_logit(part, nsplit, bias, T, E, t, e) : 0.f;
+      lg[i] = e < E ? token_logit(part, nsplit, bias, T, E, t, e, rinv) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -540,7 +567,6 @@ __global__ void __launch_bounds__(256) table_scan_kernel(int32_t* __restrict__ c
                                                          int4* __restrict__ groups, int32_t* __restrict__ n_groups) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int s_off[257], s_goff[257];
   const int e = threadIdx.x, warp = e >> 5, lane = e & 31;
   // chunk counts in batches of 8 independent loads
   int total = 0;

@@ -82,19 +82,20 @@ def ws_view(ws: torch.Tensor, off: int, dtype, shape):
 # comparisons
 # ----------------------------------------------------------------------------------------
 
-def logit_bounds(d, absdot, depth=None):
+def logit_bounds(d, absdot, depth=None, extra_depth=0):
     """Rigorous bound on |fp32 GPU logit - correctly rounded logit|: a sum
     evaluated as a tree of depth n has error <= n * u * sum|terms|; the router
     kernel's tree is at most 4*H/128 lane terms + 5 shuffle levels + 16
-    split partials deep, plus half an ulp for the oracle's rounding."""
+    split partials deep, plus half an ulp for the oracle's rounding.
+    extra_depth adds rounding steps per term (the block's router input)."""
     if depth is None:
-        depth = 4 * d.H // 128 + 5 + 16
+        depth = 4 * d.H // 128 + 5 + 16 + extra_depth
     return (depth + 1) * 2.0 ** -24 * absdot
 
 
-def near_tie_tokens(d, logits, absdot):
+def near_tie_tokens(d, logits, absdot, extra_depth=0):
     """Tokens whose top-k boundary lies within the summation error bound."""
-    b = logit_bounds(d, absdot)
+    b = logit_bounds(d, absdot, extra_depth=extra_depth)
     order = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")
     l = logits.astype(np.float64)
     sel = order[:, :d.k]
@@ -108,15 +109,15 @@ def near_tie_tokens(d, logits, absdot):
     return np.nonzero((lo_sel <= hi_rest) | inner)[0]
 
 
-def check_indices(d, gpu_idx, ref_idx, logits, absdot):
+def check_indices(d, gpu_idx, ref_idx, logits, absdot, extra_depth=0):
     """Exact equality outside near-tie tokens; a valid top-k choice inside.
     Returns (flagged tokens, tokens whose GPU choice differs)."""
-    flagged = near_tie_tokens(d, logits, absdot)
+    flagged = near_tie_tokens(d, logits, absdot, extra_depth)
     ok = np.ones(gpu_idx.shape[0], bool)
     ok[flagged] = False
     bad = np.nonzero((gpu_idx != ref_idx).any(1) & ok)[0]
     assert bad.size == 0, f"index mismatch outside near ties: tokens {bad[:10]}"
-    b = logit_bounds(d, absdot)
+    b = logit_bounds(d, absdot, extra_depth=extra_depth)
     l = logits.astype(np.float64)
     for t in flagged:
         S = gpu_idx[t]

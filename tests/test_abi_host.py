@@ -61,6 +61,15 @@ def test_workspace_sizing_without_gpu(lm):
         assert lay.z + 2 * d.T * d.L <= n
 
 
+def test_block_workspace_sizing_without_gpu(lm):
+    for name, d in synth.CONFIGS.items():
+        dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+        n, nb = lm.lmoe_workspace_bytes(dims), lm.lmoe_block_workspace_bytes(dims)
+        # the layer's workspace plus the pre-norm output, the split router input and the layer output
+        assert nb >= n + 2 * d.T * d.H + 4 * d.T * d.H + 2 * d.T * d.H, name
+    assert lm.lmoe_block_workspace_bytes(lm.dims_of(0, 512, 256, 256, 16, 4, 1e-6)) == 0
+
+
 @pytest.mark.parametrize("field,value", [("T", 0), ("top_k", 9), ("top_k", 0), ("n_experts", 257),
                                          ("hidden", 100), ("latent", 96), ("inter", 0), ("eps", -1.0)])
 def test_bad_dims_rejected(lm, field, value):

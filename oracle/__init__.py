@@ -71,6 +71,12 @@ class Oracle:
         L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, vp, ctypes.c_float, vp]
         L.oracle_bf16_round.argtypes = [i64, vp, vp]
         L.oracle_residual_add.argtypes = [i64, vp, vp, vp]
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+        L.oracle_e4m3_value.restype = ctypes.c_float
+        L.oracle_nvfp4_value.argtypes = [ctypes.c_uint, ctypes.c_uint]
+        L.oracle_nvfp4_value.restype = ctypes.c_float
+        L.oracle_experts_nvfp4.argtypes = [dp] + [vp] * 11
+        L.oracle_experts_nvfp4.restype = None
         for f in ("oracle_router_logits", "oracle_topk", "oracle_table", "oracle_pool", "oracle_experts",
                   "oracle_norm_combine", "oracle_unpool", "oracle_forward", "oracle_set_threads",
                   "oracle_router_logits_f32", "oracle_rmsnorm_rows", "oracle_bf16_round", "oracle_residual_add"):
@@ -94,6 +100,12 @@ class Oracle:
 
     def mxfp4_value(self, code: int, scale: int) -> float:
         return float(self.lib.oracle_mxfp4_value(code, scale))
+
+    def e4m3_value(self, b: int) -> float:
+        return float(self.lib.oracle_e4m3_value(b))
+
+    def nvfp4_value(self, code: int, scale_byte: int) -> float:
+        return float(self.lib.oracle_nvfp4_value(code, scale_byte))
 
     # -- stages ---------------------------------------------------------------------
     def router_logits(self, d, x, router_w, router_bias=None, want_absdot=False):
@@ -134,6 +146,30 @@ class Oracle:
         self.lib.oracle_experts(ctypes.byref(od), _p(x_lat), _p(np.ascontiguousarray(topk_idx)),
                                 _p(w["w13_q"]), _p(w["w13_s"]), _p(w["w2_q"]), _p(w["w2_s"]), _p(h), _p(gu), _p(y))
         return (y, h, gu) if want_intermediates else y
+
+    def experts_nvfp4(self, d, x_lat, topk_idx, w, want_intermediates=False):
+        """The experts on NVFP4 weights: w holds w13_q, w13_s (E4M3 [E][2I][L/16]),
+        w13_gs (fp32 [E]), w2_q, w2_s ([E][L][I/16]) and w2_gs."""
+        od = self.dims(d, x_lat.shape[0])
+        R = od.T * d.k
+        y = np.empty((R, d.L), np.float32)
+        h = np.empty((R, d.I), np.uint16) if want_intermediates else None
+        gu = np.empty((R, 2 * d.I), np.float32) if want_intermediates else None
+        self.lib.oracle_experts_nvfp4(ctypes.byref(od), _p(x_lat), _p(np.ascontiguousarray(topk_idx)),
+                                      _p(w["w13_q"]), _p(w["w13_s"]), _p(w["w13_gs"]), _p(w["w2_q"]),
+                                      _p(w["w2_s"]), _p(w["w2_gs"]), _p(h), _p(gu), _p(y))
+        return (y, h, gu) if want_intermediates else y
+
+    def forward_nvfp4(self, d, x, w):
+        """Whole layer with NVFP4 expert weights (the router, pooler, norm and
+        unpooler as in forward())."""
+        logits = self.router_logits(d, x, w["router_w"], w.get("router_bias"))
+        idx, tw = self.topk(d, logits)
+        x_lat = self.pool(d, x, w["pooler_w"])
+        y = self.experts_nvfp4(d, x_lat, idx, w)
+        z = self.norm_combine(d, y, idx, tw, w["norm_g"])
+        return {"out": self.unpool(d, z, w["unpooler_w"]), "x_lat": x_lat, "y": y, "z": z, "topk_idx": idx,
+                "topk_w": tw}
 
     def norm_combine(self, d, y, topk_idx, topk_w, norm_g, want_yhat=False):
         T = topk_idx.shape[0]

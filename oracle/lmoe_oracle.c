@@ -49,6 +49,17 @@
  *   5 weights not renormalised      6 ties go to the higher index
  *   7 norm applied to the sum       8 norm gain dropped
  *   9 row RMSNorm drops its gain    10 block drops the residual
+ *  11 NVFP4 blocks of 32           12 NVFP4 global scale dropped
+ *
+ * NVFP4 expert weights ("Muse Spark Open on Gaudi 2" and the vLLM page name
+ * the NVFP4 checkpoint; they give no layout).  The format follows NVIDIA's
+ * public NVFP4 description: E2M1 elements as in MXFP4 (two per byte, low
+ * nibble = even element), one FP8 E4M3 scale per 16 consecutive elements
+ * along K (the OCP 8-bit floating point E4M3 encoding: bias 7, no infinity,
+ * S.1111.111 = NaN), and one fp32 scale per expert matrix:
+ *   w[n][c] = (E2M1(nibble) * E4M3(scale[n][c/16])) * global[e].
+ * E2M1 * E4M3 has at most 6 significant bits, exact in fp32 (and bf16); the
+ * product with the fp32 global scale is rounded once.
  *
  * The transformer block around the layer ("Soporte de dia 0 para Muse Spark
  * Open en vLLM", section "Normalizacion en sandwich": one norm before the
@@ -120,6 +131,24 @@ static float e8m0_value(unsigned s) {
   return ldexpf(1.0f, (int)s - 127 + (LMOE_ORACLE_PLANT == 4));
 }
 
+/* OCP FP8 E4M3: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa;
+ * exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinity. */
+float oracle_e4m3_value(unsigned b) {
+  unsigned s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
+  float mag;
+  if (e == 15u && m == 7u) return NAN;
+  if (e == 0u)
+    mag = ldexpf((float)m / 8.0f, -6);
+  else
+    mag = ldexpf(1.0f + (float)m / 8.0f, (int)e - 7);
+  return s ? -mag : mag;
+}
+
+/* E2M1 code times an E4M3 scale byte (the NVFP4 block value before the global scale). */
+float oracle_nvfp4_value(unsigned code, unsigned scale_byte) {
+  return e2m1_value(code & 15u) * oracle_e4m3_value(scale_byte & 255u);
+}
+
 /* One dequantised MXFP4 element: value of code `code` under block scale `s`.
  * Exact in fp32 for s <= 252 (the product has at most 2 significant bits). */
 float oracle_mxfp4_value(unsigned code, unsigned s) { return e2m1_value(code & 15u) * e8m0_value(s); }
@@ -128,10 +157,12 @@ float oracle_mxfp4_value(unsigned code, unsigned s) { return e2m1_value(code & 1
  * entry is exactly the function's value). */
 static float g_e2m1_tab[16];
 static float g_e8m0_tab[256];
+static float g_e4m3_tab[256];
 static pthread_once_t g_tab_once = PTHREAD_ONCE_INIT;
 static void fill_tables(void) {
   for (unsigned c = 0; c < 16; ++c) g_e2m1_tab[c] = e2m1_value(c);
   for (unsigned s = 0; s < 256; ++s) g_e8m0_tab[s] = e8m0_value(s);
+  for (unsigned s = 0; s < 256; ++s) g_e4m3_tab[s] = oracle_e4m3_value(s);
 }
 
 /* Element c of row n of a packed [N][K/2] code matrix with [N][K/32] scales. */
@@ -139,6 +170,21 @@ static inline float mx_elem(const uint8_t* q, const uint8_t* sc, int64_t n, int6
   uint8_t byte = q[n * (K / 2) + c / 2];
   unsigned code = ((c & 1) ^ (LMOE_ORACLE_PLANT == 1)) ? (byte >> 4) : (byte & 15u);
   return g_e2m1_tab[code] * g_e8m0_tab[sc[n * (K / 32) + c / 32]];
+}
+
+/* NVFP4 element c of row n: [N][K/2] codes, [N][K/16] E4M3 scales, the
+ * matrix's global scale gs. */
+#define NV_BLOCK (LMOE_ORACLE_PLANT == 11 ? 32 : 16)
+static inline float nv_elem(const uint8_t* q, const uint8_t* sc, int64_t n, int64_t K, int64_t c, float gs) {
+  uint8_t byte = q[n * (K / 2) + c / 2];
+  unsigned code = (c & 1) ? (byte >> 4) : (byte & 15u);
+  float v = g_e2m1_tab[code] * g_e4m3_tab[sc[n * (K / 16) + c / NV_BLOCK]];
+#if LMOE_ORACLE_PLANT == 12
+  (void)gs;
+  return v;
+#else
+  return v * gs;
+#endif
 }
 
 /* ------------------------------------------------------------------------ */
@@ -350,7 +396,18 @@ typedef struct {
   uint16_t* h;  /* [R][I] bf16, required scratch */
   float* gu;    /* [R][2I] optional pre-activation gate/up */
   float* y;     /* [R][L] */
+  const float *w13gs, *w2gs; /* NVFP4 global scales [E] (both NULL: MXFP4) */
 } exp_ctx;
+
+/* element c of row n of W13 / W2 in the context's format */
+static inline float w13_elem(const exp_ctx* c, int64_t e, int64_t n, int64_t col) {
+  int64_t L = c->d->L;
+  return c->w13gs ? nv_elem(c->w13q, c->w13s, n, L, col, c->w13gs[e]) : mx_elem(c->w13q, c->w13s, n, L, col);
+}
+static inline float w2_elem(const exp_ctx* c, int64_t e, int64_t n, int64_t col) {
+  int64_t I = c->d->I;
+  return c->w2gs ? nv_elem(c->w2q, c->w2s, n, I, col, c->w2gs[e]) : mx_elem(c->w2q, c->w2s, n, I, col);
+}
 
 /* phase 1 body: one (row, feature) pair -> gate, up, h */
 static void gateup_body(void* p, int64_t i) {
@@ -364,8 +421,8 @@ static void gateup_body(void* p, int64_t i) {
   { int64_t tmp = gate_row; gate_row = up_row; up_row = tmp; }
 #endif
   float g = 0.0f, u = 0.0f;
-  for (int64_t l = 0; l < L; ++l) g += bf16_val(xr[l]) * mx_elem(c->w13q, c->w13s, gate_row, L, l);
-  for (int64_t l = 0; l < L; ++l) u += bf16_val(xr[l]) * mx_elem(c->w13q, c->w13s, up_row, L, l);
+  for (int64_t l = 0; l < L; ++l) g += bf16_val(xr[l]) * w13_elem(c, e, gate_row, l);
+  for (int64_t l = 0; l < L; ++l) u += bf16_val(xr[l]) * w13_elem(c, e, up_row, l);
   float silu = g / (1.0f + expf(-g));
   c->h[r * I + f] = oracle_bf16_rne(silu * u);
   if (c->gu) {
@@ -383,9 +440,9 @@ static void down_body(void* p, int64_t i) {
   const uint16_t* hr = c->h + r * I;
   float acc = 0.0f;
 #if LMOE_ORACLE_PLANT == 3
-  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * mx_elem(c->w2q, c->w2s, e * L + f, I, l);
+  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + f, l);
 #else
-  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * mx_elem(c->w2q, c->w2s, e * L + l, I, f);
+  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + l, f);
 #endif
   c->y[r * L + l] = acc;
 }
@@ -399,7 +456,21 @@ void oracle_experts(const or_dims* d, const uint16_t* x_lat, const int32_t* topk
   int64_t R = (int64_t)d->T * d->k;
   pthread_once(&g_tab_once, fill_tables);
   uint16_t* h = h_out ? h_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(R * d->I));
-  exp_ctx c = {d, x_lat, topk_idx, w13_q, w13_s, w2_q, w2_s, h, gu_out, y};
+  exp_ctx c = {d, x_lat, topk_idx, w13_q, w13_s, w2_q, w2_s, h, gu_out, y, NULL, NULL};
+  parallel_for(R * d->I, gateup_body, &c);
+  parallel_for(R * d->L, down_body, &c);
+  if (!h_out) free(h);
+}
+
+/* The same experts on NVFP4 weights: w13_s [E][2I][L/16] and w2_s [E][L][I/16]
+ * E4M3 bytes, w13_gs and w2_gs the fp32 global scale of each expert's matrix. */
+void oracle_experts_nvfp4(const or_dims* d, const uint16_t* x_lat, const int32_t* topk_idx, const uint8_t* w13_q,
+                          const uint8_t* w13_s, const float* w13_gs, const uint8_t* w2_q, const uint8_t* w2_s,
+                          const float* w2_gs, uint16_t* h_out, float* gu_out, float* y) {
+  int64_t R = (int64_t)d->T * d->k;
+  pthread_once(&g_tab_once, fill_tables);
+  uint16_t* h = h_out ? h_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(R * d->I));
+  exp_ctx c = {d, x_lat, topk_idx, w13_q, w13_s, w2_q, w2_s, h, gu_out, y, w13_gs, w2_gs};
   parallel_for(R * d->I, gateup_body, &c);
   parallel_for(R * d->L, down_body, &c);
   if (!h_out) free(h);

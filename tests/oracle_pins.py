@@ -31,6 +31,14 @@ en sandwich") is pinned by BLOCK_PINS:
   * block               -> a zero post-norm gain or a zero unpooler gives y = x
     exactly; with eps = 0 the layer output does not change when x is scaled by
     a power of two (the norm comes first); token independence
+
+NVFP4 expert weights (NV_PINS):
+  * E4M3 decode         -> torch's float8_e4m3fn conversion over all 256 bytes and
+    the OCP FP8 values in tests/golden
+  * E2M1 x E4M3         -> exact in fp32 and bf16 for every code and scale byte
+  * experts             -> brute-force dense evaluation from an independent numpy
+    NVFP4 dequantiser (16-element blocks, per-matrix global scale)
+  * global scale        -> doubling an expert's W2 global scale doubles its y rows exactly
 """
 from __future__ import annotations
 
@@ -417,3 +425,99 @@ def pin_block_token_independence(o, c):
 
 BLOCK_PINS = [pin_rmsnorm_invariants, pin_router_f32_input, pin_block_identity_paths, pin_block_norm_first,
               pin_block_token_independence]
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 expert weights
+# --------------------------------------------------------------------------------------
+
+def golden_e4m3() -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, "e4m3_ocp_fp8.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                b, v = line.split()
+                out[int(b, 16)] = float(v)
+    return out
+
+
+def e4m3_torch(b: np.ndarray) -> np.ndarray:
+    """E4M3 bytes -> fp64 through torch's float8_e4m3fn conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def dequant_dense_nvfp4(q: np.ndarray, s: np.ndarray, gs: np.ndarray) -> np.ndarray:
+    """[E, N, K/2] codes + [E, N, K/16] E4M3 scales + [E] global scales -> fp64
+    [E, N, K]: element 2m is the low nibble of byte m, 2m+1 the high one."""
+    table = golden_e2m1()
+    codes = np.stack([table[q & 15], table[q >> 4]], axis=-1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    scale = np.repeat(e4m3_torch(s), 16, axis=-1)
+    return codes * scale * gs.astype(np.float64)[:, None, None]
+
+
+class NvCase:
+    def __init__(self, o, d, x, w):
+        self.d, self.x, self.w = d, x, w
+        lg = o.router_logits(d, x, w["router_w"], w["router_bias"])
+        self.idx, self.tw = o.topk(d, lg)
+        self.x_lat = o.pool(d, x, w["pooler_w"])
+        self.y, self.h, self.gu = o.experts_nvfp4(d, self.x_lat, self.idx, w, want_intermediates=True)
+
+
+def make_nv_case(o, T=16, seed=0):
+    d = synth.with_tokens(synth.CONFIGS["tiny"], T)
+    return NvCase(o, d, synth.make_x(d, seed), synth.make_weights_nvfp4(d, seed))
+
+
+def pin_e4m3_decode(o, c):
+    ref = e4m3_torch(np.arange(256, dtype=np.uint8))
+    for b in range(256):
+        v = o.e4m3_value(b)
+        if math.isnan(ref[b]):
+            assert math.isnan(v), b
+        else:
+            assert v == ref[b] and math.copysign(1.0, v) == math.copysign(1.0, ref[b]), (b, v, ref[b])
+    for b, v in golden_e4m3().items():
+        got = o.e4m3_value(b)
+        assert (math.isnan(got) and math.isnan(v)) or (got == v and math.copysign(1, got) == math.copysign(1, v)), b
+
+
+def pin_nvfp4_products_exact(o, c):
+    table = golden_e2m1()
+    sc = e4m3_torch(np.arange(256, dtype=np.uint8))
+    for b in range(256):
+        if math.isnan(sc[b]):
+            continue
+        for code in range(16):
+            v = o.nvfp4_value(code, b)
+            assert v == table[code] * sc[b], (code, b)
+            bits = np.array([v], np.float32).view(np.uint32)[0]
+            assert bits & 0xFFFF == 0, (code, b)  # exact in bf16 as well
+
+
+def pin_experts_nvfp4_dense(o, c):
+    d, w = c.d, c.w
+    W13 = dequant_dense_nvfp4(w["w13_q"], w["w13_s"], w["w13_gs"])
+    W2 = dequant_dense_nvfp4(w["w2_q"], w["w2_s"], w["w2_gs"])
+    xl = bf16_to_f64(c.x_lat)
+    t_of_r = np.arange(d.T * d.k) // d.k
+    e_of_r = c.idx.reshape(-1)
+    G = np.einsum("rl,rfl->rf", xl[t_of_r], W13[e_of_r])
+    A = np.einsum("rl,rfl->rf", np.abs(xl[t_of_r]), np.abs(W13[e_of_r]))
+    # one more rounding per term: the fp32 product with the global scale
+    assert np.all(np.abs(c.gu.astype(np.float64) - G) <= (d.L + 2) * EPS32 * A + 1e-30), \
+        np.max(np.abs(c.gu - G) / (A + 1e-30))
+    h_got = bf16_to_f64(c.h)
+    Y = np.einsum("ri,rli->rl", h_got, W2[e_of_r])
+    B = np.einsum("ri,rli->rl", np.abs(h_got), np.abs(W2[e_of_r]))
+    assert np.all(np.abs(c.y.astype(np.float64) - Y) <= (d.I + 2) * EPS32 * B + 1e-30)
+
+
+def pin_nvfp4_global_scale(o, c):
+    w2 = dict(c.w, w2_gs=(c.w["w2_gs"] * 2).astype(np.float32))
+    y2 = o.experts_nvfp4(c.d, c.x_lat, c.idx, w2)
+    assert np.array_equal(y2, c.y * 2)
+
+
+NV_PINS = [pin_e4m3_decode, pin_nvfp4_products_exact, pin_experts_nvfp4_dense, pin_nvfp4_global_scale]

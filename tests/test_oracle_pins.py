@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from oracle_pins import BLOCK_PINS, PINS, make_block_case, make_case
+from oracle_pins import BLOCK_PINS, NV_PINS, PINS, make_block_case, make_case, make_nv_case
 
 
 @pytest.fixture(scope="module")
@@ -114,9 +114,20 @@ def test_block_pin(pin, o, block_case):
     pin(o, block_case)
 
 
+@pytest.fixture(scope="module")
+def nv_case(o):
+    return make_nv_case(o)
+
+
+@pytest.mark.parametrize("pin", NV_PINS, ids=[p.__name__ for p in NV_PINS])
+def test_nv_pin(pin, o, nv_case):
+    pin(o, nv_case)
+
+
 PLANTS = {1: "nibble order", 2: "gate/up swapped", 3: "W2 transposed", 4: "scale off by one",
           5: "no renormalisation", 6: "ties to higher index", 7: "norm on the sum", 8: "gain dropped",
-          9: "row RMSNorm gain dropped", 10: "block residual dropped"}
+          9: "row RMSNorm gain dropped", 10: "block residual dropped", 11: "NVFP4 blocks of 32",
+          12: "NVFP4 global scale dropped"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=[PLANTS[k] for k in sorted(PLANTS)])
@@ -136,6 +147,12 @@ def test_planted_mistake_is_caught(plant):
     for pin in BLOCK_PINS:
         try:
             pin(bad, bc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    nc = make_nv_case(bad)
+    for pin in NV_PINS:
+        try:
+            pin(bad, nc)
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake '{PLANTS[plant]}' passed every pin"

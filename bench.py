@@ -43,6 +43,7 @@ import synth  # noqa: E402
 
 METRIC = "latent-MoE layer tokens/s and HBM GB/s (frac of roofline) at T=1..4096"
 EXPERT_BYTES = 26_738_688          # one expert: 3 matrices x (codes 8 MiB + scales 512 KiB)
+EXPERT_BYTES_NVFP4 = 28_311_552    # NVFP4: 3 matrices x (codes 8 MiB + E4M3 scales 1 MiB) (+ 8 B global scales)
 GATEUP_BYTES = 2 * EXPERT_BYTES // 3
 PROJ_BYTES = 134_217_728           # pooler + unpooler bf16
 # source files each measured kernel is built from (the ncu summary's source_sha256 covers these)
@@ -202,7 +203,7 @@ def allreduce_max(world, v: float) -> float:
     return float(t.item())
 
 
-def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000, block_norms=None):
+def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000, block_norms=None, nvfp4=False):
     """Tokens/s of the CPU oracle on repeated whole-layer (or whole-block) evaluations of `x`."""
     import oracle
     o = oracle.get()
@@ -210,6 +211,8 @@ def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000, block_norms=None)
     while reps < max_reps:
         if block_norms is not None:
             o.block_forward(d, x, hw, block_norms)
+        elif nvfp4:
+            o.forward_nvfp4(d, x, hw)
         else:
             o.forward(d, x, hw)
         reps += 1
@@ -328,6 +331,9 @@ def main():
                     help="a step runs this many layers back to back, each layer's output the next one's input "
                          "and each layer with its own device copy of the weights")
     ap.add_argument("--graph", action="store_true", help="capture one step in a CUDA graph and replay it")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="NVFP4 expert weights (E4M3 scale per 16 elements, fp32 global scale per expert matrix) "
+                         "through lmoe_forward_nvfp4")
     ap.add_argument("--block", action="store_true",
                     help="time the sandwich block around the layer (lmoe_block_forward: pre-norm, layer, "
                          "post-norm and residual) instead of the layer alone")
@@ -353,7 +359,13 @@ def main():
         run_stage(args, d, name, lm, dev)
         return
 
-    hw = synth.make_weights(d)
+    if args.nvfp4 and (args.block or args.routed):
+        raise SystemExit("--nvfp4 times lmoe_forward_nvfp4; it does not combine with --block or --routed")
+    if args.nvfp4:
+        global EXPERT_BYTES, GATEUP_BYTES
+        EXPERT_BYTES = EXPERT_BYTES_NVFP4
+        GATEUP_BYTES = 2 * EXPERT_BYTES // 3
+    hw = synth.make_weights_nvfp4(d) if args.nvfp4 else synth.make_weights(d)
     x = synth.make_x(d)
 
     def to_dev(a):
@@ -377,7 +389,12 @@ def main():
     block_norms = synth.make_block_norms(d) if args.block else None
     if args.block and args.routed:
         raise SystemExit("--block runs the block's own router; it does not combine with --routed")
-    if args.block:
+    if args.nvfp4:
+        nv_layers = [lm.nvfp4_of(wl) for wl in w_layers]
+
+        def forward(xd, o, layer=0):
+            lm.lmoe_forward_nvfp4(dims, wts_layers[layer], nv_layers[layer], xd, o, ws)
+    elif args.block:
         nw_dev = {k: to_dev(v) for k, v in block_norms.items()}
         norms = lm.norms_of(nw_dev, d.eps)
 
@@ -520,7 +537,7 @@ def main():
         roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic = traffic_from_profiles(dom, name)
+    traffic = None if args.nvfp4 else traffic_from_profiles(dom, name)
     roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes_per_launch": dom_bytes,
                  "launch_ms": dom_ms, "peak_source": pk["source"] + (
                      "" if roof["bound"] == "hbm" else
@@ -535,6 +552,8 @@ def main():
                                                           "lmoe_forward_routed)" if args.routed else "") +
                    (" inside the sandwich block (pre-norm, fp32 router input, post-norm, residual; "
                     "lmoe_block_forward)" if args.block else "") +
+                   (" with NVFP4 experts (E4M3 scale per 16 elements, fp32 global scale per matrix; "
+                    "lmoe_forward_nvfp4)" if args.nvfp4 else "") +
                    (f", {n_layers} layers per step" if n_layers > 1 else "") + (", CUDA graph" if args.graph else ""),
                    "T": d.T, "touched_experts": touched, "layers_per_step": n_layers,
                    "l2": "flushed between steps (512 MB device write outside the timed events)",
@@ -550,7 +569,7 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, reps, dt = cpu_oracle_rate(d, hw, x, block_norms=block_norms)
+        rate, cores, reps, dt = cpu_oracle_rate(d, hw, x, block_norms=block_norms, nvfp4=args.nvfp4)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{reps} whole-{'block' if args.block else 'layer'} evaluations of the T={d.T} workload ({dt:.1f} s)"}
     if rank == 0:

@@ -187,6 +187,31 @@ LMOE_API int lmoe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weig
                                  const int32_t* topk_idx, const float* topk_w, uint16_t* out, void* ws,
                                  size_t ws_bytes, lmoe_stream_t stream);
 
+/* NVFP4 expert weights (the pages' checkpoint format, "Muse Spark Open on
+ * Gaudi 2" and the vLLM page; they give no layout, so this follows NVIDIA's
+ * public NVFP4 description): the same E2M1 codes as MXFP4 (two per byte, low
+ * nibble = even element), one FP8 E4M3 scale byte per 16 elements along K
+ * (OCP FP8 E4M3: bias 7, no infinity, S.1111.111 = NaN), and an fp32 global
+ * scale per expert matrix:  w[n][c] = E2M1 * E4M3(s[n][c/16]) * global[e].
+ * With NVFP4, lmoe_weights.w13_s is E4M3 [E][2I][L/16] and w2_s [E][L][I/16]. */
+typedef struct {
+  const float* w13_gs; /* fp32 [E], global scale of each expert's W13 (gate and up) */
+  const float* w2_gs;  /* fp32 [E], global scale of each expert's W2 */
+} lmoe_nvfp4_scales;
+
+/* lmoe_experts_mxfp4 on NVFP4 weights (see above); same arguments otherwise.
+ *   w13_s E4M3 [E][2I][L/16];  w2_s E4M3 [E][L][I/16];  w13_gs, w2_gs fp32 [E] */
+LMOE_API int lmoe_experts_nvfp4(const lmoe_dims* dims, const uint16_t* x_lat, const int32_t* expert_offsets,
+                                const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s,
+                                const float* w13_gs, const uint8_t* w2_q, const uint8_t* w2_s, const float* w2_gs,
+                                float* y, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
+/* lmoe_forward with NVFP4 experts: weights->w13_s and w2_s hold the E4M3
+ * scales, `nv` the global scales.  Workspace, streams and errors as for
+ * lmoe_forward (LMOE_EINVAL if nv or one of its arrays is NULL). */
+LMOE_API int lmoe_forward_nvfp4(const lmoe_dims* dims, const lmoe_weights* weights, const lmoe_nvfp4_scales* nv,
+                                const uint16_t* x, uint16_t* out, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
 /* The transformer block around the layer, with sandwich normalisation
  * ("Soporte de dia 0 para Muse Spark Open en vLLM", section "Normalizacion en
  * sandwich": y = x + post_norm(F(pre_norm(x)))), and the router fed by the

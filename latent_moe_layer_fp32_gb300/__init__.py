@@ -20,7 +20,8 @@ __all__ = [
     "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
     "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_route_noalloc", "lmoe_pool", "lmoe_experts_mxfp4",
     "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_block_workspace_bytes",
-    "lmoe_block_forward", "norms_of", "lmoe_status_check", "lmoe_error_string",
+    "lmoe_block_forward", "norms_of", "lmoe_experts_nvfp4", "lmoe_forward_nvfp4", "nvfp4_of",
+    "lmoe_status_check", "lmoe_error_string",
     "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
 ]
 
@@ -42,6 +43,10 @@ class LmoeWeights(ctypes.Structure):
 
 class LmoeBlockNorms(ctypes.Structure):
     _fields_ = [("pre_g", ctypes.c_void_p), ("post_g", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
+class LmoeNvfp4Scales(ctypes.Structure):
+    _fields_ = [("w13_gs", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p)]
 
 
 class LmoeWsLayout(ctypes.Structure):
@@ -75,6 +80,9 @@ def load(path: str | None = None):
     lib.lmoe_route.argtypes = [dp] + [vp] * 8 + [vp, sz, vp]
     lib.lmoe_pool.argtypes = [dp, vp, vp, vp, vp, sz, vp]
     lib.lmoe_experts_mxfp4.argtypes = [dp] + [vp] * 8 + [vp, sz, vp]
+    lib.lmoe_experts_nvfp4.argtypes = [dp] + [vp] * 10 + [vp, sz, vp]
+    lib.lmoe_forward_nvfp4.argtypes = [dp, ctypes.POINTER(LmoeWeights), ctypes.POINTER(LmoeNvfp4Scales), vp, vp, vp,
+                                       sz, vp]
     lib.lmoe_norm_combine_unpool.argtypes = [dp] + [vp] * 6 + [vp, sz, vp]
     lib.lmoe_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
     lib.lmoe_forward_routed.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, vp, vp, sz, vp]
@@ -94,7 +102,8 @@ def load(path: str | None = None):
     lib.lmoe_last_launch_name.argtypes = [i32]
     lib.lmoe_last_launch_name.restype = ctypes.c_char_p
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
-              "lmoe_forward", "lmoe_forward_routed", "lmoe_block_forward", "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
+              "lmoe_forward", "lmoe_forward_routed", "lmoe_block_forward", "lmoe_forward_nvfp4", "lmoe_experts_nvfp4",
+              "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
               "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option", "lmoe_selftest_dequant_bf16"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -193,6 +202,28 @@ def lmoe_experts_mxfp4(dims, x_lat, expert_offsets, sorted_rows, w13_q, w13_s, w
                                      _ptr(sorted_rows, _I32), _ptr(w13_q, _U8), _ptr(w13_s, _U8), _ptr(w2_q, _U8),
                                      _ptr(w2_s, _U8), _ptr(y, _F32), _ptr(ws), ws.numel() * ws.element_size(),
                                      _stream(stream)), "lmoe_experts_mxfp4")
+
+
+def lmoe_experts_nvfp4(dims, x_lat, expert_offsets, sorted_rows, w13_q, w13_s, w13_gs, w2_q, w2_s, w2_gs, y, ws,
+                       stream=None):
+    """The experts on NVFP4 weights: E4M3 scales per 16 elements, fp32 global scales [E]."""
+    _check(load().lmoe_experts_nvfp4(ctypes.byref(dims), _ptr(x_lat, _BF16), _ptr(expert_offsets, _I32),
+                                     _ptr(sorted_rows, _I32), _ptr(w13_q, _U8), _ptr(w13_s, _U8),
+                                     _ptr(w13_gs, _F32), _ptr(w2_q, _U8), _ptr(w2_s, _U8), _ptr(w2_gs, _F32),
+                                     _ptr(y, _F32), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "lmoe_experts_nvfp4")
+
+
+def nvfp4_of(w: dict) -> LmoeNvfp4Scales:
+    """LmoeNvfp4Scales from device tensors {"w13_gs", "w2_gs"} (fp32 [E])."""
+    return LmoeNvfp4Scales(_ptr(w["w13_gs"], _F32), _ptr(w["w2_gs"], _F32))
+
+
+def lmoe_forward_nvfp4(dims, weights: LmoeWeights, nv: LmoeNvfp4Scales, x, out, ws, stream=None):
+    """The layer with NVFP4 experts (weights.w13_s / w2_s hold the E4M3 scales)."""
+    _check(load().lmoe_forward_nvfp4(ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(nv), _ptr(x, _BF16),
+                                     _ptr(out, _BF16), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "lmoe_forward_nvfp4")
 
 
 def lmoe_norm_combine_unpool(dims, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, stream=None):

@@ -344,7 +344,7 @@ int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uin
 int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
                 const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                 const uint8_t* w2_s, float* y, void* ws, cudaStream_t s, bool xs_ready = false,
-                bool groups_early = false) {
+                bool groups_early = false, const float* w13_gs = nullptr, const float* w2_gs = nullptr) {
   const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
   if (experts_tc(T)) {
@@ -362,6 +362,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
     t.st = st;
     t.q = w13_q;
     t.s = w13_s;
+    t.gs = w13_gs;
     t.K = L;
     t.h_out = at<uint16_t>(ws, w.h);
     pre_launch(s, "expert_gateup_tc");
@@ -369,6 +370,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
     ++g_launches;
     t.q = w2_q;
     t.s = w2_s;
+    t.gs = w2_gs;
     t.K = I;
     t.h_out = nullptr;
     t.y_out = y;
@@ -390,6 +392,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.st = st;
   a.q = w13_q;
   a.s = w13_s;
+  a.gs = w13_gs;
   a.act = x_lat;
   a.K = L;
   a.h_out = at<uint16_t>(ws, w.h);
@@ -401,6 +404,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   ++g_launches;
   a.q = w2_q;
   a.s = w2_s;
+  a.gs = w2_gs;
   a.act = at<uint16_t>(ws, w.h);
   a.K = I;
   a.h_out = nullptr;
@@ -454,9 +458,11 @@ int check_weights(const lmoe_weights* wt) {
 
 // The layer, routed by its own router.  x_route feeds the router (times pre_g
 // and rinv when given), x_pool the pooler; in lmoe_forward both are x.
+// nv (NVFP4 experts, else null): the global scales; wt->w13_s and w2_s are then E4M3 per 16
 int run_layer(const lmoe_dims* d, const lmoe_weights* wt, const WsLayout& w, const DevInfo& di,
               const uint16_t* x_route, const uint16_t* x_pool, const uint16_t* pre_g, const float* rinv,
-              const uint16_t* usplit, uint16_t* out, void* ws, cudaStream_t s) {
+              const uint16_t* usplit, uint16_t* out, void* ws, cudaStream_t s,
+              const lmoe_nvfp4_scales* nv = nullptr) {
   int32_t* idx = at<int32_t>(ws, w.pub.topk_idx);
   float* tw = at<float>(ws, w.pub.topk_w);
   int32_t* srows = at<int32_t>(ws, w.pub.sorted_rows);
@@ -485,7 +491,8 @@ int run_layer(const lmoe_dims* d, const lmoe_weights* wt, const WsLayout& w, con
     CHECK(run_pool(d, di, x_pool, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
   }
   // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork,
+                    nv ? nv->w13_gs : nullptr, nv ? nv->w2_gs : nullptr));
   CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
   return LMOE_OK;
 }
@@ -576,6 +583,37 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   CHECK(check_weights(wt));
   CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s));
   return post_call(s, LMOE_OK);
+}
+
+int lmoe_forward_nvfp4(const lmoe_dims* d, const lmoe_weights* wt, const lmoe_nvfp4_scales* nv, const uint16_t* x,
+                       uint16_t* out, void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  if (!x || !out || !aligned16(x) || !aligned16(out) || !nv || !nv->w13_gs || !nv->w2_gs) return LMOE_EINVAL;
+  CHECK(check_weights(wt));
+  CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s, nv));
+  return post_call(s, LMOE_OK);
+}
+
+int lmoe_experts_nvfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
+                       const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const float* w13_gs,
+                       const uint8_t* w2_q, const uint8_t* w2_s, const float* w2_gs, float* y, void* ws,
+                       size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s));
+  const void* ptrs[] = {x_lat, expert_offsets, sorted_rows, w13_q, w13_s, w2_q, w2_s, y};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LMOE_EINVAL;
+  if (!w13_gs || !w2_gs) return LMOE_EINVAL;
+  const int R = d->T * d->top_k;
+  LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
+         group_rows(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
+  return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s, false, false,
+                                  w13_gs, w2_gs));
 }
 
 size_t lmoe_block_workspace_bytes(const lmoe_dims* d) {

@@ -37,6 +37,13 @@
 // 32 K positions in a fixed permutation that the activation fragment follows;
 // the fresh block result is scaled by the block's E8M0 value (expanded once
 // per plane into a per-warp fp32 table) and added to the fp32 accumulator.
+//
+// NVFP4 weights (FMT_NV): one E4M3 scale per 16 elements and an fp32 global
+// scale per expert matrix.  A lane's 8 codes of a 32-element block lie in one
+// 16-element half, and E2M1 x E4M3 is exact in f16 (at most 6 significant
+// bits, magnitudes 2^-10 .. 2688), so each f16x2 pair of codes is multiplied
+// by its block scale before the MMA and the MMAs accumulate the whole item in
+// fp32; the epilogue applies the global scale.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.cuh"
@@ -44,29 +51,34 @@
 namespace lmoe {
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+enum { FMT_MX = 0, FMT_NV = 1 };  // MXFP4 (E8M0 per 32) or NVFP4 (E4M3 per 16 + global)
 
 constexpr int kRows = 32;  // weight rows per item: two m16 tiles
 constexpr int kKC = 2048;  // K elements per chunk when K > 2048 (else the whole K): 16 KB code boxes
 
 // Group header the producer writes next to an activation panel.
 struct PanelHdr {
-  int p0, ntok, pad0, pad1;
+  int p0, ntok, expert, pad1;
   int rows[8];  // per token: sorted_rows[p0 + j] (the original route row id)
 };
 
 // Item header a consumer passes to the epilogue warp with the partials.
 struct ItemHdr {
-  int p0, ntok, tile, pad;
+  int p0, ntok, tile;
+  float gscale;  // NVFP4: the expert matrix's global scale
   int aexp[8];  // per token of the group: power of two mapping its activation row into f16 range
   int rows[8];
 };
 
 // One ring slot: codes and scales of a K chunk of one item.
+template <int FMT>
 struct Layout {
+  static constexpr int kSB = (FMT == FMT_NV) ? 16 : 32;  // elements per scale byte
   static constexpr int kBox = 16 * (kKC / 2);  // one code box: 16 rows x kc/2 bytes (16 KB)
   static constexpr int kCodes = 2 * kBox;      // box A (rows 0-15 of the item), box B (rows 16-31)
-  static constexpr int kScales = kRows * (kKC / 32);
+  static constexpr int kScales = kRows * (kKC / kSB);
   static constexpr int kSlot = (kCodes + kScales + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
+  static constexpr int kTable = (FMT == FMT_NV) ? 512 : 256;  // 4-byte entries of a warp's scale table
 };
 
 constexpr int kMaxSlots = 8;
@@ -150,28 +162,99 @@ __device__ __forceinline__ void plane_blocks(uint32_t sbase, uint32_t act_addr, 
   }
 }
 
+// NVFP4: the 16 E4M3 bytes of one 128-byte plane p (16 blocks of 16, scale
+// region [32 rows][nsb]) as f16 pairs (s, s), in the warp's table
+// [block j][mtile][g][lo,hi].  E4M3 -> f16 is exact (cvt.rn.f16x2.e4m3x2).
+template <int MODE>
+__device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int nsb, int p, uint32_t* table, int lane) {
+  const int r = lane;
+  const int box = r >> 4, rb = r & 15;
+  const int mt = (MODE == MODE_GATEUP) ? (rb >> 3) : box;
+  const int hi = (MODE == MODE_GATEUP) ? box : (rb >> 3);
+  const int g = r & 7;
+  const uint4 v = *reinterpret_cast<const uint4*>(sc + r * nsb + p * 16);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t* dst = table + (mt * 8 + g) * 2 + hi;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      uint32_t f2;  // f16 pair of blocks 4i + 2hw (low half) and 4i + 2hw + 1 (high half)
+      const uint16_t b2 = (uint16_t)(w[i] >> (16 * hw));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"(b2));
+      const int j = 4 * i + 2 * hw;
+      dst[j * 32] = __byte_perm(f2, f2, 0x1010);
+      dst[(j + 1) * 32] = __byte_perm(f2, f2, 0x3232);
+    }
+  }
+}
+
+// NVFP4: the 8 blocks of 32 of plane p.  The lane's codes of a block lie in its
+// 16-element half q / 2; their f16 values times that half's scale are exact, so
+// the MMAs accumulate straight into acc4 (two chains per m-tile, by block parity).
+template <int NV>
+__device__ __forceinline__ void plane_blocks_nv(uint32_t sbase, uint32_t act_addr, const uint32_t* table,
+                                                const uint32_t (&box_off)[2], const int (&row_in_box)[2], int lm,
+                                                int g, int q, float (&acc4)[2][2][4], int p) {
+  const uint2* tab2 = reinterpret_cast<const uint2*>(table) + g;
+  const int rr = row_in_box[0] & 7;
+  const uint32_t pb0 = sbase + box_off[0] + row_in_box[0] * 128 + p * 2048;
+  const uint32_t pb1 = sbase + box_off[1] + row_in_box[1] * 128 + p * 2048;
+  const uint32_t pact = act_addr + p * 512;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t coff = static_cast<uint32_t>(((2 * i + (lm >> 1)) ^ rr) << 4);
+    uint32_t w[2][4];
+    ldmatrix_x4(w[0][0], w[0][1], w[0][2], w[0][3], pb0 + coff);
+    ldmatrix_x4(w[1][0], w[1][1], w[1][2], w[1][3], pb1 + coff);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int blk = 2 * i + half;
+      uint32_t b0, b1, b2, b3;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                   : "r"(pact + blk * 64));
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        uint32_t l[4], h[4];
+        e2m1x8_to_f16x8(w[m][2 * half], l[0], l[1], l[2], l[3]);
+        e2m1x8_to_f16x8(w[m][2 * half + 1], h[0], h[1], h[2], h[3]);
+        const uint2 sc = tab2[((2 * blk + (q >> 1)) * 2 + m) * 8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(l[t]) : "r"(sc.x));
+          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[t]) : "r"(sc.y));
+        }
+        mma_f16(acc4[half][m], l[0], h[0], l[1], h[1], b0, b1);
+        mma_f16(acc4[half][m], l[2], h[2], l[3], h[3], b2, b3);
+      }
+    }
+  }
+}
+
 // Shared-memory plan of one CTA (bytes), shared by the kernel and the launch.
 // NP activation panels: two when one group's rows are small (G = 1), so the
 // next group's rows load while the current group is still being consumed.
-template <int G, int Q>
+template <int G, int Q, int FMT>
 struct Smem {
+  using Lay = Layout<FMT>;
   static constexpr int NP = (G == 1) ? 2 : 1;
   static constexpr int NV = (G == 1) ? 1 : 2;        // token columns per lane that can hold a valid token
   static constexpr int kPart = 2 * 2 * NV * 32;      // floats per warp partial: [mtile][lo/hi][v][lane]
   static __host__ __device__ int panel_row(int K) { return K * 2 + 64; }  // padded: conflict-free 16-byte loads
   static __host__ __device__ int fixed(int K) {
-    return NP * G * panel_row(K) + Q * 256 * 4 + 2 * Q * kPart * 4 + Q * G * 4 + 2 * (int)sizeof(ItemHdr) +
+    return NP * G * panel_row(K) + Q * Lay::kTable * 4 + 2 * Q * kPart * 4 + Q * G * 4 + 2 * (int)sizeof(ItemHdr) +
            NP * (int)sizeof(PanelHdr) + (2 * kMaxSlots + 2 * NP + 6) * 8;
   }
-  static __host__ __device__ int bytes(int K, int D) { return D * Layout::kSlot + fixed(K) + 1024; }
+  static __host__ __device__ int bytes(int K, int D) { return D * Lay::kSlot + fixed(K) + 1024; }
 };
 
-template <int MODE, int G, int Q>
+template <int MODE, int G, int Q, int FMT>
 __global__ void __launch_bounds__(32 * (Q + 2), 1)
     expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                   int D) {
-  using Lay = Layout;
-  using SM = Smem<G, Q>;
+  using Lay = Layout<FMT>;
+  using SM = Smem<G, Q, FMT>;
   constexpr int NP = SM::NP;
   constexpr int NV = SM::NV;
   constexpr int kPart = SM::kPart;
@@ -179,10 +262,11 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   // 1 KB alignment for the swizzled boxes
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int K = a.K, kc = a.kc, nch = K / kc, nb = kc / 32, cbk = kc / 256;  // cbk: 128-byte planes per chunk
+  const int nsb = kc / Lay::kSB;  // scale bytes per row and chunk
   const int prow = SM::panel_row(K);
   uint8_t* panels = smem + D * Lay::kSlot;                                 // [NP][G][prow]: activation rows
-  float* tables = reinterpret_cast<float*>(panels + NP * G * prow);       // [Q][256]: per-warp scale table
-  float* red = tables + Q * 256;                                          // [2][Q][kPart]: partials
+  float* tables = reinterpret_cast<float*>(panels + NP * G * prow);       // [Q][kTable]: per-warp scale table
+  float* red = tables + Q * Lay::kTable;                                  // [2][Q][kPart]: partials
   float* smax = red + 2 * Q * kPart;                                      // [Q][G]: per-warp row maxima
   ItemHdr* ihdr = reinterpret_cast<ItemHdr*>(smax + Q * G);               // [2]
   PanelHdr* phdr = reinterpret_cast<PanelHdr*>(ihdr + 2);                 // [NP]
@@ -196,7 +280,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   uint64_t* rempty = rfull + 2;                                           // [2] partials taken (1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Ks = K / 32;
+  const int Ks = K / Lay::kSB;  // scale bytes per weight row
   const int tiles = (MODE == MODE_GATEUP) ? a.inter / 16 : a.latent / kRows;
   const int rows_per_expert = (MODE == MODE_GATEUP) ? 2 * a.inter : a.latent;
 
@@ -286,16 +370,16 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
         if (good) {
           uint8_t* slot = smem + d * Lay::kSlot;
           uint64_t* bar = &full[d];
-          mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nb);
+          mbar_arrive_expect_tx(bar, kRows * (kc / 2) + kRows * nsb);
           tma_load_3d(slot, &tm_q, 0, rowA, c * cbk, bar, pol);
           tma_load_3d(slot + 16 * (kc / 2), &tm_q, 0, rowB, c * cbk, bar, pol);
           uint8_t* sdst = slot + Lay::kCodes;
           if (nch > 1) {
-            tma_load_2d(sdst, &tm_s, c * nb, rowA, bar, pol);
-            tma_load_2d(sdst + 16 * nb, &tm_s, c * nb, rowB, bar, pol);
+            tma_load_2d(sdst, &tm_s, c * nsb, rowA, bar, pol);
+            tma_load_2d(sdst + 16 * nsb, &tm_s, c * nsb, rowB, bar, pol);
           } else {  // one chunk: the 16 rows' scales are contiguous
             bulk_g2s(sdst, a.s + (size_t)rowA * Ks, 16 * Ks, bar);
-            bulk_g2s(sdst + 16 * nb, a.s + (size_t)rowB * Ks, 16 * Ks, bar);
+            bulk_g2s(sdst + 16 * nsb, a.s + (size_t)rowB * Ks, 16 * Ks, bar);
           }
         }
       }
@@ -355,6 +439,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
           if (lane == 0) {
             h->p0 = p0;
             h->ntok = ntok;
+            h->expert = g4.x;
           }
           if (lane < G) h->rows[lane] = my_row;
           __syncwarp();
@@ -388,6 +473,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       if (!mbar_wait(&rfull[pb], (j >> 1) & 1, a.st, 6)) break;
       const ItemHdr* h = ihdr + pb;
       const int p0 = h->p0, ntok = h->ntok, tile = h->tile;
+      const float gsc = h->gscale;
       int aexp[G], arow_id[G];
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) {
@@ -426,7 +512,8 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
           }
         if (tok < ntok) {
           const int p = p0 + tok;
-          const float inv = ldexpf(1.0f, -e_tok);
+          float inv = ldexpf(1.0f, -e_tok);
+          if (FMT == FMT_NV) inv *= gsc;  // a power of two times the global scale: one rounding
           if (MODE == MODE_GATEUP) {
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
@@ -469,7 +556,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   const int g = lane >> 2, q = lane & 3;
   // ldmatrix.x4 for m-tile m and blocks (b, b+1): matrices (lo rows, b) (hi rows, b) (lo rows, b+1) (hi rows, b+1)
   const int lm = lane >> 3, rr = lane & 7;
-  float* table = tables + warp * 256;
+  float* table = tables + warp * Lay::kTable;
   // per m-tile: byte offset of this lane's ldmatrix box and its row in the box
   uint32_t box_off[2];
   int row_in_box[2];
@@ -490,6 +577,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
   const int units = K / 8;  // 16-byte units per activation row
   int seq = 0, pseq = 0, cur = -1;
   int p0 = 0, ntok = 0;
+  float gscale = 1.f;  // NVFP4: the current group's expert matrix global scale
   uint32_t act_row = 0;  // this lane's activation row (token g) in the current panel
   int aexp[G], arow_id[G];
 #pragma unroll
@@ -507,6 +595,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       uint8_t* panel = panels + pb * G * prow;
       p0 = h->p0;
       ntok = h->ntok;
+      if constexpr (FMT == FMT_NV) gscale = a.gs[h->expert];
 #pragma unroll
       for (int jj = 0; jj < G; ++jj) arow_id[jj] = h->rows[jj];
       for (int r = 0; r < ntok; ++r) {
@@ -567,6 +656,13 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int v = 0; v < NV; ++v) acc[m][h][v] = 0.f;
+    float acc4[2][2][4];  // NVFP4: [block parity][mtile][mma accumulator]
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc4[u][m][i] = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int d = seq % D;
       const uint32_t par = (seq / D) & 1;
@@ -579,14 +675,30 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       const uint32_t sbase = smem_u32(slot);
       const uint32_t act_addr = act_row + c * kc * 2;
       for (int pl = warp; pl < nplanes; pl += Q) {
-        expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
-        __syncwarp();
-        plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
+        if constexpr (FMT == FMT_NV) {
+          uint32_t* tab = reinterpret_cast<uint32_t*>(table);
+          expand_plane_scales_nv<MODE>(slot + Lay::kCodes, nsb, pl, tab, lane);
+          __syncwarp();
+          plane_blocks_nv<NV>(sbase, act_addr, tab, box_off, row_in_box, lm, g, q, acc4, pl);
+        } else {
+          expand_plane_scales<MODE>(slot + Lay::kCodes, nb, pl, table, lane);
+          __syncwarp();
+          plane_blocks<NV>(sbase, act_addr, table, box_off, row_in_box, lm, g, acc, pl);
+        }
         __syncwarp();
       }
       if (lane == 0) mbar_arrive(&empty[d]);
     }
     if (!alive) break;
+    if constexpr (FMT == FMT_NV) {
+      // m16n8 accumulator: d0, d1 row g, columns 2q, 2q+1; d2, d3 row g + 8
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int v = 0; v < NV; ++v) acc[m][h][v] = acc4[0][m][2 * h + v] + acc4[1][m][2 * h + v];
+    }
     const bool last_of_group = (j + 1 == nloc) || ((it + 1) / tiles != grp);
     if (last_of_group) {
       // panel reads (and this warp's conversion writes) come before the next bulk copy into it
@@ -610,6 +722,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
         h->p0 = p0;
         h->ntok = ntok;
         h->tile = tile;
+        h->gscale = gscale;
       }
       if (lane < G) {
 #pragma unroll
@@ -630,14 +743,16 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
 // ---------------------------------------------------------------------------
 int expert_max_group(int T) { return T <= 1 ? 1 : 8; }
 
-template <int MODE, int G, int Q>
+template <int MODE, int G, int Q, int FMT>
 static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
-  using SM = Smem<G, Q>;
-  auto kern = expert_kernel<MODE, G, Q>;
+  using SM = Smem<G, Q, FMT>;
+  using Lay = Layout<FMT>;
+  auto kern = expert_kernel<MODE, G, Q, FMT>;
+  if (FMT == FMT_NV && !a.gs) return LMOE_EINVAL;
   constexpr int kSmemMax = 232448;
   if (a.K > kMaxK) return LMOE_EUNSUPPORTED;
   // as many ring slots as fit next to the panel (at least 2)
-  const int D = min(kMaxSlots, (kSmemMax - SM::fixed(a.K) - 1024) / Layout::kSlot);
+  const int D = min(kMaxSlots, (kSmemMax - SM::fixed(a.K) - 1024) / Lay::kSlot);
   if (D < 2) return LMOE_EUNSUPPORTED;
   const int smem = SM::bytes(a.K, D);
   static int attr_done[64] = {};  // per device: largest dynamic shared memory size set so far
@@ -662,9 +777,10 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
       return LMOE_ECUDA;
   }
   if (a.K > kKC) {
-    const uint64_t dims[2] = {(uint64_t)a.K / 32, rows_total};
-    const uint64_t strides[1] = {(uint64_t)a.K / 32};
-    const uint32_t box[2] = {(uint32_t)(a.kc / 32), 16};
+    // scales as {K/SB bytes, rows}: SB = 32 (E8M0) or 16 (E4M3) elements per byte
+    const uint64_t dims[2] = {(uint64_t)a.K / Lay::kSB, rows_total};
+    const uint64_t strides[1] = {(uint64_t)a.K / Lay::kSB};
+    const uint32_t box[2] = {(uint32_t)(a.kc / Lay::kSB), 16};
     if (get_tmap(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return LMOE_ECUDA;
   } else {
@@ -684,13 +800,21 @@ static int launch_one(ExpertArgs a, cudaStream_t s, int num_sms) {
 }
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 8>(a, s, num_sms);
-  return launch_one<MODE_GATEUP, 8, 8>(a, s, num_sms);
+  if (a.gs) {
+    if (max_group == 1) return launch_one<MODE_GATEUP, 1, 8, FMT_NV>(a, s, num_sms);
+    return launch_one<MODE_GATEUP, 8, 8, FMT_NV>(a, s, num_sms);
+  }
+  if (max_group == 1) return launch_one<MODE_GATEUP, 1, 8, FMT_MX>(a, s, num_sms);
+  return launch_one<MODE_GATEUP, 8, 8, FMT_MX>(a, s, num_sms);
 }
 
 int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms) {
-  if (max_group == 1) return launch_one<MODE_DOWN, 1, 8>(a, s, num_sms);
-  return launch_one<MODE_DOWN, 8, 8>(a, s, num_sms);
+  if (a.gs) {
+    if (max_group == 1) return launch_one<MODE_DOWN, 1, 8, FMT_NV>(a, s, num_sms);
+    return launch_one<MODE_DOWN, 8, 8, FMT_NV>(a, s, num_sms);
+  }
+  if (max_group == 1) return launch_one<MODE_DOWN, 1, 8, FMT_MX>(a, s, num_sms);
+  return launch_one<MODE_DOWN, 8, 8, FMT_MX>(a, s, num_sms);
 }
 
 }  // namespace lmoe

@@ -37,7 +37,8 @@ __global__ void table_kernel(const int32_t* topk_idx, int R, int E, int G, int32
 // int4 {e, p0, n, 0}.
 struct ExpertArgs {
   const uint8_t* q;         // codes [E][rows_per_expert][K/2]
-  const uint8_t* s;         // scales [E][rows_per_expert][K/32]
+  const uint8_t* s;         // scales [E][rows_per_expert][K/32] E8M0, or [K/16] E4M3 when gs is set
+  const float* gs;          // NVFP4: fp32 global scale per expert matrix [E]; null for MXFP4
   const uint16_t* act;      // bf16 activations, row-major [*][K] (x_lat by token, or h by sorted position)
   const int4* groups;       // group list
   const int32_t* n_groups;  // device count of groups
@@ -103,7 +104,8 @@ constexpr int kTcGemmN = 256, kTcGemmK = 64;
 // Grouped W4A16 expert GEMMs on tcgen05 (groups of up to 256 sorted rows).
 struct TcExpertArgs {
   const uint8_t* q;         // codes [E][rows_per_expert][K/2]
-  const uint8_t* s;         // scales [E][rows_per_expert][K/32]
+  const uint8_t* s;         // scales [E][rows_per_expert][K/32] E8M0, or [K/16] E4M3 when gs is set
+  const float* gs;          // NVFP4: fp32 global scale per expert matrix [E]; null for MXFP4
   const int4* groups;       // {e, p0, n <= 256, 0}
   const int32_t* n_groups;
   const int32_t* sorted_rows;  // down: original row id of each sorted position

@@ -26,6 +26,11 @@
 //   warps 11-18 epilogue: tcgen05.ld, SwiGLU -> h (gate/up), or y and the
 //               per-32-column sums of squares for post_expert_norm (down);
 //               two warps per TMEM lane quarter take alternate 32-column chunks
+// NVFP4 weights (FMT = 1): E4M3 scales per 16 elements and an fp32 global
+// scale per expert matrix.  E2M1 x E4M3 has at most 6 significant bits and is
+// exact in bf16 for every scale byte, so the dequantiser builds each 16-block's
+// eight scaled patterns with fp32 products; the epilogue applies the global
+// scale to the accumulators.
 // Tensor memory (512 columns): accumulators of 160 columns (gate/up: gate at
 // 0, up at 160, so SwiGLU pairs are lane-local; down: the item's two 128-row
 // output tiles at 0 and 160, or with one tile per item two buffers), and from
@@ -125,6 +130,27 @@ __device__ __forceinline__ void dq8(uint32_t w, const DqTable& t, uint32_t* o) {
   o[3] = __byte_perm(lo, hi, 0x7362);
 }
 
+// NVFP4: the eight patterns of one 16-element block under E4M3 scale byte s,
+// as products in fp32 (exact, with at most 6 significant bits, so the bf16
+// pattern is the top half).  E4M3 -> f16 -> f32 is exact.
+__device__ __forceinline__ DqTable dq_table_nv(uint32_t s) {
+  uint32_t f2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"((uint16_t)s));
+  const float sc = __half2float(__ushort_as_half((unsigned short)(f2 & 0xffffu)));
+  const float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  uint32_t pat[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pat[i] = __float_as_uint(__fmul_rn(mags[i], sc)) >> 16;
+  const uint32_t p01 = pat[0] | (pat[1] << 16), p23 = pat[2] | (pat[3] << 16);
+  const uint32_t p45 = pat[4] | (pat[5] << 16), p67 = pat[6] | (pat[7] << 16);
+  DqTable t;
+  t.la = __byte_perm(p01, p23, 0x6420);
+  t.ha = __byte_perm(p01, p23, 0x7531);
+  t.lb = __byte_perm(p45, p67, 0x6420);
+  t.hb = __byte_perm(p45, p67, 0x7531);
+  return t;
+}
+
 // Scales outside the exponent-add range (subnormal, overflowing or NaN
 // results): the value in fp32, then bf16 (exact: every finite product is
 // representable in bf16).
@@ -185,7 +211,7 @@ __device__ __forceinline__ bool x_item(const TcExpertArgs& a, int4 g, int it, in
   return true;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kXThreads, 1)
     tc_expert_kernel(const TcExpertArgs a, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_act) {
@@ -394,11 +420,22 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (!x_item(a, g_cur, it, nft, &x)) continue;
       const size_t grow = (size_t)x.e * rows_pe +
                           (MODE == 0 ? (size_t)m * a.inter + (size_t)x.ft * kXM : (size_t)(x.ft * TPI + m) * kXM) + rr;
-      const uint8_t* srow = a.s + grow * (size_t)(K / 32);
-      uint2 sc_next = __ldg(reinterpret_cast<const uint2*>(srow));
+      constexpr int kSB = FMT == 1 ? 16 : 32;  // elements per scale byte
+      const uint8_t* srow = a.s + grow * (size_t)(K / kSB);
+      // a stage's scale bytes: 8 E8M0 or 16 E4M3 (in .x, .y or all four words)
+      auto load_sc = [&](int kr) -> uint4 {
+        if constexpr (FMT == 1) {
+          return __ldg(reinterpret_cast<const uint4*>(srow + kr * 16));
+        } else {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(srow + kr * 8));
+          return make_uint4(v.x, v.y, 0u, 0u);
+        }
+      };
+      uint4 sc_next = load_sc(0);  // loaded one stage ahead
       for (int kr = 0; kr < nkr && ok; ++kr) {
-        const uint2 sc8 = sc_next;  // this stage's 8 scale bytes, loaded one stage ahead
-        if (kr + 1 < nkr) sc_next = __ldg(reinterpret_cast<const uint2*>(srow + (kr + 1) * 8));
+        const uint4 sc16 = sc_next;
+        const uint2 sc8 = make_uint2(sc16.x, sc16.y);
+        if (kr + 1 < nkr) sc_next = load_sc(kr + 1);
         // all eight in the exponent-add range [2, 252]: bytewise (s - 2) <= 250
         const bool fast = (__vcmpleu4(__vsub4(sc8.x, 0x02020202u), 0xFAFAFAFAu) &
                            __vcmpleu4(__vsub4(sc8.y, 0x02020202u), 0xFAFAFAFAu)) == 0xFFFFFFFFu;
@@ -415,9 +452,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
             const int b = C::NMAT == 2 ? bi : b_only;
             const int kb = 2 * j + b;  // 32-block within the raw stage
             const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
-            const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
-            const uint32_t sb = (sword >> (8 * (kb & 3))) & 0xFFu;
-            dq_block(c, sb, o + 16 * bi, fast || (sb >= 2u && sb <= 252u));
+            if constexpr (FMT == 1) {
+              // 16-blocks 2 kb (codes in c.x, c.y) and 2 kb + 1 (c.z, c.w)
+              const uint32_t sword = (kb < 2) ? sc16.x : (kb < 4) ? sc16.y : (kb < 6) ? sc16.z : sc16.w;
+              const uint32_t sh = 16 * (kb & 1);
+              const DqTable t0 = dq_table_nv((sword >> sh) & 0xFFu), t1 = dq_table_nv((sword >> (sh + 8)) & 0xFFu);
+              dq8(c.x, t0, o + 16 * bi);
+              dq8(c.y, t0, o + 16 * bi + 4);
+              dq8(c.z, t1, o + 16 * bi + 8);
+              dq8(c.w, t1, o + 16 * bi + 12);
+            } else {
+              const uint32_t sword = kb < 4 ? sc8.x : sc8.y;
+              const uint32_t sb = (sword >> (8 * (kb & 3))) & 0xFFu;
+              dq_block(c, sb, o + 16 * bi, fast || (sb >= 2u && sb <= 252u));
+            }
           }
           if (pend_as >= 0) {
             tmem_st_wait();
@@ -470,6 +518,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (!x_item(a, g_cur, it, nft, &x)) continue;
       if (!mbar_wait_sleep(&acc_full[acc], cph, a.st, 72, 256)) break;
       tc_fence_after();
+      const float gsc = FMT == 1 ? __ldg(a.gs + x.e) : 1.0f;  // NVFP4 global scale of this expert matrix
       for (int m = 0; m < TPI; ++m) {
       const int f = (x.ft * TPI + m) * kXM + q * 32 + lane;  // output feature of this lane
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 1 ? (uint32_t)acc * kXAcc : (uint32_t)m * kXAcc);
@@ -485,7 +534,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (c0 + i < x.n) {
-              const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+              float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+              if (FMT == 1) {
+                gv *= gsc;
+                uv *= gsc;
+              }
               hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv * __frcp_rn(1.0f + __expf(-gv)) * uv);
             }
           }
@@ -497,6 +550,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int rid = __shfl_sync(0xffffffffu, my_row, i);
+            if (FMT == 1) v[i] = __float_as_uint(__uint_as_float(v[i]) * gsc);
             if (c0 + i < x.n) a.y_out[(size_t)rid * a.latent + f] = __uint_as_float(v[i]);
           }
           // sum of squares over this warp's 32 features for each of the 32 columns:
@@ -536,7 +590,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   }
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 int launch_tc_expert(const TcExpertArgs& a, const uint16_t* act, cudaStream_t s, int num_sms) {
   const int K = a.K;
   if (K % 256 || a.inter % kXM || a.latent % (MODE == 2 ? 2 * kXM : kXM)) return LMOE_EUNSUPPORTED;
@@ -545,7 +599,7 @@ int launch_tc_expert(const TcExpertArgs& a, const uint16_t* act, cudaStream_t s,
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ECUDA;
   if (!(attr_done.load() >> (dev & 63) & 1ull)) {
-    if (cudaFuncSetAttribute(tc_expert_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(tc_expert_kernel<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return LMOE_ECUDA;
     attr_done.fetch_or(1ull << (dev & 63));
@@ -576,17 +630,22 @@ int launch_tc_expert(const TcExpertArgs& a, const uint16_t* act, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_expert_kernel<MODE>, a, tq, ta) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+  return cudaLaunchKernelEx(&cfg, tc_expert_kernel<MODE, FMT>, a, tq, ta) == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
 int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream_t s, int num_sms) {
-  return launch_tc_expert<0>(a, x_sorted, s, num_sms);
+  if (a.gs) return launch_tc_expert<0, 1>(a, x_sorted, s, num_sms);
+  return launch_tc_expert<0, 0>(a, x_sorted, s, num_sms);
 }
 
 int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms) {
   // two output tiles per item halve the activation traffic per MMA
-  if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2>(a, h, s, num_sms);
-  return launch_tc_expert<1>(a, h, s, num_sms);
+  if (a.gs) {
+    if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2, 1>(a, h, s, num_sms);
+    return launch_tc_expert<1, 1>(a, h, s, num_sms);
+  }
+  if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2, 0>(a, h, s, num_sms);
+  return launch_tc_expert<1, 0>(a, h, s, num_sms);
 }
 
 // x_sorted[p] = x_lat[sorted_rows[p] / k]: one warp per sorted row, 16-byte copies.

@@ -122,3 +122,33 @@ def test_block_zero_post_gain_is_identity(lm):
     y = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
     run_block(lm, d, w, {k: to_dev(v) for k, v in nw.items()}, to_dev(x), y)
     assert np.array_equal(to_host(y), x)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 37), ("decode_t1", None)])
+def test_block_replays_from_a_cuda_graph(lm, name, T):
+    """The block (pre-norm, layer, post-norm and residual, with the side stream for
+    many tokens) captured in a CUDA graph replays bit for bit."""
+    d = cfg(name, T)
+    w = device_weights(d)
+    nw_dev = {k: to_dev(v) for k, v in synth.make_block_norms(d).items()}
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    ws = torch.empty(lm.lmoe_block_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    wts, norms = lm.weights_of(w), lm.norms_of(nw_dev, d.eps)
+    x = to_dev(synth.make_x(d))
+    ref = torch.empty_like(x)
+    lm.lmoe_block_forward(dims, wts, norms, x, ref, ws)
+    y = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lm.lmoe_block_forward(dims, wts, norms, x, y, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lm.lmoe_block_forward(dims, wts, norms, x, y, ws)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lm.lmoe_status_check(ws) == 0
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))

@@ -17,8 +17,10 @@ pytestmark = pytest.mark.gpu
 
 # tiny shapes (K = 256: one chunk, scales by bulk copy), full shape (K = 4096: two
 # chunks, scales by tensor copy); T = 600 runs the grouped tensor-core experts
-STAGE_CASES = [("tiny", 1), ("tiny", 4), ("tiny", 37), ("tiny", 600), ("decode_t1", None), ("verify_t8", None)]
-FORWARD_CASES = [("tiny", 4), ("tiny", 37), ("tiny", 600), ("decode_t1", None)]
+STAGE_CASES = [("tiny", 1), ("tiny", 4), ("tiny", 37), ("tiny", 600), ("decode_t1", None), ("verify_t8", None),
+               ("batched_t64", None)]
+FORWARD_CASES = [("tiny", 4), ("tiny", 37), ("tiny", 600), ("decode_t1", None), ("verify_t8", None),
+                 ("batched_t64", None)]
 
 _W = {}
 
@@ -121,3 +123,30 @@ def test_nvfp4_scales_differ_from_mxfp4(lm):
     lm.lmoe_forward(dims, lm.weights_of(w), x, b, ws)  # the first half of each scale row read as E8M0
     assert lm.lmoe_status_check(ws) == 0
     assert not torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 600), ("decode_t1", None)])
+def test_nvfp4_forward_replays_from_a_cuda_graph(lm, name, T):
+    d = cfg(name, T)
+    _, w = nv_weights(d)
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    ws = ws_for(lm, dims)
+    wts, nv = lm.weights_of(w), lm.nvfp4_of(w)
+    x = to_dev(synth.make_x(d))
+    ref = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
+    lm.lmoe_forward_nvfp4(dims, wts, nv, x, ref, ws)
+    out = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lm.lmoe_forward_nvfp4(dims, wts, nv, x, out, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lm.lmoe_forward_nvfp4(dims, wts, nv, x, out, ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lm.lmoe_status_check(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

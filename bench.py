@@ -175,15 +175,23 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
+    """One process per GPU (torchrun): rank, world and local rank from the
+    environment.  The ranks are independent replicas; the process group only
+    carries the barrier and the max over ranks of the timed region (nccl on
+    GPUs; gloo for the host-side tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or os.environ.get("LMOE_DIST_BACKEND", "nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -198,9 +206,16 @@ def allreduce_max(world, v: float) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, units_per_rank: float, seconds: float):
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    total = allreduce_max(world, seconds)
+    return units_per_rank * world / total, total
 
 
 def cpu_oracle_rate(d, hw, x, min_seconds=10.0, max_reps=1000, block_norms=None, nvfp4=False):
@@ -473,7 +488,9 @@ def main():
             clk.__exit__(None, None, None)
         barrier(world)
         step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
-        total_s = allreduce_max(world, sum(step_ms) / 1e3)
+        # a step of n_layers layers moves each of its T tokens through n_layers layers:
+        # the metric counts token-layers, so one- and many-layer steps compare directly
+        value, total_s = job_throughput(world, d.T * n_layers * args.steps, sum(step_ms) / 1e3)
         clocks = clk.summary()
 
         # ---- end to end: host input upload and output download inside the timed region ----
@@ -492,7 +509,8 @@ def main():
             e1[i].record()
         torch.cuda.synchronize()
         barrier(world)
-        e2e_s = allreduce_max(world, sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / 1e3)
+        e2e_value, e2e_s = job_throughput(world, d.T * n_layers * args.steps,
+                                          sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / 1e3)
 
         # ---- dominant kernel, per-launch events ----
         nev = launches_per_step + 1
@@ -513,10 +531,6 @@ def main():
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
 
     pk = peaks()
-    # a step of n_layers layers moves each of its T tokens through n_layers layers:
-    # the metric counts token-layers, so one- and many-layer steps compare directly
-    tokens = d.T * n_layers * args.steps * world
-    value = tokens / total_s
     layer_bytes = touched * EXPERT_BYTES + PROJ_BYTES
     # every layer of a step streams about the same bytes (its own touched experts)
     layer_gbs = layer_bytes * n_layers * args.steps / total_s / 1e9
@@ -563,7 +577,9 @@ def main():
         "layer_bytes_per_step": layer_bytes,
         "roofline": roof,
         "kernels_ms": kern_ms,
-        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
+        "step_ms_percentiles": {"p10": float(np.percentile(step_ms, 10)), "median": float(np.median(step_ms)),
+                                "p90": float(np.percentile(step_ms, 90))},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
                 "d2h_bytes_per_step": d.T * d.H * 2},
         "gpu_launches": launches_per_step * n_layers * args.steps,
         "clocks": clocks,

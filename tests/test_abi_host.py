@@ -104,3 +104,15 @@ def test_regime_options_round_trip(lm):
 def test_launch_names_out_of_range(lm):
     assert lm.lmoe_last_launch_name(-1) is None
     assert lm.lmoe_last_launch_name(1 << 20) is None
+
+
+def test_missing_library_fails_loudly(lm, tmp_path):
+    """No CPU fallback: without the built library every entry point refuses to run."""
+    import latent_moe_layer_fp32_gb300 as pkg
+    saved = pkg._lib
+    pkg._lib = None
+    try:
+        with pytest.raises(ImportError):
+            pkg.load(str(tmp_path / "liblmoe.so"))
+    finally:
+        pkg._lib = saved

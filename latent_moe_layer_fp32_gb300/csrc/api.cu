@@ -277,10 +277,13 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
     uint16_t* w3 = at<uint16_t>(ws, w.wr3);
     const int dup = usplit ? 2 : 1;
     LAUNCH(dim3((H + 1023) / 1024, E), dim3(256), s, router_split_kernel, router_w, E, H, w3, dup);
+    // split-K: enough CTAs for the GPU, and at least 4 splits whatever T, so no fp32
+    // accumulation chain runs longer than a quarter of K (the logits' rounding error
+    // grows with the chain; the top-k weights follow it)
     const int kblocks = 3 * dup * H / 64, tiles_m = (T + 127) / 128;
     nsplit = 1;
     for (int c = 16; c >= 2; --c)
-      if (kblocks % c == 0 && tiles_m * c <= di.sms) {
+      if (kblocks % c == 0 && (tiles_m * c <= di.sms || c <= 4)) {
         nsplit = c;
         break;
       }

@@ -78,7 +78,7 @@ struct Layout {
   static constexpr int kCodes = 2 * kBox;      // box A (rows 0-15 of the item), box B (rows 16-31)
   static constexpr int kScales = kRows * (kKC / kSB);
   static constexpr int kSlot = (kCodes + kScales + 1023) / 1024 * 1024;  // 1 KB aligned (swizzle atom)
-  static constexpr int kTable = (FMT == FMT_NV) ? 512 : 256;  // 4-byte entries of a warp's scale table
+  static constexpr int kTable = 256;  // 4-byte words of a warp's scale table (fp32 E8M0 / f16 E4M3 values)
 };
 
 constexpr int kMaxSlots = 8;
@@ -163,10 +163,11 @@ __device__ __forceinline__ void plane_blocks(uint32_t sbase, uint32_t act_addr, 
 }
 
 // NVFP4: the 16 E4M3 bytes of one 128-byte plane p (16 blocks of 16, scale
-// region [32 rows][nsb]) as f16 pairs (s, s), in the warp's table
-// [block j][mtile][g][lo,hi].  E4M3 -> f16 is exact (cvt.rn.f16x2.e4m3x2).
+// region [32 rows][nsb]) as f16 values in the warp's table [block j][mtile][g][lo,hi]
+// (so one 32-bit word holds a row pair's two scales).  E4M3 -> f16 is exact
+// (cvt.rn.f16x2.e4m3x2).
 template <int MODE>
-__device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int nsb, int p, uint32_t* table, int lane) {
+__device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int nsb, int p, uint16_t* table, int lane) {
   const int r = lane;
   const int box = r >> 4, rb = r & 15;
   const int mt = (MODE == MODE_GATEUP) ? (rb >> 3) : box;
@@ -174,7 +175,7 @@ __device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int ns
   const int g = r & 7;
   const uint4 v = *reinterpret_cast<const uint4*>(sc + r * nsb + p * 16);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t* dst = table + (mt * 8 + g) * 2 + hi;
+  uint16_t* dst = table + (mt * 8 + g) * 2 + hi;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -183,8 +184,8 @@ __device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int ns
       const uint16_t b2 = (uint16_t)(w[i] >> (16 * hw));
       asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"(b2));
       const int j = 4 * i + 2 * hw;
-      dst[j * 32] = __byte_perm(f2, f2, 0x1010);
-      dst[(j + 1) * 32] = __byte_perm(f2, f2, 0x3232);
+      dst[j * 32] = (uint16_t)(f2 & 0xffffu);
+      dst[(j + 1) * 32] = (uint16_t)(f2 >> 16);
     }
   }
 }
@@ -193,10 +194,10 @@ __device__ __forceinline__ void expand_plane_scales_nv(const uint8_t* sc, int ns
 // 16-element half q / 2; their f16 values times that half's scale are exact, so
 // the MMAs accumulate straight into acc4 (two chains per m-tile, by block parity).
 template <int NV>
-__device__ __forceinline__ void plane_blocks_nv(uint32_t sbase, uint32_t act_addr, const uint32_t* table,
+__device__ __forceinline__ void plane_blocks_nv(uint32_t sbase, uint32_t act_addr, const uint16_t* table,
                                                 const uint32_t (&box_off)[2], const int (&row_in_box)[2], int lm,
                                                 int g, int q, float (&acc4)[2][2][4], int p) {
-  const uint2* tab2 = reinterpret_cast<const uint2*>(table) + g;
+  const uint32_t* tab1 = reinterpret_cast<const uint32_t*>(table) + g;  // (lo, hi) f16 pair per word
   const int rr = row_in_box[0] & 7;
   const uint32_t pb0 = sbase + box_off[0] + row_in_box[0] * 128 + p * 2048;
   const uint32_t pb1 = sbase + box_off[1] + row_in_box[1] * 128 + p * 2048;
@@ -219,11 +220,12 @@ __device__ __forceinline__ void plane_blocks_nv(uint32_t sbase, uint32_t act_add
         uint32_t l[4], h[4];
         e2m1x8_to_f16x8(w[m][2 * half], l[0], l[1], l[2], l[3]);
         e2m1x8_to_f16x8(w[m][2 * half + 1], h[0], h[1], h[2], h[3]);
-        const uint2 sc = tab2[((2 * blk + (q >> 1)) * 2 + m) * 8];
+        const uint32_t sp = tab1[((2 * blk + (q >> 1)) * 2 + m) * 8];
+        const uint32_t slo = __byte_perm(sp, sp, 0x1010), shi = __byte_perm(sp, sp, 0x3232);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(l[t]) : "r"(sc.x));
-          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[t]) : "r"(sc.y));
+          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(l[t]) : "r"(slo));
+          asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[t]) : "r"(shi));
         }
         mma_f16(acc4[half][m], l[0], h[0], l[1], h[1], b0, b1);
         mma_f16(acc4[half][m], l[2], h[2], l[3], h[3], b2, b3);
@@ -676,7 +678,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
       const uint32_t act_addr = act_row + c * kc * 2;
       for (int pl = warp; pl < nplanes; pl += Q) {
         if constexpr (FMT == FMT_NV) {
-          uint32_t* tab = reinterpret_cast<uint32_t*>(table);
+          uint16_t* tab = reinterpret_cast<uint16_t*>(table);
           expand_plane_scales_nv<MODE>(slot + Lay::kCodes, nsb, pl, tab, lane);
           __syncwarp();
           plane_blocks_nv<NV>(sbase, act_addr, tab, box_off, row_in_box, lm, g, q, acc4, pl);

@@ -307,6 +307,15 @@ LMOE_API int lmoe_profile_events(void* const* events, int n);
 enum { LMOE_OPT_DENSE_MIN_TOKENS = 1, LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2 };
 LMOE_API int lmoe_set_option(int key, int value);
 
+/* Failure-detection self-check: enqueues one kernel whose single thread waits
+ * on a barrier that nothing completes, bounded by limit_us microseconds
+ * (1 .. 1e6) and an iteration cap, as every device-side wait of the library
+ * is; when the wait runs out it records LMOE_ETIMEOUT in the status word of
+ * `ws` (which it zeroes first) and returns.  lmoe_status_check(ws) then reports
+ * LMOE_ETIMEOUT, and the context stays usable.  ws: device memory of at least
+ * 8 bytes, 256-byte aligned. */
+LMOE_API int lmoe_selftest_timeout(void* ws, size_t ws_bytes, unsigned limit_us, lmoe_stream_t stream);
+
 /* Format self-check: converts every byte value b (two E2M1 codes, low nibble
  * first) with the same in-register conversion the expert kernels use and
  * writes the two values as fp32 to out[2*b], out[2*b+1] (device pointer,

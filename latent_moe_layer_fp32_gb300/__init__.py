@@ -22,7 +22,8 @@ __all__ = [
     "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_block_workspace_bytes",
     "lmoe_block_forward", "norms_of", "lmoe_experts_nvfp4", "lmoe_forward_nvfp4", "nvfp4_of",
     "lmoe_status_check", "lmoe_error_string",
-    "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_profile_events", "dims_of", "weights_of",
+    "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_selftest_timeout", "lmoe_profile_events", "dims_of",
+    "weights_of",
 ]
 
 LMOE_OK, LMOE_EINVAL, LMOE_EUNSUPPORTED, LMOE_ECUDA, LMOE_ETIMEOUT, LMOE_EDEVICE_CHECK, LMOE_EWORKSPACE = \
@@ -95,6 +96,8 @@ def load(path: str | None = None):
     lib.lmoe_error_string.restype = ctypes.c_char_p
     lib.lmoe_last_launch_count.argtypes = []
     lib.lmoe_selftest_e2m1.argtypes = [vp]
+    lib.lmoe_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
+    lib.lmoe_selftest_timeout.restype = i32
     lib.lmoe_selftest_dequant_bf16.argtypes = [vp, vp, i32, vp]
     lib.lmoe_profile_events.argtypes = [vp, i32]
     lib.lmoe_route_noalloc.argtypes = [dp] + [vp] * 8 + [vp]
@@ -303,6 +306,13 @@ def lmoe_profile_events(events):
     torch.cuda.synchronize()
     _event_array = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(load().lmoe_profile_events(_event_array, len(events)), "lmoe_profile_events")
+
+
+def lmoe_selftest_timeout(ws, limit_us=10000, stream=None):
+    """Enqueue a wait that nothing completes, bounded by limit_us; the status word of
+    ws then reads LMOE_ETIMEOUT (lmoe_status_check)."""
+    _check(load().lmoe_selftest_timeout(_ptr(ws), ws.numel() * ws.element_size(), int(limit_us), _stream(stream)),
+           "lmoe_selftest_timeout")
 
 
 def lmoe_selftest_e2m1(out):

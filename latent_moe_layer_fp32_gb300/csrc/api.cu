@@ -752,6 +752,19 @@ int lmoe_selftest_dequant_bf16(const uint8_t* codes, const uint8_t* scales, int 
   return cudaDeviceSynchronize() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 
+int lmoe_selftest_timeout(void* ws, size_t ws_bytes, unsigned limit_us, lmoe_stream_t stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < sizeof(Status) || limit_us == 0 ||
+      limit_us > 1000000u)
+    return LMOE_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  g_launches = 0;
+  if (cudaMemsetAsync(ws, 0, sizeof(Status), s) != cudaSuccess) return LMOE_ECUDA;
+  pre_launch(s, "timeout_selftest_kernel");
+  timeout_selftest_kernel<<<1, 32, 0, s>>>(static_cast<Status*>(ws), (unsigned long long)limit_us * 1000ull);
+  ++g_launches;
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+}
+
 int lmoe_selftest_e2m1(float* out) {
   if (!out || !aligned16(out)) return LMOE_EINVAL;
   DevInfo di;

@@ -125,4 +125,22 @@ __global__ void e2m1_selftest_kernel(float* out) {
   out[2 * b + 1] = __high2float(v);
 }
 
+// Failure-detection self-test: one thread waits on a shared-memory mbarrier
+// that nothing ever completes, with the library's bounded-wait pattern but a
+// limit of limit_ns (and an iteration cap, so the kernel ends even if the
+// timer stalled), then records LMOE_ETIMEOUT in the status word and returns.
+// The context stays usable: nothing faults, nothing is left in flight.
+__global__ void __launch_bounds__(32) timeout_selftest_kernel(Status* st, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_test_wait(&bar, 0)) return;  // never: no thread arrives
+    if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) break;
+  }
+  set_error(st, LMOE_ETIMEOUT, 99);
+}
+
 }  // namespace lmoe

@@ -31,6 +31,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -130,7 +131,9 @@ class Clocks:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples (the JSON line carries their summary); LMOE_CLOCKS_DIR keeps them somewhere chosen
+        self.path = os.path.join(os.environ.get("LMOE_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"lmoe_clocks_rank{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

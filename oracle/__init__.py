@@ -77,6 +77,9 @@ class Oracle:
         L.oracle_nvfp4_value.restype = ctypes.c_float
         L.oracle_experts_nvfp4.argtypes = [dp] + [vp] * 11
         L.oracle_experts_nvfp4.restype = None
+        L.oracle_set_acc64.argtypes = [ctypes.c_int]
+        L.oracle_set_acc64.restype = None
+        L.oracle_get_acc64.restype = ctypes.c_int
         for f in ("oracle_router_logits", "oracle_topk", "oracle_table", "oracle_pool", "oracle_experts",
                   "oracle_norm_combine", "oracle_unpool", "oracle_forward", "oracle_set_threads",
                   "oracle_router_logits_f32", "oracle_rmsnorm_rows", "oracle_bf16_round", "oracle_residual_add"):
@@ -89,6 +92,32 @@ class Oracle:
     @property
     def threads(self) -> int:
         return self.lib.oracle_get_threads()
+
+    def set_acc64(self, on: bool):
+        """Sums in fp64 instead of fp32 (rounded at the same points): a diagnostic of
+        the oracle's own accumulation error, never the reference result."""
+        self.lib.oracle_set_acc64(1 if on else 0)
+
+    def error_report(self, d, x, w) -> dict:
+        """The oracle's own fp32 accumulation error: normwise relative difference of
+        each stage's result between fp32 sums and fp64 sums, on the same input."""
+        a = self.forward(d, x, w)
+        self.set_acc64(True)
+        try:
+            b = self.forward(d, x, w)
+        finally:
+            self.set_acc64(False)
+
+        out = {}
+        for key in ("x_lat", "y", "z", "out"):
+            u, v = a[key], b[key]
+            if u.dtype == np.uint16:
+                u = (u.astype(np.uint32) << 16).view(np.float32)
+                v = (v.astype(np.uint32) << 16).view(np.float32)
+            u, v = u.astype(np.float64), v.astype(np.float64)
+            out[key] = float(np.linalg.norm(u - v) / (np.linalg.norm(v) + 1e-300))
+        out["topk_idx_same"] = bool(np.array_equal(a["topk_idx"], b["topk_idx"]))
+        return out
 
     @staticmethod
     def dims(d, T: int | None = None) -> OrDims:

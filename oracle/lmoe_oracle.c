@@ -40,6 +40,9 @@
  *
  * Sums run sequentially in index order in fp32 (compiled with
  * -ffp-contract=off), so a result does not depend on the thread count.
+ * oracle_set_acc64(1) switches every such sum (projections, experts, norms,
+ * the weighted sum) to fp64, rounded where the fp32 sum is: the difference
+ * between the two runs is the oracle's own fp32 accumulation error.
  *
  * LMOE_ORACLE_PLANT (tests only): building with -DLMOE_ORACLE_PLANT=n plants
  * one plausible mistake so the pin tests can show that they catch it.  The
@@ -195,6 +198,10 @@ static inline float nv_elem(const uint8_t* q, const uint8_t* sc, int64_t n, int6
 
 static int g_threads = 1;
 void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : (n > 256 ? 256 : n); }
+
+static int g_acc64 = 0; /* 1: sums in fp64 (diagnostic), rounded at the same points */
+void oracle_set_acc64(int on) { g_acc64 = on ? 1 : 0; }
+int oracle_get_acc64(void) { return g_acc64; }
 int oracle_get_threads(void) { return g_threads; }
 
 typedef void (*body_fn)(void* ctx, int64_t i);
@@ -375,7 +382,13 @@ static void pool_body(void* p, int64_t i) {
   pool_ctx* c = (pool_ctx*)p;
   int64_t t = i / c->d->L, l = i % c->d->L, H = c->d->H;
   float acc = 0.0f;
-  for (int64_t h = 0; h < H; ++h) acc += bf16_val(c->x[t * H + h]) * bf16_val(c->P[l * H + h]);
+  if (g_acc64) {
+    double a = 0.0;
+    for (int64_t h = 0; h < H; ++h) a += (double)bf16_val(c->x[t * H + h]) * (double)bf16_val(c->P[l * H + h]);
+    acc = (float)a;
+  } else {
+    for (int64_t h = 0; h < H; ++h) acc += bf16_val(c->x[t * H + h]) * bf16_val(c->P[l * H + h]);
+  }
   c->x_lat[t * c->d->L + l] = oracle_bf16_rne(acc);
 }
 
@@ -421,8 +434,16 @@ static void gateup_body(void* p, int64_t i) {
   { int64_t tmp = gate_row; gate_row = up_row; up_row = tmp; }
 #endif
   float g = 0.0f, u = 0.0f;
-  for (int64_t l = 0; l < L; ++l) g += bf16_val(xr[l]) * w13_elem(c, e, gate_row, l);
-  for (int64_t l = 0; l < L; ++l) u += bf16_val(xr[l]) * w13_elem(c, e, up_row, l);
+  if (g_acc64) {
+    double gd = 0.0, ud = 0.0;
+    for (int64_t l = 0; l < L; ++l) gd += (double)bf16_val(xr[l]) * (double)w13_elem(c, e, gate_row, l);
+    for (int64_t l = 0; l < L; ++l) ud += (double)bf16_val(xr[l]) * (double)w13_elem(c, e, up_row, l);
+    g = (float)gd;
+    u = (float)ud;
+  } else {
+    for (int64_t l = 0; l < L; ++l) g += bf16_val(xr[l]) * w13_elem(c, e, gate_row, l);
+    for (int64_t l = 0; l < L; ++l) u += bf16_val(xr[l]) * w13_elem(c, e, up_row, l);
+  }
   float silu = g / (1.0f + expf(-g));
   c->h[r * I + f] = oracle_bf16_rne(silu * u);
   if (c->gu) {
@@ -439,12 +460,19 @@ static void down_body(void* p, int64_t i) {
   int64_t e = c->idx[r];
   const uint16_t* hr = c->h + r * I;
   float acc = 0.0f;
+  double accd = 0.0;
 #if LMOE_ORACLE_PLANT == 3
-  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + f, l);
+  for (int64_t f = 0; f < I; ++f) {
+    if (g_acc64) accd += (double)bf16_val(hr[f]) * (double)w2_elem(c, e, e * L + f, l);
+    else acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + f, l);
+  }
 #else
-  for (int64_t f = 0; f < I; ++f) acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + l, f);
+  for (int64_t f = 0; f < I; ++f) {
+    if (g_acc64) accd += (double)bf16_val(hr[f]) * (double)w2_elem(c, e, e * L + l, f);
+    else acc += bf16_val(hr[f]) * w2_elem(c, e, e * L + l, f);
+  }
 #endif
-  c->y[r * L + l] = acc;
+  c->y[r * L + l] = g_acc64 ? (float)accd : acc;
 }
 
 /* y[r][:] for every route row r = t*k + j with expert e = topk_idx[r].
@@ -487,13 +515,21 @@ void oracle_norm_combine(const or_dims* d, const float* y, const int32_t* topk_i
                          const float* topk_w, const uint16_t* norm_g, float* yhat_out, float* z) {
   int64_t L = d->L, k = d->k;
   float* yh = (float*)malloc(sizeof(float) * (size_t)L);
+  double* zd = (double*)malloc(sizeof(double) * (size_t)L); /* fp64 sums (acc64) */
   for (int64_t t = 0; t < d->T; ++t) {
     for (int64_t l = 0; l < L; ++l) z[t * L + l] = 0.0f;
+    for (int64_t l = 0; l < L; ++l) zd[l] = 0.0;
     for (int64_t j = 0; j < k; ++j) {
       int64_t r = t * k + j, e = topk_idx[r];
       const float* yr = y + r * L;
       float ss = 0.0f;
-      for (int64_t l = 0; l < L; ++l) ss += yr[l] * yr[l];
+      if (g_acc64) {
+        double sd = 0.0;
+        for (int64_t l = 0; l < L; ++l) sd += (double)yr[l] * (double)yr[l];
+        ss = (float)sd;
+      } else {
+        for (int64_t l = 0; l < L; ++l) ss += yr[l] * yr[l];
+      }
       float ms = ss / (float)L;
       float rinv = 1.0f / sqrtf(ms + d->eps);
 #if LMOE_ORACLE_PLANT == 7
@@ -506,8 +542,14 @@ void oracle_norm_combine(const or_dims* d, const float* y, const int32_t* topk_i
 #endif
       if (yhat_out) memcpy(yhat_out + r * L, yh, sizeof(float) * (size_t)L);
       float w = topk_w[r];
-      for (int64_t l = 0; l < L; ++l) z[t * L + l] += w * yh[l];
+      if (g_acc64) {
+        for (int64_t l = 0; l < L; ++l) zd[l] += (double)(w * yh[l]);
+      } else {
+        for (int64_t l = 0; l < L; ++l) z[t * L + l] += w * yh[l];
+      }
     }
+    if (g_acc64)
+      for (int64_t l = 0; l < L; ++l) z[t * L + l] = (float)zd[l];
 #if LMOE_ORACLE_PLANT == 7
     {
       float ss = 0.0f;
@@ -518,6 +560,7 @@ void oracle_norm_combine(const or_dims* d, const float* y, const int32_t* topk_i
 #endif
   }
   free(yh);
+  free(zd);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -535,7 +578,13 @@ static void unpool_body(void* p, int64_t i) {
   unpool_ctx* c = (unpool_ctx*)p;
   int64_t t = i / c->d->H, o = i % c->d->H, L = c->d->L;
   float acc = 0.0f;
-  for (int64_t l = 0; l < L; ++l) acc += bf16_val(c->zb[t * L + l]) * bf16_val(c->U[o * L + l]);
+  if (g_acc64) {
+    double a = 0.0;
+    for (int64_t l = 0; l < L; ++l) a += (double)bf16_val(c->zb[t * L + l]) * (double)bf16_val(c->U[o * L + l]);
+    acc = (float)a;
+  } else {
+    for (int64_t l = 0; l < L; ++l) acc += bf16_val(c->zb[t * L + l]) * bf16_val(c->U[o * L + l]);
+  }
   c->out[t * c->d->H + o] = oracle_bf16_rne(acc);
 }
 
@@ -591,7 +640,13 @@ void oracle_rmsnorm_rows(int64_t rows, int64_t W, const uint16_t* x, const uint1
   for (int64_t r = 0; r < rows; ++r) {
     const uint16_t* xr = x + r * W;
     float ss = 0.0f;
-    for (int64_t c = 0; c < W; ++c) ss += bf16_val(xr[c]) * bf16_val(xr[c]);
+    if (g_acc64) {
+      double sd = 0.0;
+      for (int64_t c = 0; c < W; ++c) sd += (double)bf16_val(xr[c]) * (double)bf16_val(xr[c]);
+      ss = (float)sd;
+    } else {
+      for (int64_t c = 0; c < W; ++c) ss += bf16_val(xr[c]) * bf16_val(xr[c]);
+    }
     float rinv = 1.0f / sqrtf(ss / (float)W + eps);
     for (int64_t c = 0; c < W; ++c) {
 #if LMOE_ORACLE_PLANT == 9

@@ -156,3 +156,17 @@ def test_planted_mistake_is_caught(plant):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake '{PLANTS[plant]}' passed every pin"
+
+
+def test_acc64_mode_reports_the_oracles_own_error(o, case):
+    """fp64 sums (the diagnostic mode) against the default fp32 sums: the same
+    routing, per-stage differences at the level of fp32 rounding and one bf16
+    ulp, and the default restored bit for bit afterwards."""
+    d = case.d
+    rep = o.error_report(d, case.x, case.w)
+    assert rep["topk_idx_same"]
+    assert rep["x_lat"] <= 2 ** -8 and rep["out"] <= 2 ** -8, rep   # at most bf16 rounding flips
+    assert rep["y"] <= 1e-3 and rep["z"] <= 1e-3, rep
+    assert 0 < rep["y"]  # the fp32 sums do round
+    again = o.forward(d, case.x, case.w)
+    assert np.array_equal(again["out"], case.out)

@@ -33,8 +33,8 @@
 // scale to the accumulators.
 // Tensor memory (512 columns): accumulators of 160 columns (gate/up: gate at
 // 0, up at 160, so SwiGLU pairs are lane-local; down: the item's two 128-row
-// output tiles at 0 and 160, or with one tile per item two buffers), and from
-// column 320 the A stages, 32 columns (64 K of bf16) per weight matrix.
+// output tiles at 0 and 160), and from column 320 the A stages, 32 columns
+// (64 K of bf16) per weight matrix.
 #include <atomic>
 
 #include "common.cuh"
@@ -63,15 +63,10 @@ struct XCfg<0> {  // gate/up: two weight matrices per item, single accumulator p
   static constexpr int NMAT = 2, RAW = 3, ST = 3, NACC = 1;
 };
 template <>
-struct XCfg<1> {  // down, one 128-row output tile per item: double-buffered accumulator
-  static constexpr int NMAT = 1, RAW = 4, ST = 6, NACC = 2;
-};
-template <>
 struct XCfg<2> {  // down, two 128-row output tiles per item sharing each activation stage
   static constexpr int NMAT = 2, RAW = 3, ST = 3, NACC = 1;
 };
 static_assert(kXACol + XCfg<0>::ST * XCfg<0>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
-static_assert(kXACol + XCfg<1>::ST * XCfg<1>::NMAT * 32 <= 512 && XCfg<1>::NACC * kXAcc <= kXACol, "TMEM columns");
 static_assert(kXACol + XCfg<2>::ST * XCfg<2>::NMAT * 32 <= 512 && 2 * kXAcc <= kXACol, "TMEM columns");
 
 template <int MODE>
@@ -83,7 +78,7 @@ template <int MODE>
 constexpr int xsmem_bytes() {
   return xring_bytes<MODE>() + 1024 + 256;
 }
-static_assert(xsmem_bytes<0>() <= 232448 && xsmem_bytes<1>() <= 232448 && xsmem_bytes<2>() <= 232448,
+static_assert(xsmem_bytes<0>() <= 232448 && xsmem_bytes<2>() <= 232448,
               "shared memory budget");
 
 // ---------------------------------------------------------------------------
@@ -260,7 +255,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   pdl_trigger();
 
   // rows of the weight matrix per item and matrix tile m: gate/up: tile ft of the gate
-  // (m = 0) and up (m = 1) halves; down: tile ft (MODE 1) or 128-row tiles 2 ft, 2 ft + 1
+  // (m = 0) and up (m = 1) halves; down: the 128-row tiles 2 ft and 2 ft + 1
   constexpr int TPI = MODE == 2 ? 2 : 1;                            // output tiles per item
   const int nft = (MODE == 0 ? a.inter : a.latent) / (kXM * TPI);  // items per group
   const int n_items = *a.n_groups * nft;
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(kXM, (x.n + 15) & ~15);
         if (!mbar_wait(&acc_empty[acc], cph ^ 1, a.st, 65)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (MODE == 1 ? (uint32_t)acc * kXAcc : 0u);
+        const uint32_t d = tmem;  // one accumulator pair per item (NACC = 1)
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait(&full[as], aph, a.st, 66)) {
             ok = false;
@@ -395,17 +390,15 @@ __global__ void __launch_bounds__(kXThreads, 1)
   } else if (warp < 3 + kDqWarps) {
     // ---------------- dequantisation: codes -> bf16 A stages in TMEM ----------------
     // A warp may only touch the TMEM lanes of its quarter (warp % 4): warp w
-    // handles rows 32 (w % 4) .. +31.  Two tiles per item (gate/up; down in
-    // MODE 2): warps 3-6 the first tile, 7-10 the second, both 32-blocks of each
-    // 64-K step; one tile (MODE 1): warps 3-6 the first and 7-10 the second
-    // 32-block of each step.
+    // handles rows 32 (w % 4) .. +31.  Two tiles per item (gate and up, or two
+    // down tiles): warps 3-6 the first tile, 7-10 the second, both 32-blocks of
+    // each 64-K step.
     const int dw = warp - 3, q = warp & 3;
-    const int m = C::NMAT == 2 ? dw >> 2 : 0;
-    const int b_only = C::NMAT == 2 ? 0 : dw >> 2;
+    const int m = dw >> 2;
     const int rr = q * 32 + lane;
     const int sw = rr & 7;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    constexpr int NB = C::NMAT == 2 ? 2 : 1;
+    constexpr int NB = 2;  // 32-blocks per 64-K step
     int rs = 0, as = 0;
     uint32_t rph = 0, aph = 0;
     bool ok = true;
@@ -449,7 +442,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           uint32_t o[16 * NB];
 #pragma unroll
           for (int bi = 0; bi < NB; ++bi) {
-            const int b = C::NMAT == 2 ? bi : b_only;
+            const int b = bi;
             const int kb = 2 * j + b;  // 32-block within the raw stage
             const uint4 c = *reinterpret_cast<const uint4*>(rawt + ((kb ^ sw) << 4));
             if constexpr (FMT == 1) {
@@ -480,10 +473,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           }
           tc_fence_after();
           const uint32_t acol = tmem + lane_base + kXACol + (uint32_t)(as * C::NMAT + m) * 32u;
-          if (C::NMAT == 2)
-            tmem_st32(acol, o);
-          else
-            tmem_st16(acol + 16u * b_only, o);
+          tmem_st32(acol, o);
           pend_as = as;
           if (++as == C::ST) {
             as = 0;
@@ -521,7 +511,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       const float gsc = FMT == 1 ? __ldg(a.gs + x.e) : 1.0f;  // NVFP4 global scale of this expert matrix
       for (int m = 0; m < TPI; ++m) {
       const int f = (x.ft * TPI + m) * kXM + q * 32 + lane;  // output feature of this lane
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (MODE == 1 ? (uint32_t)acc * kXAcc : (uint32_t)m * kXAcc);
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)m * kXAcc;
       for (int c0 = 32 * half; c0 < x.n; c0 += 64) {
         if (MODE == 0) {
           uint32_t g[32], u[32];
@@ -640,12 +630,10 @@ int launch_tc_gateup(const TcExpertArgs& a, const uint16_t* x_sorted, cudaStream
 
 int launch_tc_down(const TcExpertArgs& a, const uint16_t* h, cudaStream_t s, int num_sms) {
   // two output tiles per item halve the activation traffic per MMA
-  if (a.gs) {
-    if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2, 1>(a, h, s, num_sms);
-    return launch_tc_expert<1, 1>(a, h, s, num_sms);
-  }
-  if (a.latent % (2 * kXM) == 0) return launch_tc_expert<2, 0>(a, h, s, num_sms);
-  return launch_tc_expert<1, 0>(a, h, s, num_sms);
+  // two 128-row output tiles per item: every supported latent width is a multiple of 256
+  if (a.latent % (2 * kXM)) return LMOE_EUNSUPPORTED;
+  if (a.gs) return launch_tc_expert<2, 1>(a, h, s, num_sms);
+  return launch_tc_expert<2, 0>(a, h, s, num_sms);
 }
 
 // x_sorted[p] = x_lat[sorted_rows[p] / k]: one warp per sorted row, 16-byte copies.

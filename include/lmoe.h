@@ -297,9 +297,9 @@ LMOE_API int lmoe_profile_events(void* const* events, int n);
  *    output tiles accumulated in tensor memory); below it, as a
  *    weight-streaming kernel tuned for a few tokens.  Default 64.
  *  LMOE_OPT_EXPERT_TC_MIN_TOKENS: from this many tokens on, the experts run
- *    as grouped tensor-core GEMMs (weights dequantised to bf16 in shared
- *    memory, up to 256 rows of one expert per tile); below it, as the
- *    weight-streaming kernels.  Default 512.
+ *    as grouped tensor-core GEMMs (weights dequantised to bf16 into tensor
+ *    memory, up to 160 rows of one expert per group); below it, as the
+ *    weight-streaming kernels.  Default 352.
  *
  * Both implementations of a stage give bf16 (or fp32) of an fp32 sum per
  * output and differ only in the order of that sum.  value <= 0 restores the

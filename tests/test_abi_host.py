@@ -92,7 +92,7 @@ def test_unsupported_width(lm):
 
 
 def test_regime_options_round_trip(lm):
-    for key, default in ((lm.LMOE_OPT_DENSE_MIN_TOKENS, 64), (lm.LMOE_OPT_EXPERT_TC_MIN_TOKENS, 512)):
+    for key, default in ((lm.LMOE_OPT_DENSE_MIN_TOKENS, 64), (lm.LMOE_OPT_EXPERT_TC_MIN_TOKENS, 352)):
         prev = lm.lmoe_set_option(key, 7)
         assert prev == default
         assert lm.lmoe_set_option(key, 0) == 7  # 0 restores the default

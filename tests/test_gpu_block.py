@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 # (config, T, dense threshold or None): decode chain with one- and several-row groups,
 # many-token routing next to the pooler, the tensor-core router, pooler and unpooler
-# (32 experts, threshold 1), and the grouped tensor-core experts (T >= 512)
+# (32 experts, threshold 1), and the grouped tensor-core experts (T >= 352)
 CASES = [("tiny", 4, None), ("tiny", 37, None), ("tiny_e32", 37, 1), ("tiny_e32", 200, None),
          ("tiny", 600, None), ("decode_t1", None, None), ("verify_t8", None, None)]
 

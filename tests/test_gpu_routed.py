@@ -13,7 +13,7 @@ from parity_util import check_out, device_weights, host_weights, to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 # (config, T): decode with one- and several-row groups, many-token routing next to
-# the pooler, tensor-core projections, and the grouped tensor-core experts (T >= 512)
+# the pooler, tensor-core projections, and the grouped tensor-core experts (T >= 352)
 CASES = [("tiny", 4), ("tiny", 37), ("tiny", 300), ("tiny", 600), ("decode_t1", None), ("verify_t8", None)]
 
 

@@ -554,7 +554,7 @@ def main():
         roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic = None if args.nvfp4 else traffic_from_profiles(dom, name)
+    traffic = traffic_from_profiles(dom, name + ("_nvfp4" if args.nvfp4 else ""))
     roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes_per_launch": dom_bytes,
                  "launch_ms": dom_ms, "peak_source": pk["source"] + (
                      "" if roof["bound"] == "hbm" else

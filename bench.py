@@ -334,6 +334,152 @@ def run_stage(args, d, name, lm, dev):
                       "kernels_ms": {names[j]: statistics.mean(per[j]) for j in range(n)}}), flush=True)
 
 
+PER_CONFIG = ["verify_t4", "verify_t8", "verify_t4_skewed", "verify_t8_skewed", "batched_t64", "prefill_t4096"]
+
+
+def layer_work(d: synth.Dims, touched: int):
+    """Algorithmic bytes and flops of one layer step: the decode roofline's
+    bytes (touched expert slices + pooler + unpooler weights) and the tensor
+    flops (experts, pooler, unpooler; 2 per MAC)."""
+    T, H, L, I, k = d.T, d.H, d.L, d.I, d.k
+    nbytes = touched * EXPERT_BYTES + PROJ_BYTES
+    flops = 2 * T * k * (2 * I * L + L * I) + 2 * 2 * T * H * L
+    return nbytes, flops
+
+
+def layer_fraction(d, touched, ms, pk, tc_peak):
+    """The layer's roofline fraction: HBM bytes for a bandwidth-bound step,
+    tensor flops against the bf16 peak for a compute-bound one (whichever
+    roof the step's arithmetic intensity puts it under)."""
+    nbytes, flops = layer_work(d, touched)
+    balance = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if flops / nbytes > balance:
+        ach = flops / (ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak,
+                "algorithmic_flops": flops}
+    ach = nbytes / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+            "algorithmic_bytes": nbytes}
+
+
+def dominant_roofline(d, touched, kern_ms, pk, tc_peak, traffic_key):
+    """The modelled launch with the largest mean device time, against the
+    roof its own arithmetic intensity puts it under."""
+    cand = [(ms, n) for n, ms in kern_ms.items() if kernel_work(n, d, touched) is not None]
+    dom_ms, dom = max(cand)
+    dom_bytes, dom_flops = kernel_work(dom, d, touched)
+    balance = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if dom_flops / dom_bytes > balance:
+        roof = {"bound": "tensor", "achieved": dom_flops / (dom_ms / 1e3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "algorithmic_flops_per_launch": dom_flops}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": traffic_from_profiles(dom, traffic_key), "kernel": dom,
+                 "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
+                 "peak_source": pk["source"] + ("" if roof["bound"] == "hbm" else
+                                                (" burst" if tc_peak == pk["bf16_tflops"] else " sustained"))})
+    return roof
+
+
+def time_steps(call, steps, flush):
+    """Device time of `steps` calls, each after an L2 flush outside the timed events."""
+    import torch
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        e0[i].record()
+        call()
+        e1[i].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(e0, e1)]
+
+
+def per_launch_ms(lm, call, n_launch, reps, flush):
+    """Mean device time of each kernel launch of one call (CUDA events between launches)."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
+    per = [[] for _ in range(n_launch)]
+    lm.lmoe_profile_events(evs)
+    try:
+        for _ in range(reps):
+            flush.zero_()
+            call()
+            torch.cuda.synchronize()
+            for j in range(n_launch):
+                per[j].append(evs[j].elapsed_time(evs[j + 1]))
+    finally:
+        lm.lmoe_profile_events(None)
+    return per
+
+
+def run_per_config(args, lm, w_dev, hw, dev, flush, pk, want_cpu):
+    """Every other workload config of the layer, timed like the headline one
+    (plain lmoe_forward, inputs resident, L2 flushed between steps): ms per
+    step, tokens/s, the layer's roofline fraction, the dominant kernel's
+    roofline and the CPU oracle on a bounded token sample."""
+    import torch
+    res = {}
+    steps = max(5, min(args.steps, 20))
+    for name in PER_CONFIG:
+        d = synth.CONFIGS[name]
+        bias = synth.make_router_bias(d)
+        w = dict(w_dev)
+        w["router_bias"] = None if bias is None else torch.from_numpy(bias).to(dev)
+        wts = lm.weights_of(w)
+        dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+        ws = torch.empty(lm.lmoe_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        x_np = synth.make_x(d)
+        x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            lm.lmoe_forward(dims, wts, x, out, ws)
+        for _ in range(max(3, args.warmup)):
+            call()
+        rc = lm.lmoe_status_check(ws)
+        if rc != 0:
+            raise RuntimeError(f"{name}: device status {rc}: {lm.lmoe_error_string(rc)}")
+        n_launch = lm.lmoe_last_launch_count()
+        names = [lm.lmoe_last_launch_name(j) for j in range(n_launch)]
+        lay = lm.lmoe_workspace_layout(dims)
+        offs = ws[lay.expert_offsets:lay.expert_offsets + 4 * (d.E + 1)].view(torch.int32).cpu().numpy()
+        touched = int(np.count_nonzero(np.diff(offs)))
+        step_ms = time_steps(call, steps, flush)
+        ms = float(np.mean(step_ms))
+        per = per_launch_ms(lm, call, n_launch, 5, flush)
+        kern_ms = {}
+        for j, nm in enumerate(names):  # a name may repeat (e.g. two tensor-core GEMMs): keep both
+            key = nm if nm not in kern_ms else f"{nm}#{j}"
+            kern_ms[key] = statistics.mean(per[j])
+        tc_peak = pk["bf16_tflops"]
+        entry = {"workload": workload_name(d, name), "T": d.T, "touched_experts": touched, "ms_per_step": ms,
+                 "tokens_per_s": d.T / (ms / 1e3), "launches_per_step": n_launch,
+                 "step_ms_percentiles": {"p10": float(np.percentile(step_ms, 10)),
+                                         "median": float(np.median(step_ms)),
+                                         "p90": float(np.percentile(step_ms, 90))},
+                 "layer_roofline": layer_fraction(d, touched, ms, pk, tc_peak),
+                 "roofline": dominant_roofline(d, touched, {k.split("#")[0] if "#" in k else k: v
+                                                            for k, v in kern_ms.items()}, pk, tc_peak, name),
+                 "kernels_ms": kern_ms}
+        if want_cpu:
+            # the layer is token-independent: the oracle on a bounded sample of the step's tokens
+            ns = min(d.T, 8)
+            S = np.linspace(0, d.T - 1, ns).astype(np.int64)
+            dS = synth.with_tokens(d, ns)
+            hws = dict(hw)
+            hws["router_bias"] = bias
+            rate, cores, reps, dt = cpu_oracle_rate(dS, hws, np.ascontiguousarray(x_np[S]), min_seconds=2.0)
+            entry["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                     "sample": f"{reps} whole-layer evaluations of {ns} of the step's {d.T} "
+                                               f"token(s) ({dt:.1f} s)"}
+        res[name] = entry
+        del ws
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -355,6 +501,9 @@ def main():
     ap.add_argument("--block", action="store_true",
                     help="time the sandwich block around the layer (lmoe_block_forward: pre-norm, layer, "
                          "post-norm and residual) instead of the layer alone")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --config (by default the decode_t1 run also times every other workload "
+                         "config of the layer and reports them under per_config)")
     ap.add_argument("--stage", choices=["pool", "unpool"], default=None,
                     help="time one dense projection call alone (for profiling); prints a stage line")
     args = ap.parse_args()
@@ -540,25 +689,16 @@ def main():
 
     # dominant kernel: the modelled launch with the largest mean device time
     kern_ms = {names[j]: statistics.mean(v) for j, v in enumerate(per_launch)}
-    cand = [(ms, n) for n, ms in kern_ms.items() if kernel_work(n, d, touched) is not None]
-    dom_ms, dom = max(cand)
-    dom_bytes, dom_flops = kernel_work(dom, d, touched)
     step_ms_mean = 1e3 * total_s / args.steps
     tc_peak = pk["bf16_tflops"] if step_ms_mean < 50 or not pk.get("bf16_tflops_sustained") \
         else pk["bf16_tflops_sustained"]
-    balance = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)  # flops per byte where the two roofs meet
-    if dom_flops / dom_bytes > balance:
-        roof = {"bound": "tensor", "achieved": dom_flops / (dom_ms / 1e3) / 1e12, "peak": tc_peak,
-                "unit": "TFLOP/s", "algorithmic_flops_per_launch": dom_flops}
-    else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic = traffic_from_profiles(dom, name + ("_nvfp4" if args.nvfp4 else ""))
-    roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes_per_launch": dom_bytes,
-                 "launch_ms": dom_ms, "peak_source": pk["source"] + (
-                     "" if roof["bound"] == "hbm" else
-                     (" burst" if tc_peak == pk["bf16_tflops"] else " sustained"))})
+    roof = dominant_roofline(d, touched, kern_ms, pk, tc_peak, name + ("_nvfp4" if args.nvfp4 else ""))
+    # the layer's own fraction: HBM bytes at decode, tensor flops at prefill
+    layer_roof = layer_fraction(d, touched, step_ms_mean / n_layers, pk, tc_peak)
+    if args.nvfp4 and layer_roof["bound"] == "hbm":
+        layer_roof["achieved"] = layer_bytes / (step_ms_mean / n_layers / 1e3) / 1e9
+        layer_roof["frac"] = layer_roof["achieved"] / layer_roof["peak"]
+        layer_roof["algorithmic_bytes"] = layer_bytes
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -576,7 +716,7 @@ def main():
                    "l2": "flushed between steps (512 MB device write outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ms_per_layer": 1e3 * total_s / args.steps / n_layers,
-        "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_gbs / pk["hbm_gbs"],
+        "layer_hbm_gbs": layer_gbs, "layer_roofline_frac": layer_roof["frac"], "layer_roofline": layer_roof,
         "layer_bytes_per_step": layer_bytes,
         "roofline": roof,
         "kernels_ms": kern_ms,
@@ -587,6 +727,10 @@ def main():
         "gpu_launches": launches_per_step * n_layers * args.steps,
         "clocks": clocks,
     }
+    plain = not (args.nvfp4 or args.block or args.routed or args.graph or n_layers > 1)
+    if world == 1 and name == "decode_t1" and plain and not args.no_per_config:
+        with torch.cuda.stream(stream):
+            line["per_config"] = run_per_config(args, lm, w, hw, dev, flush, pk, not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, reps, dt = cpu_oracle_rate(d, hw, x, block_norms=block_norms, nvfp4=args.nvfp4)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",

@@ -133,7 +133,13 @@ LMOE_API int lmoe_route(const lmoe_dims* dims, const uint16_t* x, const float* r
 /* Pooler ("Soporte de dia 0 ...", "MoE latente": 8192 -> 4096 learned
  * projection shared by all experts).
  *   x        bf16 [T][H];  pooler_w bf16 [L][H]
- *   x_lat    out bf16 [T][L] = bf16_rne(sum_h x*P), fp32 accumulation. */
+ *   x_lat    out bf16 [T][L] = bf16_rne(sum_h x*P), fp32 accumulation.
+ *   ws, ws_bytes  optional (ws may be NULL): the projection needs no
+ *            scratch.  When a workspace is given, the call zeroes its status
+ *            word and a bounded device wait that runs out is reported there
+ *            (lmoe_status_check), as for every other layer call; with NULL
+ *            nothing is recorded.  This optional pair is the only difference
+ *            from a plain (dims, x, pooler_w, x_lat, stream) signature. */
 LMOE_API int lmoe_pool(const lmoe_dims* dims, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
               void* ws, size_t ws_bytes, lmoe_stream_t stream);
 
@@ -263,7 +269,15 @@ LMOE_API const char* lmoe_last_launch_name(int i);
  * runtime's enqueue path, where that runtime owns every device allocation, or
  * an embedded runtime with a memory budget fixed at start-up).  The pages
  * have no counterpart: this is a deployment variant of lmoe_route.
- *   Same arguments, outputs and results as lmoe_route, minus ws/ws_bytes.
+ *   Same arguments and outputs as lmoe_route, minus ws/ws_bytes, and the same
+ *   dimension rules (LMOE_EINVAL, LMOE_EUNSUPPORTED).  It always runs the
+ *   CUDA-core router (fp32 FMA, split-K), so its results are bit-identical to
+ *   lmoe_route's wherever lmoe_route runs that router too: below 64 tokens,
+ *   or when n_experts is not a multiple of 32.  From 64 tokens with
+ *   n_experts % 32 == 0, lmoe_route computes the logits on the tensor cores,
+ *   which sums the same exact fp32 products in another order; the picks then
+ *   agree except where two logits lie within that rounding of each other,
+ *   and the weights agree to fp32 rounding.
  *   Its scratch is a fixed array inside the library (about 1.1 MB, held on
  *   every GPU that loads the library until the process exits), so it accepts
  *   at most T = 64 tokens and n_experts <= 256, and returns LMOE_ENOSCRATCH

@@ -9,6 +9,53 @@
 
 using namespace lmoe;
 
+namespace lmoe {
+
+thread_local int g_launches = 0;
+constexpr int kMaxNamed = 32;
+thread_local const char* g_names[kMaxNamed];
+thread_local void* const* g_events = nullptr;
+thread_local int g_nevents = 0;
+
+void calls_begin() { g_launches = 0; }
+
+void pre_launch(cudaStream_t s, const char* name) {
+  if (g_launches < kMaxNamed) g_names[g_launches] = name;
+  if (g_events && g_launches < g_nevents) cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
+}
+
+void launched() { ++g_launches; }
+
+int post_call(cudaStream_t s, int rc) {
+  if (rc == LMOE_OK && g_events && g_launches < g_nevents)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
+  return rc;
+}
+
+int check_dims(const lmoe_dims* d) {
+  if (!d) return LMOE_EINVAL;
+  if (d->T < 1 || d->T > 65536 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k ||
+      d->n_experts > 256 || d->hidden < 128 || d->latent < 128 || d->inter < 128 || d->hidden % 128 ||
+      d->latent % 128 || d->inter % 128 || !(d->eps >= 0.f))
+    return LMOE_EINVAL;
+  // expert kernels stream K in 128-byte planes and 2048-element chunks, the
+  // projections in 256- or 512-element chunks
+  if (d->hidden % 256 || d->latent % 256 || d->inter % 256) return LMOE_EUNSUPPORTED;
+  if ((d->latent > 2048 && d->latent % 2048) || (d->inter > 2048 && d->inter % 2048)) return LMOE_EUNSUPPORTED;
+  // the decode expert kernels keep a group's activation rows (whole K) in shared memory
+  if (d->latent > 8192 || d->inter > 8192) return LMOE_EUNSUPPORTED;
+  return LMOE_OK;
+}
+
+int router_splits(int T, int E, int H, int sms, int max_split) {
+  const int base = ((E + 31) / 32) * ((T + 7) / 8);
+  int ns = 1;
+  while (base * ns < 2 * sms && ns < max_split && H % (128 * ns * 2) == 0) ns *= 2;
+  return ns;
+}
+
+}  // namespace lmoe
+
 namespace {
 
 constexpr int kDenseMinTokensDefault = 64;
@@ -36,22 +83,6 @@ bool experts_tc(int T) { return T >= t_expert_tc_min_t; }
 // rows per group of the routing table: what the expert kernels of this regime consume
 int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
 
-thread_local int g_launches = 0;
-constexpr int kMaxNamed = 32;
-thread_local const char* g_names[kMaxNamed];
-thread_local void* const* g_events = nullptr;
-thread_local int g_nevents = 0;
-
-void pre_launch(cudaStream_t s, const char* name) {
-  if (g_launches < kMaxNamed) g_names[g_launches] = name;
-  if (g_events && g_launches < g_nevents) cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
-}
-
-int post_call(cudaStream_t s, int rc) {
-  if (rc == LMOE_OK && g_events && g_launches < g_nevents)
-    cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
-  return rc;
-}
 
 struct DevInfo {
   int sms = 0;
@@ -126,29 +157,9 @@ int set_carveouts() {
   return LMOE_OK;
 }
 
-int check_dims(const lmoe_dims* d) {
-  if (!d) return LMOE_EINVAL;
-  if (d->T < 1 || d->T > 65536 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k ||
-      d->n_experts > 256 || d->hidden < 128 || d->latent < 128 || d->inter < 128 || d->hidden % 128 ||
-      d->latent % 128 || d->inter % 128 || !(d->eps >= 0.f))
-    return LMOE_EINVAL;
-  // expert kernels stream K in 128-byte planes and 2048-element chunks, the
-  // projections in 256- or 512-element chunks
-  if (d->hidden % 256 || d->latent % 256 || d->inter % 256) return LMOE_EUNSUPPORTED;
-  if ((d->latent > 2048 && d->latent % 2048) || (d->inter > 2048 && d->inter % 2048)) return LMOE_EUNSUPPORTED;
-  // the decode expert kernels keep a group's activation rows (whole K) in shared memory
-  if (d->latent > 8192 || d->inter > 8192) return LMOE_EUNSUPPORTED;
-  return LMOE_OK;
-}
-
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
-int router_splits(const lmoe_dims* d, int sms) {
-  const int base = ((d->n_experts + 31) / 32) * ((d->T + 7) / 8);
-  int ns = 1;
-  while (base * ns < 2 * sms && ns < 16 && d->hidden % (128 * ns * 2) == 0) ns *= 2;
-  return ns;
-}
+int router_splits(const lmoe_dims* d, int sms) { return lmoe::router_splits(d->T, d->n_experts, d->hidden, sms, 16); }
 
 struct WsLayout {
   lmoe_ws_layout pub;
@@ -230,7 +241,7 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttr
     cudaLaunchConfig_t cfg_ = pdl_cfg(grid, block, stream, attr_);               \
     pre_launch(stream, #kern);                                                   \
     if (cudaLaunchKernelEx(&cfg_, kern, __VA_ARGS__) != cudaSuccess) return LMOE_ECUDA; \
-    ++g_launches;                                                                \
+    launched();                                                                \
   } while (0)
 
 #define CHECK(x)                 \
@@ -241,7 +252,7 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttr
 
 int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayout* w, cudaStream_t s,
              bool need_ws = true, bool block = false) {
-  g_launches = 0;
+  calls_begin();
   snapshot_options();
   CHECK(check_dims(d));
   CHECK(dev_info(di));
@@ -300,7 +311,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
     g.nsplit = nsplit;
     pre_launch(s, "router_tc_gemm");
     CHECK(launch_tc_gemm_bf16(g, usplit ? usplit : x, w3, s, di.sms));
-    ++g_launches;
+    launched();
   } else {
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, router_partial_kernel, x, router_w, part, T,
            H, E, H / w.nsplit, pre_g);
@@ -338,7 +349,7 @@ int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uin
     GemvArgs g{pooler_w, x, x_lat, d->latent, d->hidden, d->T, st, wait_mode};
     CHECK(launch_gemv_bf16(g, s, di.sms));
   }
-  ++g_launches;
+  launched();
   return LMOE_OK;
 }
 
@@ -372,7 +383,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
     t.h_out = at<uint16_t>(ws, w.h);
     pre_launch(s, "expert_gateup_tc");
     CHECK(launch_tc_gateup(t, xs, s, di.sms));
-    ++g_launches;
+    launched();
     t.q = w2_q;
     t.s = w2_s;
     t.gs = w2_gs;
@@ -382,7 +393,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
     t.ssq_out = at<float>(ws, w.ssq);
     pre_launch(s, "expert_down_tc");
     CHECK(launch_tc_down(t, at<uint16_t>(ws, w.h), s, di.sms));
-    ++g_launches;
+    launched();
     return LMOE_OK;
   }
   const int G = expert_max_group(T);
@@ -406,7 +417,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.rows = T * k;
   pre_launch(s, "expert_gateup");
   CHECK(launch_gateup(a, T, G, s, di.sms));
-  ++g_launches;
+  launched();
   a.q = w2_q;
   a.s = w2_s;
   a.gs = w2_gs;
@@ -418,7 +429,7 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.early = 1;  // the gate/up kernel waited for whatever wrote the group list
   pre_launch(s, "expert_down");
   CHECK(launch_down(a, T, G, s, di.sms));
-  ++g_launches;
+  launched();
   return LMOE_OK;
 }
 
@@ -441,13 +452,13 @@ int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di,
     pre_launch(s, "unpool_gemv");
     GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st, kWaitAfterWeights};
     CHECK(launch_gemv_bf16(g, s, di.sms));
-    ++g_launches;
+    launched();
     return LMOE_OK;
   }
   pre_launch(s, "unpool_tc_gemm");
   TcGemmArgs g{out, d->T, d->hidden, d->latent, st};
   CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
-  ++g_launches;
+  launched();
   return LMOE_OK;
 }
 
@@ -759,11 +770,11 @@ int lmoe_selftest_timeout(void* ws, size_t ws_bytes, unsigned limit_us, lmoe_str
       limit_us > 1000000u)
     return LMOE_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  g_launches = 0;
+  calls_begin();
   if (cudaMemsetAsync(ws, 0, sizeof(Status), s) != cudaSuccess) return LMOE_ECUDA;
   pre_launch(s, "timeout_selftest_kernel");
   timeout_selftest_kernel<<<1, 32, 0, s>>>(static_cast<Status*>(ws), (unsigned long long)limit_us * 1000ull);
-  ++g_launches;
+  launched();
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
 }
 

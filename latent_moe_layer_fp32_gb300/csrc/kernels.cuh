@@ -6,6 +6,18 @@
 
 namespace lmoe {
 
+// ---- api.cu: argument checks and launch bookkeeping shared by the entry points ----
+// LMOE_OK, LMOE_EINVAL or LMOE_EUNSUPPORTED for the layer dimensions
+int check_dims(const lmoe_dims* d);
+// split-K factor of the CUDA-core router: enough CTAs for the GPU, at most max_split
+int router_splits(int T, int E, int H, int sms, int max_split);
+// per-call launch count and names (lmoe_last_launch_count / _name) and the optional
+// per-launch timing events (lmoe_profile_events)
+void calls_begin();
+void pre_launch(cudaStream_t s, const char* name);
+void launched();
+int post_call(cudaStream_t s, int rc);
+
 // ---- route.cu -------------------------------------------------------------
 // g (optional): the sandwich block's pre-norm gain, the router input becomes x * g;
 // rinv (optional): per-token scale of the summed dot products (before the bias)

@@ -62,6 +62,20 @@ int scratch_for_current_device(void** addr, int* sms) {
 
 bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// One launch of `kern` on `s` through cudaLaunchKernelEx (its own return code, not a
+// sticky error of an earlier call), counted and named like every other launch.
+template <typename... KArgs, typename... Args>
+int launch(dim3 grid, dim3 block, cudaStream_t s, const char* name, void (*kern)(KArgs...), Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  lmoe::pre_launch(s, name);
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return LMOE_ECUDA;
+  lmoe::launched();
+  return LMOE_OK;
+}
+
 }  // namespace
 
 extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x, const float* router_w,
@@ -69,17 +83,17 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
                                            int32_t* expert_offsets, int32_t* sorted_rows, int32_t* row_pos,
                                            lmoe_stream_t stream) {
   using namespace lmoe;
-  if (!d || d->T < 1 || d->top_k < 1 || d->top_k > 8 || d->n_experts < d->top_k || d->n_experts > 256 ||
-      d->hidden < 128 || d->hidden % 128 || d->latent < 128 || d->latent % 128 || d->inter < 128 ||
-      d->inter % 128 || !(d->eps >= 0.f))
-    return LMOE_EINVAL;
+  calls_begin();
+  // the same dimension rules as lmoe_route, then the limits of the fixed scratch
+  int rc = check_dims(d);
+  if (rc != LMOE_OK) return rc;
   if (d->T > kNoAllocMaxT || d->n_experts > kNoAllocMaxE) return LMOE_ENOSCRATCH;
   if (!al16(x) || !al16(router_w) || !topk_idx || !topk_w || !expert_offsets || !sorted_rows || !row_pos ||
       (router_bias && !al16(router_bias)))
     return LMOE_EINVAL;
   void* base = nullptr;
   int sms = 0;
-  int rc = scratch_for_current_device(&base, &sms);
+  rc = scratch_for_current_device(&base, &sms);
   if (rc != LMOE_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = d->T, E = d->n_experts, k = d->top_k, H = d->hidden;
@@ -90,13 +104,15 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
   int4* groups = reinterpret_cast<int4*>(scratch + kStatusBytes + kPartBytes);
   // the status word must start at zero; everything else is written before it is read
   if (cudaMemsetAsync(st, 0, sizeof(Status), s) != cudaSuccess) return LMOE_ECUDA;
-  // same split rule as lmoe_route, capped by the scratch (at most 16 splits)
-  const int tiles = ((E + 31) / 32) * ((T + 7) / 8);
-  int ns = 1;
-  while (tiles * ns < 2 * sms && ns < kNoAllocMaxSplit && H % (128 * ns * 2) == 0) ns *= 2;
-  router_partial_kernel<<<dim3((E + 31) / 32, (T + 7) / 8, ns), 256, 0, s>>>(x, router_w, part, T, H, E, H / ns, nullptr);
-  topk_kernel<<<dim3(T), 256, 0, s>>>(part, ns, router_bias, T, E, k, topk_idx, topk_w, nullptr);
-  table_kernel<<<1, 1024, 0, s>>>(topk_idx, T * k, E, expert_max_group(T), expert_offsets, sorted_rows, row_pos,
-                                  groups, n_groups, st);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ECUDA;
+  // the split rule of lmoe_route (at most 16 splits, which the scratch holds)
+  const int ns = router_splits(T, E, H, sms, kNoAllocMaxSplit);
+  rc = launch(dim3((E + 31) / 32, (T + 7) / 8, ns), dim3(256), s, "router_partial_kernel", router_partial_kernel, x,
+              router_w, part, T, H, E, H / ns, (const uint16_t*)nullptr);
+  if (rc == LMOE_OK)
+    rc = launch(dim3(T), dim3(256), s, "topk_kernel", topk_kernel, (const float*)part, ns, router_bias, T, E, k,
+                topk_idx, topk_w, (const float*)nullptr);
+  if (rc == LMOE_OK)
+    rc = launch(dim3(1), dim3(1024), s, "table_kernel", table_kernel, (const int32_t*)topk_idx, T * k, E,
+                expert_max_group(T), expert_offsets, sorted_rows, row_pos, groups, n_groups, st);
+  return post_call(s, rc);
 }

@@ -4,11 +4,16 @@ workspace handling and the comparison rules with their tolerances.
 Tolerances (the layer's contract is "bit-exact indices and tables; output
 max relative error 2e-2 and cosine >= 0.9999"):
 
-* topk_idx, expert_offsets, sorted_rows, row_pos: bit-exact, except tokens
-  whose top-k boundary (or order) lies inside the fp32 summation error bound
-  of the router's reduction tree (logit_bounds); for those the GPU's choice
-  must be a valid top-k for some logits inside the bounds, and the table must
-  satisfy its invariants for the GPU's own choice.
+* topk_idx: bit-exact, except tokens whose top-k boundary (or order) lies
+  inside the fp32 summation error bound of the router's reduction
+  (logit_bounds); for those the GPU's choice must be a valid top-k for some
+  logits inside the bounds.  Every such token is counted and recorded
+  (record_route), and the configs of the layer's workload list must have
+  none.
+* expert_offsets, sorted_rows, row_pos: always bit-exact against the
+  oracle's table of the GPU's own picks.
+* tokens the GPU routed differently are never dropped: their outputs are
+  compared with the oracle run on the GPU's routing (forward_routed).
 * topk_w: the GPU logits differ from the oracle's correctly rounded ones by
   the fp32 summation error (|dl| <~ 1e-5 here), so w = softmax-renormalised
   differs by |dw| <= 2 |dl| w; the test uses 5e-5 relative + 1e-6 absolute.
@@ -82,20 +87,48 @@ def ws_view(ws: torch.Tensor, off: int, dtype, shape):
 # comparisons
 # ----------------------------------------------------------------------------------------
 
-def logit_bounds(d, absdot, depth=None, extra_depth=0):
+def router_regime(d, dense_min_t=64):
+    """Which router the library runs for d: the tensor-core GEMM above 16
+    tokens from the dense threshold on when the experts fill 32-column
+    chunks, else the CUDA-core split-K reduction."""
+    return "tensor" if (d.T > 16 and d.T >= dense_min_t and d.E % 32 == 0) else "simt"
+
+
+def router_depth(d, regime="simt"):
+    """Rounding steps per term of the GPU router's fp32 logit sum.
+    simt: a lane chain of at most 4*H/128 FMAs, 5 shuffle levels, at most 16
+    split partials added in order.  tensor: x against the three bf16 parts of
+    each weight, K = 3H split at least four ways; the order inside an MMA is not
+    documented, so every product of a split counts as its own step, and each
+    step twice (a rounding that truncates), plus at most 16 split partials."""
+    if regime == "tensor":
+        return 2 * (3 * d.H // 4) + 16
+    return 4 * d.H // 128 + 5 + 16
+
+
+def logit_bounds(d, absdot, depth=None, extra_depth=0, regime="simt"):
     """Rigorous bound on |fp32 GPU logit - correctly rounded logit|: a sum
-    evaluated as a tree of depth n has error <= n * u * sum|terms|; the router
-    kernel's tree is at most 4*H/128 lane terms + 5 shuffle levels + 16
-    split partials deep, plus half an ulp for the oracle's rounding.
-    extra_depth adds rounding steps per term (the block's router input)."""
+    evaluated with at most n rounding steps per term has error <= n * u *
+    sum|terms|, plus half an ulp for the oracle's rounding.  extra_depth adds
+    rounding steps per term (the block's router input)."""
     if depth is None:
-        depth = 4 * d.H // 128 + 5 + 16 + extra_depth
+        depth = router_depth(d, regime) + extra_depth
     return (depth + 1) * 2.0 ** -24 * absdot
 
 
-def near_tie_tokens(d, logits, absdot, extra_depth=0):
-    """Tokens whose top-k boundary lies within the summation error bound."""
-    b = logit_bounds(d, absdot, extra_depth=extra_depth)
+def boundary_gaps(d, logits):
+    """Per token: the gap between the k-th and (k+1)-th largest logit (inf
+    when k = E) and the smallest gap between consecutive picks."""
+    l = np.sort(logits.astype(np.float64), axis=1)[:, ::-1]
+    kth = l[:, d.k - 1] - l[:, d.k] if d.k < d.E else np.full(l.shape[0], np.inf)
+    inner = np.min(l[:, :d.k - 1] - l[:, 1:d.k], axis=1) if d.k > 1 else np.full(l.shape[0], np.inf)
+    return kth, inner
+
+
+def near_tie_tokens(d, logits, absdot, extra_depth=0, regime="simt"):
+    """Tokens whose top-k boundary (or the order inside the top k) lies within
+    the summation error bound."""
+    b = logit_bounds(d, absdot, extra_depth=extra_depth, regime=regime)
     order = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")
     l = logits.astype(np.float64)
     sel = order[:, :d.k]
@@ -109,25 +142,59 @@ def near_tie_tokens(d, logits, absdot, extra_depth=0):
     return np.nonzero((lo_sel <= hi_rest) | inner)[0]
 
 
-def check_indices(d, gpu_idx, ref_idx, logits, absdot, extra_depth=0):
+def check_indices(d, gpu_idx, ref_idx, logits, absdot, extra_depth=0, regime="simt"):
     """Exact equality outside near-tie tokens; a valid top-k choice inside.
     Returns (flagged tokens, tokens whose GPU choice differs)."""
-    flagged = near_tie_tokens(d, logits, absdot, extra_depth)
+    flagged = near_tie_tokens(d, logits, absdot, extra_depth, regime)
     ok = np.ones(gpu_idx.shape[0], bool)
     ok[flagged] = False
     bad = np.nonzero((gpu_idx != ref_idx).any(1) & ok)[0]
     assert bad.size == 0, f"index mismatch outside near ties: tokens {bad[:10]}"
-    b = logit_bounds(d, absdot, extra_depth=extra_depth)
+    b = logit_bounds(d, absdot, extra_depth=extra_depth, regime=regime)
     l = logits.astype(np.float64)
-    for t in flagged:
+    differs = np.nonzero((gpu_idx != ref_idx).any(1))[0]
+    for t in differs:
         S = gpu_idx[t]
         assert len(set(S.tolist())) == d.k and S.min() >= 0 and S.max() < d.E
         notS = np.setdiff1d(np.arange(d.E), S)
         # some logits within the bounds make S the top-k, in this order
         assert np.min(l[t, S] + b[t, S]) >= (np.max(l[t, notS] - b[t, notS]) if notS.size else -np.inf)
         assert np.all(l[t, S[:-1]] + b[t, S[:-1]] >= l[t, S[1:]] - b[t, S[1:]])
-    differs = np.nonzero((gpu_idx != ref_idx).any(1))[0]
     return flagged, differs
+
+
+def weights_at(logits, idx):
+    """Softmax over all experts renormalised over the picks idx, in fp64, from
+    the oracle's logits: the weights the oracle gives when it picks idx."""
+    l = logits.astype(np.float64)
+    sel = np.take_along_axis(l, idx.astype(np.int64), 1)
+    p = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def record_route(label, d, regime, logits, absdot, flagged, differs, extra_depth=0):
+    """One line per routed config into $LMOE_RECORD_DIR/route_record.jsonl (when
+    set): how many tokens lie inside the bound and how many the GPU routed
+    differently, with the logit gap at the top-k boundary and the bound there."""
+    import json
+    import os
+    out_dir = os.environ.get("LMOE_RECORD_DIR")
+    kth, inner = boundary_gaps(d, logits)
+    b = logit_bounds(d, absdot, extra_depth=extra_depth, regime=regime)
+    bmax = b.max(axis=1)
+    ratio = np.minimum(kth, inner) / np.maximum(bmax, 1e-300)
+    t_min = int(np.argmin(ratio))
+    rec = {"config": label, "T": int(d.T), "E": int(d.E), "k": int(d.k), "regime": regime,
+           "flagged": int(len(flagged)), "differs": int(len(differs)),
+           "closest_token": t_min, "closest_gap": float(min(kth[t_min], inner[t_min])),
+           "closest_bound": float(bmax[t_min]),
+           "differing": [{"t": int(t), "gap": float(min(kth[t], inner[t])), "bound": float(bmax[t])}
+                         for t in differs[:32]]}
+    if out_dir:
+        os.makedirs(out_dir, exist_ok=True)
+        with open(os.path.join(out_dir, "route_record.jsonl"), "a") as f:
+            f.write(json.dumps(rec) + "\n")
+    return rec
 
 
 def check_table_properties(d, idx, off, rows, pos):

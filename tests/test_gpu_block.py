@@ -12,8 +12,8 @@ import torch
 
 import oracle
 import synth
-from parity_util import (bf, check_indices, check_out, check_table_properties, device_weights, host_weights, to_dev,
-                         to_host, ws_view)
+from parity_util import (bf, check_indices, check_out, device_weights, host_weights, record_route, router_regime,
+                         to_dev, to_host, weights_at, ws_view)
 from test_gpu_dense import dense_from
 
 pytestmark = pytest.mark.gpu
@@ -75,25 +75,39 @@ def test_block_matches_oracle(lm, orc, name, T, dense):
     # the two roundings of n (2 ulp per term), within the bound below
     gidx = to_host(ws_view(ws, lay.topk_idx, torch.int32, (d.T, d.k)))
     gw = to_host(ws_view(ws, lay.topk_w, torch.float32, (d.T, d.k)))
-    flagged, differs = check_indices(d, gidx, ref["topk_idx"], ref["logits"], ref["absdot"], extra_depth=3)
-    print(f"[block {name} T={d.T}] near-tie tokens {len(flagged)}, choice differs on {len(differs)}")
+    regime = router_regime(d, dense if dense is not None else 64)
+    # the tensor-core router of the block runs over K = 6H (the input in two bf16 parts)
+    extra = 3 + (2 * (3 * d.H // 4) if regime == "tensor" else 0)
+    flagged, differs = check_indices(d, gidx, ref["topk_idx"], ref["logits"], ref["absdot"], extra_depth=extra,
+                                     regime=regime)
+    rec = record_route(f"block {name} T={d.T}", d, regime, ref["logits"], ref["absdot"], flagged, differs, extra)
+    print(f"[block {name} T={d.T}] {rec}")
     same = np.ones(d.T, bool)
     same[differs] = False
     assert np.allclose(gw[same], ref["topk_w"][same], rtol=1e-4, atol=2e-6), np.abs(gw[same] - ref["topk_w"][same]).max()
+    if differs.size:
+        assert np.allclose(gw[differs], weights_at(ref["logits"][differs], gidx[differs]), rtol=1e-4, atol=2e-6)
     off = to_host(ws_view(ws, lay.expert_offsets, torch.int32, (d.E + 1,)))
     rows = to_host(ws_view(ws, lay.sorted_rows, torch.int32, (d.T * d.k,)))
     pos = to_host(ws_view(ws, lay.row_pos, torch.int32, (d.T * d.k,)))
-    check_table_properties(d, gidx, off, rows, pos)
+    # the table: bit-exact against the oracle's table of the GPU's picks
+    o_off, o_rows, o_pos = orc.table(d, gidx)
+    assert np.array_equal(off, o_off) and np.array_equal(rows, o_rows) and np.array_equal(pos, o_pos)
     y = to_host(y_dev)
-    if differs.size == 0:
-        check_out(y, ref["y"], "y")
-    else:  # rows of tokens routed differently (near ties) are compared on the other tokens only
-        check_out(y[same], ref["y"][same], "y (tokens routed alike)")
+    want = ref["y"].copy()
+    if differs.size:
+        # tokens routed differently (near ties): the oracle's block on the GPU's routing
+        dS = synth.with_tokens(d, len(differs))
+        r = orc.forward_routed(dS, np.ascontiguousarray(ref["nb"][differs]), hw, np.ascontiguousarray(gidx[differs]),
+                               np.ascontiguousarray(gw[differs]))
+        p = orc.rmsnorm(r["out"], nw["post_g"], d.eps)
+        want[differs] = orc.residual_add(np.ascontiguousarray(x[differs]), p)
+    check_out(y, want, "y")
     # y minus the residual: the post-norm of the layer output, compared on its own scale
     post_g = bf(nw["post_g"])
-    got_p, ref_p = bf(y) - bf(x), bf(ref["y"]) - bf(x)
-    num = np.linalg.norm((got_p - ref_p)[same], axis=1)
-    den = np.linalg.norm(ref_p[same], axis=1) + 1e-30
+    got_p, ref_p = bf(y) - bf(x), bf(want) - bf(x)
+    num = np.linalg.norm(got_p - ref_p, axis=1)
+    den = np.linalg.norm(ref_p, axis=1) + 1e-30
     assert np.all(num / den <= 2e-2), np.max(num / den)
     assert np.abs(post_g).max() > 0
 

@@ -133,4 +133,5 @@ def test_router_regimes(lm, orc, name, T, regime):
         got = run_route(lm, d, to_dev(x), w)
         names = [lm.lmoe_last_launch_name(i) for i in range(lm.lmoe_last_launch_count())]
     assert ("router_tc_gemm" in names) == (regime == "tensor"), names
-    check_route(orc, d, x, hw, got)
+    check_route(orc, d, x, hw, got, regime="tensor" if regime == "tensor" else "simt",
+                label=f"{name} T={T} {regime} router")

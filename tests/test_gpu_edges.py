@@ -87,22 +87,27 @@ def test_largest_token_count(lm, orc):
     """T = 65536, the most the library accepts: the routing table is checked in
     full against the oracle's, the output on sampled tokens (the layer is
     token-independent)."""
-    from test_gpu_parity import check_route, run_route, sample_tokens
-    from parity_util import device_weights, host_weights
+    from test_gpu_parity import check_out_routed, check_route, run_route, sample_tokens
+    from parity_util import device_weights, host_weights, ws_view
     d = synth.with_tokens(synth.CONFIGS["prefill_t4096"], 65536)
     hw = host_weights(d)
     w = device_weights(d)
     x = synth.make_x(d)
     x_dev = to_dev(x)
     got = run_route(lm, d, x_dev, w)
-    _, _, differs = check_route(orc, d, x, hw, got)
+    _, _, differs = check_route(orc, d, x, hw, got, label="T=65536")
     dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
     ws = ws_for(lm, dims)
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_forward(dims, lm.weights_of(w), x_dev, out, ws)
     assert lm.lmoe_status_check(ws) == 0
-    S = sample_tokens(d.T)
-    S = S[~np.isin(S, differs)]
+    lay = lm.lmoe_workspace_layout(dims)
+    fidx = to_host(ws_view(ws, lay.topk_idx, torch.int32, (d.T, d.k)))
+    fw = to_host(ws_view(ws, lay.topk_w, torch.float32, (d.T, d.k)))
+    assert np.array_equal(fidx, got["idx"])
+    # sampled tokens, plus every token routed differently from the oracle (checked on its own routing)
+    S = np.union1d(sample_tokens(d.T), differs)
     dS = synth.with_tokens(d, len(S))
     ref = orc.forward(dS, np.ascontiguousarray(x[S]), hw)
-    check_out(to_host(out)[S], ref["out"], "out (T = 65536, sampled tokens)")
+    check_out_routed(orc, d, x, hw, to_host(out)[S], ref["out"], differs, fidx, fw,
+                     "out (T = 65536, sampled tokens)", tokens=S)

@@ -1,13 +1,19 @@
 """lmoe_forward captured in a CUDA graph: the memset, the programmatic-launch
-chain and the side-stream fork/join all replay, and a replay equals the eager
-call bit for bit, also after new input is copied into the captured buffer."""
+chain and the side-stream fork/join all replay.  A replay equals the eager
+call bit for bit and matches the CPU oracle, also after new input is copied
+into the captured buffer; a two-layer stack captured in one graph (each
+layer's bf16 output the next layer's input) matches the oracle layer by
+layer and the oracle applied twice."""
 from __future__ import annotations
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from parity_util import device_weights, to_dev, ws_for
+from parity_util import (check_indices, check_out, device_weights, host_weights, router_regime, to_dev, to_host,
+                         ws_for, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,14 +31,35 @@ def lm():
     return lm
 
 
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def check_layer(lm, orc, d, x_u16, out_u16, ws, dims, what):
+    """One layer's output against the oracle on the same input: the oracle's
+    own routing where the GPU picked the same experts, the oracle on the GPU's
+    routing for near-tie tokens (none are expected)."""
+    from test_gpu_parity import check_out_routed
+    hw = host_weights(d)
+    ref = orc.forward(d, x_u16, hw)
+    lay = lm.lmoe_workspace_layout(dims)
+    gidx = to_host(ws_view(ws, lay.topk_idx, torch.int32, (d.T, d.k)))
+    gw = to_host(ws_view(ws, lay.topk_w, torch.float32, (d.T, d.k)))
+    logits, absdot = orc.router_logits(d, x_u16, hw["router_w"], hw["router_bias"], want_absdot=True)
+    _, differs = check_indices(d, gidx, ref["topk_idx"], logits, absdot, regime=router_regime(d))
+    check_out_routed(orc, d, x_u16, hw, out_u16, ref["out"], differs, gidx, gw, what)
+    return ref
+
+
 @pytest.mark.parametrize("name,T", CASES, ids=[f"{n}_T{t}" for n, t in CASES])
-def test_forward_replays_from_a_cuda_graph(lm, name, T):
+def test_forward_replays_from_a_cuda_graph(lm, orc, name, T):
     d = synth.CONFIGS[name] if T is None else synth.with_tokens(synth.CONFIGS[name], T)
     wts = lm.weights_of(device_weights(d))
     dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
     ws = ws_for(lm, dims)
-    x = to_dev(synth.make_x(d))
-    x2 = to_dev(synth.make_x(d, token0=d.T))  # the next T tokens of the same stream
+    xh, x2h = synth.make_x(d), synth.make_x(d, token0=d.T)  # the next T tokens of the same stream
+    x, x2 = to_dev(xh), to_dev(x2h)
     ref = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
     ref2 = torch.empty_like(ref)
     lm.lmoe_forward(dims, wts, x, ref, ws)
@@ -56,8 +83,57 @@ def test_forward_replays_from_a_cuda_graph(lm, name, T):
     torch.cuda.synchronize()
     assert lm.lmoe_status_check(ws) == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    check_layer(lm, orc, d, xh, to_host(out), ws, dims, "graph replay")
     xin.copy_(x2)
     g.replay()
     torch.cuda.synchronize()
     assert lm.lmoe_status_check(ws) == 0
     assert torch.equal(out.view(torch.int16), ref2.view(torch.int16))
+    check_layer(lm, orc, d, x2h, to_host(out), ws, dims, "graph replay, new input")
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("decode_t1", None)], ids=["tiny_T4", "decode_t1"])
+def test_two_layer_stack_from_a_cuda_graph(lm, orc, name, T):
+    """Two layers back to back in one captured graph, layer 2 reading layer 1's
+    bf16 output, each layer with its own device copy of the weights and its
+    own workspace (the multi-layer decode loop)."""
+    d = synth.CONFIGS[name] if T is None else synth.with_tokens(synth.CONFIGS[name], T)
+    w1 = device_weights(d)
+    w2 = {k: (None if v is None else v.clone()) for k, v in w1.items()}
+    wts = [lm.weights_of(w1), lm.weights_of(w2)]
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    ws = [ws_for(lm, dims), ws_for(lm, dims)]
+    xh = synth.make_x(d)
+    x = to_dev(xh)
+    mid = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(mid)
+
+    def stack():
+        lm.lmoe_forward(dims, wts[0], x, mid, ws[0])
+        lm.lmoe_forward(dims, wts[1], mid, out, ws[1])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        stack()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        stack()
+    mid.zero_()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lm.lmoe_status_check(ws[0]) == 0 and lm.lmoe_status_check(ws[1]) == 0
+    mid_h, out_h = to_host(mid), to_host(out)
+    # layer by layer: each layer against the oracle on the same input
+    ref1 = check_layer(lm, orc, d, xh, mid_h, ws[0], dims, "layer 1")
+    check_layer(lm, orc, d, mid_h, out_h, ws[1], dims, "layer 2 (on the GPU's layer-1 output)")
+    # end to end: the oracle applied twice (layer 2 on the oracle's own layer-1 output)
+    hw = host_weights(d)
+    ref2 = orc.forward(d, ref1["out"], hw)
+    lay = lm.lmoe_workspace_layout(dims)
+    gidx2 = to_host(ws_view(ws[1], lay.topk_idx, torch.int32, (d.T, d.k)))
+    assert np.array_equal(gidx2, ref2["topk_idx"]), "layer 2 routed differently from the oracle applied twice"
+    check_out(out_h, ref2["out"], "two layers against the oracle applied twice")

@@ -16,8 +16,9 @@ import torch
 
 import oracle
 import synth
-from parity_util import (bf, check_bf16_close, sum_err, check_indices, check_out, check_rows_normwise, check_table_properties,
-                         device_weights, host_weights, to_dev, to_host, ws_for, ws_view)
+from parity_util import (bf, check_bf16_close, check_indices, check_out, check_rows_normwise, device_weights,
+                         host_weights, record_route, router_regime, sum_err, to_dev, to_host, weights_at, ws_for,
+                         ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -78,25 +79,52 @@ def pool_err(d, x, hw):
     return sum_err(d.H, np.abs(bf(x)), np.abs(bf(hw["pooler_w"])))
 
 
-def check_route(orc, d, x, hw, got):
-    """Returns the oracle's (idx, w) and the tokens where the GPU chose a
-    different (valid, near-tie) set or order."""
+def check_route(orc, d, x, hw, got, regime=None, label=None, strict=False):
+    """Top-k, weights and table of one routing call against the oracle.
+
+    Indices: bit-exact outside near ties (a valid choice inside).  Weights: the
+    oracle's weights at the GPU's picks.  Table: bit-exact against the oracle's
+    table of the GPU's picks, always.  The counts of near-tie and differently
+    routed tokens are recorded; strict (the layer's workload configs) asserts
+    that no token was routed differently.  Returns the oracle's (idx, w), the
+    tokens the GPU routed differently and the oracle logits."""
+    regime = regime or router_regime(d)
     logits, absdot = orc.router_logits(d, x, hw["router_w"], hw["router_bias"], want_absdot=True)
     idx, tw = orc.topk(d, logits)
-    flagged, differs = check_indices(d, got["idx"], idx, logits, absdot)
-    print(f"[route {d.T}] near-tie tokens {len(flagged)}, GPU choice differs on {len(differs)}: {differs[:8]}")
+    flagged, differs = check_indices(d, got["idx"], idx, logits, absdot, regime=regime)
+    rec = record_route(label or f"T={d.T}", d, regime, logits, absdot, flagged, differs)
+    print(f"[route {rec['config']}] {rec}")
     same = np.ones(d.T, bool)
     same[differs] = False
     assert np.allclose(got["w"][same], tw[same], rtol=5e-5, atol=1e-6), np.abs(got["w"][same] - tw[same]).max()
+    if differs.size:
+        ref_w = weights_at(logits[differs], got["idx"][differs])
+        assert np.allclose(got["w"][differs], ref_w, rtol=5e-5, atol=1e-6)
     assert np.allclose(got["w"].sum(1), 1.0, atol=1e-5)
-    if differs.size == 0:
-        off, rows, pos = orc.table(d, idx)
-        assert np.array_equal(got["off"], off)
-        assert np.array_equal(got["rows"], rows)
-        assert np.array_equal(got["pos"], pos)
-    else:
-        check_table_properties(d, got["idx"], got["off"], got["rows"], got["pos"])
+    off, rows, pos = orc.table(d, got["idx"])
+    assert np.array_equal(got["off"], off)
+    assert np.array_equal(got["rows"], rows)
+    assert np.array_equal(got["pos"], pos)
+    if strict:
+        assert differs.size == 0, f"{rec['config']}: tokens routed differently from the oracle: {rec['differing']}"
     return idx, tw, differs
+
+
+def check_out_routed(orc, d, x, hw, out_u16, ref_out, differs, gpu_idx, gpu_w, what="forward", tokens=None):
+    """Layer output of every token: the oracle's own output where the GPU
+    routed like the oracle, the oracle run on the GPU's routing
+    (forward_routed) where it did not.  tokens: the rows of out_u16 / ref_out
+    (default: all T)."""
+    tokens = np.arange(d.T) if tokens is None else np.asarray(tokens)
+    want = ref_out.copy()
+    dt = np.nonzero(np.isin(tokens, differs))[0]
+    if dt.size:
+        tt = tokens[dt]
+        dS = synth.with_tokens(d, len(tt))
+        r = orc.forward_routed(dS, np.ascontiguousarray(x[tt]), hw, np.ascontiguousarray(gpu_idx[tt]),
+                               np.ascontiguousarray(gpu_w[tt]))
+        want[dt] = r["out"]
+    return check_out(out_u16, want, what)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -115,7 +143,7 @@ def test_stages_small(lm, orc, name, T):
     ws = ws_for(lm, dims)
     # route
     got = run_route(lm, d, x_dev, w)
-    check_route(orc, d, x, hw, got)
+    check_route(orc, d, x, hw, got, label=f"{name} T={T}", strict=(name == "tiny" and T == 4))
     # pool
     x_lat = torch.empty(T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
@@ -169,7 +197,7 @@ def test_full_shape(lm, orc, name):
     dims = dims_c(lm, d)
     ws = ws_for(lm, dims)
     got = run_route(lm, d, x_dev, w)
-    _, _, differs = check_route(orc, d, x, hw, got)
+    _, _, differs = check_route(orc, d, x, hw, got, label=name, strict=True)
     x_lat = torch.empty(d.T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
     check_bf16_close(to_host(x_lat), ref["x_lat"], "x_lat", pool_err(d, x, hw))
@@ -186,9 +214,11 @@ def test_full_shape(lm, orc, name):
     out2 = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_forward(dims, lm.weights_of(w), x_dev, out2, ws)
     assert lm.lmoe_status_check(ws) == 0
-    keep = np.ones(d.T, bool)
-    keep[differs] = False  # near-tie tokens routed differently (validated above)
-    check_out(to_host(out2)[keep], ref["out"][keep], "forward")
+    lay = lm.lmoe_workspace_layout(dims)
+    fidx = to_host(ws_view(ws, lay.topk_idx, torch.int32, (d.T, d.k)))
+    fw = to_host(ws_view(ws, lay.topk_w, torch.float32, (d.T, d.k)))
+    assert np.array_equal(fidx, got["idx"])  # the fused call routes like lmoe_route
+    check_out_routed(orc, d, x, hw, to_host(out2), ref["out"], differs, fidx, fw, "forward")
     if d.skewed:
         touched = np.count_nonzero(np.diff(got["off"]))
         assert touched < 40, touched  # routes concentrate on the biased experts
@@ -207,7 +237,7 @@ def test_prefill_sampled(lm, orc):
     xS = np.ascontiguousarray(x[S])
     # route: all tokens (indices and tables are checked in full)
     got = run_route(lm, d, x_dev, w)
-    idx, tw, differs = check_route(orc, d, x, hw, got)
+    idx, tw, differs = check_route(orc, d, x, hw, got, label="prefill_t4096", strict=True)
     # pool: sampled rows
     x_lat = torch.empty(d.T, d.L, dtype=torch.bfloat16, device="cuda")
     lm.lmoe_pool(dims, x_dev, w["pooler_w"], x_lat, ws)
@@ -234,8 +264,11 @@ def test_prefill_sampled(lm, orc):
     lm.lmoe_forward(dims, lm.weights_of(w), x_dev, out2, ws)
     assert lm.lmoe_status_check(ws) == 0
     refS = orc.forward(dS, xS, hw)
-    keep = ~np.isin(S, differs)
-    check_out(to_host(out2)[S][keep], refS["out"][keep], "forward")
+    lay = lm.lmoe_workspace_layout(dims)
+    fidx = to_host(ws_view(ws, lay.topk_idx, torch.int32, (d.T, d.k)))
+    fw = to_host(ws_view(ws, lay.topk_w, torch.float32, (d.T, d.k)))
+    assert np.array_equal(fidx, got["idx"])
+    check_out_routed(orc, d, x, hw, to_host(out2)[S], refS["out"], differs, fidx, fw, "forward", tokens=S)
 
 
 # ------------------------------------------------------------------------------------------------

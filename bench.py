@@ -49,6 +49,7 @@ GATEUP_BYTES = 2 * EXPERT_BYTES // 3
 PROJ_BYTES = 134_217_728           # pooler + unpooler bf16
 # source files each measured kernel is built from (the ncu summary's source_sha256 covers these)
 KERNEL_SOURCES = {
+    "expert_fused": ("fused_experts.cu", "common.cuh"),
     "expert_gateup": ("experts.cu", "common.cuh"),
     "expert_down": ("experts.cu", "common.cuh"),
     "pool_tc_gemm": ("tc_gemm.cu", "tc.cuh", "common.cuh"),
@@ -81,6 +82,9 @@ def kernel_work(kernel: str, d: synth.Dims, touched: int):
     every operand read once, every result written once, 2 flops per MAC."""
     T, H, L, I, k = d.T, d.H, d.L, d.I, d.k
     R = T * k
+    if kernel == "expert_fused":  # gate/up + SwiGLU and down in one launch
+        return (touched * EXPERT_BYTES + 2 * T * L + 2 * 2 * R * I + 4 * R * L + 4 * R * (L // 32),
+                2 * R * 3 * I * L)
     if kernel.startswith("expert_gateup"):
         return touched * GATEUP_BYTES + 2 * T * L + 2 * R * I, 2 * R * 2 * I * L
     if kernel.startswith("expert_down"):

@@ -62,15 +62,20 @@ constexpr int kDenseMinTokensDefault = 64;
 // measured crossover on GB300 at the full layer shape: the streaming experts win up to
 // about 350 tokens (256: 2.28 against 2.93 ms per step), the grouped GEMMs from there (384: 2.96 against 3.16)
 constexpr int kExpertTcMinTokensDefault = 352;
+// decode sizes: gate/up and down in one persistent launch up to this many tokens
+constexpr int kFusedMaxTokensDefault = 0;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
+std::atomic<int> g_fused_max_t{kFusedMaxTokensDefault};
 // the options as read once at the start of the current call on this thread, so
 // that every decision inside one call sees the same regime
 thread_local int t_dense_min_t = kDenseMinTokensDefault;
 thread_local int t_expert_tc_min_t = kExpertTcMinTokensDefault;
+thread_local int t_fused_max_t = kFusedMaxTokensDefault;
 void snapshot_options() {
   t_dense_min_t = g_dense_min_t.load(std::memory_order_relaxed);
   t_expert_tc_min_t = g_expert_tc_min_t.load(std::memory_order_relaxed);
+  t_fused_max_t = g_fused_max_t.load(std::memory_order_relaxed);
 }
 
 // the router as a tensor-core GEMM: above the fused small-T routing, from the
@@ -80,6 +85,10 @@ bool router_tc(const lmoe_dims* d) {
 }
 
 bool experts_tc(int T) { return T >= t_expert_tc_min_t; }
+// the persistent decode experts: MXFP4, at most 8 tokens and 64 route rows
+bool experts_fused(const lmoe_dims* d, bool nvfp4) {
+  return !nvfp4 && !experts_tc(d->T) && d->T <= t_fused_max_t && d->T <= 8 && d->T * d->top_k <= 64;
+}
 // rows per group of the routing table: what the expert kernels of this regime consume
 int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
 
@@ -163,7 +172,7 @@ int router_splits(const lmoe_dims* d, int sms) { return lmoe::router_splits(d->T
 
 struct WsLayout {
   lmoe_ws_layout pub;
-  size_t n_groups, route_count, zero_bytes, groups, part, h, ssq, xs, wr3, rank, chunk;
+  size_t n_groups, route_count, ctr, zero_bytes, groups, part, h, ssq, xs, wr3, rank, chunk;
   // the sandwich block: pre-norm output (bf16), its per-token rinv, the router
   // input split in two bf16 parts (tensor-core router), the layer's output
   size_t nb = 0, rinv = 0, usplit = 0, lout = 0;
@@ -186,7 +195,8 @@ int layout(const lmoe_dims* d, int sms, WsLayout* w, bool block = false) {
   w->pub.status = 0;
   w->n_groups = 16;
   w->route_count = 64;  // small-T routing tickets: [0] last block overall, [1 + b] last split of block b (b < 16)
-  w->zero_bytes = 160;
+  w->ctr = 256;         // persistent decode experts: per-group completion counters (64) + down-done count
+  w->zero_bytes = 768;
   take(w->zero_bytes);
   w->pub.topk_idx = take(4 * R);
   w->pub.topk_w = take(4 * R);
@@ -357,10 +367,20 @@ int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uin
 // groups_early: the group list was written by a kernel before the preceding one
 // (lmoe_forward: the routing precedes the pooler), so the gate/up kernel may
 // stream its first weights before waiting for its predecessor
+// nz (the layer's norm and sum, else null): the persistent decode experts then also
+// form bf16(z) in the workspace and set *z_ready
+struct NormSum {
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const uint16_t* norm_g;
+  bool* z_ready;
+};
+
 int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const uint16_t* x_lat,
                 const int32_t* sorted_rows, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                 const uint8_t* w2_s, float* y, void* ws, cudaStream_t s, bool xs_ready = false,
-                bool groups_early = false, const float* w13_gs = nullptr, const float* w2_gs = nullptr) {
+                bool groups_early = false, const float* w13_gs = nullptr, const float* w2_gs = nullptr,
+                const NormSum* nz = nullptr) {
   const int T = d->T, k = d->top_k, L = d->latent, I = d->inter;
   Status* st = at<Status>(ws, w.pub.status);
   if (experts_tc(T)) {
@@ -393,6 +413,41 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
     t.ssq_out = at<float>(ws, w.ssq);
     pre_launch(s, "expert_down_tc");
     CHECK(launch_tc_down(t, at<uint16_t>(ws, w.h), s, di.sms));
+    launched();
+    return LMOE_OK;
+  }
+  if (experts_fused(d, w13_gs != nullptr)) {
+    FusedExpertArgs f{};
+    f.w13_q = w13_q;
+    f.w13_s = w13_s;
+    f.w2_q = w2_q;
+    f.w2_s = w2_s;
+    f.x_lat = x_lat;
+    f.groups = at<int4>(ws, w.groups);
+    f.n_groups = at<int32_t>(ws, w.n_groups);
+    f.sorted_rows = sorted_rows;
+    f.h = f.h_out = at<uint16_t>(ws, w.h);
+    f.y_out = y;
+    f.ssq_out = at<float>(ws, w.ssq);
+    f.ctr = at<int32_t>(ws, w.ctr);
+    f.st = st;
+    f.T = T;
+    f.latent = L;
+    f.inter = I;
+    f.top_k = k;
+    f.n_experts = d->n_experts;
+    f.rows = T * k;
+    f.early = groups_early ? 1 : 0;
+    if (nz) {
+      f.topk_idx = nz->topk_idx;
+      f.topk_w = nz->topk_w;
+      f.norm_g = nz->norm_g;
+      f.zb = at<uint16_t>(ws, w.pub.z);
+      f.eps = d->eps;
+      *nz->z_ready = true;
+    }
+    pre_launch(s, "expert_fused");
+    CHECK(launch_fused_experts(f, s, di.sms));
     launched();
     return LMOE_OK;
   }
@@ -433,11 +488,26 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   return LMOE_OK;
 }
 
+// z_ready: bf16(z) is already in the workspace (the persistent decode experts formed it)
 int run_combine_unpool(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const float* y,
                        const int32_t* topk_idx, const float* topk_w, const uint16_t* norm_g,
-                       const uint16_t* unpooler_w, uint16_t* out, void* ws, cudaStream_t s, bool ssq_ready) {
+                       const uint16_t* unpooler_w, uint16_t* out, void* ws, cudaStream_t s, bool ssq_ready,
+                       bool z_ready = false) {
   Status* st = at<Status>(ws, w.pub.status);
   uint16_t* zb = at<uint16_t>(ws, w.pub.z);
+  if (z_ready) {
+    if (d->T < t_dense_min_t) {
+      pre_launch(s, "unpool_gemv");
+      GemvArgs g{unpooler_w, zb, out, d->hidden, d->latent, d->T, st, kWaitAfterWeights};
+      CHECK(launch_gemv_bf16(g, s, di.sms));
+    } else {
+      pre_launch(s, "unpool_tc_gemm");
+      TcGemmArgs g{out, d->T, d->hidden, d->latent, st};
+      CHECK(launch_tc_gemm_bf16(g, zb, unpooler_w, s, di.sms));
+    }
+    launched();
+    return LMOE_OK;
+  }
   if (!ssq_ready) {
     const long long n = (long long)d->T * d->top_k * (d->latent / 32);
     LAUNCH(dim3((unsigned)((n + 7) / 8)), dim3(256), s, ssq_kernel, y, d->T * d->top_k, d->latent,
@@ -507,9 +577,11 @@ int run_layer(const lmoe_dims* d, const lmoe_weights* wt, const WsLayout& w, con
     CHECK(run_pool(d, di, x_pool, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
   }
   // (with the fork, the expert kernels follow the join: nothing may stream before their wait)
+  bool z_ready = false;
+  const NormSum nz{idx, tw, wt->norm_g, &z_ready};
   CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork,
-                    nv ? nv->w13_gs : nullptr, nv ? nv->w2_gs : nullptr));
-  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true));
+                    nv ? nv->w13_gs : nullptr, nv ? nv->w2_gs : nullptr, &nz));
+  CHECK(run_combine_unpool(d, w, di, y, idx, tw, wt->norm_g, wt->unpooler_w, out, ws, s, true, z_ready));
   return LMOE_OK;
 }
 
@@ -704,8 +776,11 @@ int lmoe_forward_routed(const lmoe_dims* d, const lmoe_weights* wt, const uint16
   } else {
     CHECK(run_pool(d, di, x, wt->pooler_w, x_lat, st, s, nullptr, nullptr, kWaitAtEnd));
   }
-  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork));
-  CHECK(run_combine_unpool(d, w, di, y, topk_idx, topk_w, wt->norm_g, wt->unpooler_w, out, ws, s, true));
+  bool z_ready = false;
+  const NormSum nz{topk_idx, topk_w, wt->norm_g, &z_ready};
+  CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork,
+                    nullptr, nullptr, &nz));
+  CHECK(run_combine_unpool(d, w, di, y, topk_idx, topk_w, wt->norm_g, wt->unpooler_w, out, ws, s, true, z_ready));
   return post_call(s, LMOE_OK);
 }
 
@@ -744,6 +819,8 @@ int lmoe_set_option(int key, int value) {
       return g_dense_min_t.exchange(value > 0 ? value : kDenseMinTokensDefault);
     case LMOE_OPT_EXPERT_TC_MIN_TOKENS:
       return g_expert_tc_min_t.exchange(value > 0 ? value : kExpertTcMinTokensDefault);
+    case LMOE_OPT_FUSED_MAX_TOKENS:
+      return g_fused_max_t.exchange(value >= 0 ? value : kFusedMaxTokensDefault);
     default:
       return LMOE_EINVAL;
   }

@@ -120,6 +120,45 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// device-wide counters: the CTAs of one launch (all resident at once) tell each
+// other that a stage's results are in global memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void counter_add_release(int32_t* c, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(c), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int counter_load_acquire(const int32_t* c) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+  return v;
+}
+
+// Bounded wait until *c >= target: by wall clock (kWaitLimitNs) and by an
+// iteration cap; on expiry records LMOE_ETIMEOUT at `where` and returns false.
+__device__ __forceinline__ bool counter_wait(const int32_t* c, int target, Status* st, int where) {
+  if (counter_load_acquire(c) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1; it < (1u << 26); ++it) {
+    __nanosleep(100);
+    if (counter_load_acquire(c) >= target) return true;
+    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) break;
+  }
+  set_error(st, LMOE_ETIMEOUT, where);
+  return false;
+}
+
+// Orders this thread's earlier generic-proxy accesses to global memory with
+// its later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Named barrier over the `nthreads` threads (whole warps) that use id `id`.
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // TMA bulk copy global -> shared, completion counted on `bar` (bytes).
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

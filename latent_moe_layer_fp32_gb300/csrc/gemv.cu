@@ -12,7 +12,8 @@
 // elements goes to warp c % W) and add their fp32 partials in warp order at
 // the end.  Per chunk the producer issues one TMA tensor copy of the weights
 // (a 3-D view {64 elements, rows, K/64} with 128-byte swizzle: 16 rows x 512
-// elements, 16 KB) and one of the token rows (tokens beyond T read as zero);
+// elements, 16 KB) and one of the token rows (min(8*NT, T) rows: at one token a
+// 1 KB box instead of 8 KB mostly zero-filled; tokens beyond T read as zero);
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) takes both operands by
 // ldmatrix from the swizzled boxes.
 #include "common.cuh"
@@ -46,6 +47,10 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
   const int ngroups = (a.T + GT - 1) / GT;
   const int mtiles = a.N / 16;
   const int n_items = mtiles * ngroups;
+  // token rows per box: the token group (8*NT), or T when fewer -- the MMA's columns past
+  // the last token read whatever the slot holds there and are never stored
+  const int xrows = min(GT, a.T);
+  const uint32_t xbytes = (uint32_t)xrows * kGemvKC * 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * D; ++i) {
@@ -85,7 +90,7 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
             const int d = seq[w]++;
             uint8_t* slot = smem + (w * D + d) * Lay::kSlot;
             uint64_t* bar = &full[w * D + d];
-            mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // token rows follow after the wait
+            mbar_arrive_expect_tx(bar, Lay::kW + xbytes);  // token rows follow after the wait
             tma_load_3d(slot, &tm_w, 0, (it % mtiles) * 16, c * (kGemvKC / 64), bar, pol);
             ++npre;
           }
@@ -113,7 +118,7 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar, Lay::kW + Lay::kA);  // out-of-range token rows are zero-filled, bytes still count
+            mbar_arrive_expect_tx(bar, Lay::kW + xbytes);  // out-of-range token rows are zero-filled, bytes still count
             tma_load_3d(slot, &tm_w, 0, mt * 16, c * (kGemvKC / 64), bar, pol);
           }
           tma_load_3d(slot + Lay::kW, &tm_x, 0, tg * GT, c * (kGemvKC / 64), bar, pol_x);
@@ -177,7 +182,10 @@ __global__ void __launch_bounds__(32 * (W + 1), 1)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(b0, b1, b2, b3, xbase + swz128(bk8 >> 3, GT, n * 8 + rr, bk8 & 7));
+          // line (plane * xrows + row) of the token box; the 128-byte swizzle XORs the 16-byte
+          // chunk with the line index (the box base is 1024-byte aligned)
+          const int xl = (bk8 >> 3) * xrows + n * 8 + rr;
+          ldmatrix_x4(b0, b1, b2, b3, xbase + (uint32_t)((xl << 7) + (((bk8 & 7) ^ (xl & 7)) << 4)));
           mma_bf16(acc[n], a0, a1, a2, a3, b0, b1);
           mma_bf16(acc[n], a4, a5, a6, a7, b2, b3);
         }
@@ -247,7 +255,7 @@ static int launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
   {
     const uint64_t dims[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
     const uint64_t strides[2] = {(uint64_t)a.K * 2, 128};
-    const uint32_t box[3] = {64, (uint32_t)(8 * NT), kGemvKC / 64};
+    const uint32_t box[3] = {64, (uint32_t)min(8 * NT, a.T), kGemvKC / 64};
     if (get_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.act, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return LMOE_ECUDA;
   }

@@ -75,6 +75,37 @@ int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int
 int launch_down(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms);
 int expert_max_group(int T);
 
+// ---- fused_experts.cu ------------------------------------------------------
+// Decode-size experts (T <= 8, T*k <= 64 route rows), MXFP4: gate/up + SwiGLU
+// and down in one persistent launch (one CTA per SM, a device-wide counter
+// between the two stages).
+struct FusedExpertArgs {
+  const uint8_t* w13_q;     // [E][2I][L/2]
+  const uint8_t* w13_s;     // [E][2I][L/32]
+  const uint8_t* w2_q;      // [E][L][I/2]
+  const uint8_t* w2_s;      // [E][L][I/32]
+  const uint16_t* x_lat;    // bf16 [T][L]
+  const int4* groups;       // group list {e, p0, n, 0}
+  const int32_t* n_groups;
+  const int32_t* sorted_rows;
+  uint16_t* h;              // bf16 [R][I] by sorted position (written, then read back)
+  uint16_t* h_out;          // = h
+  float* y_out;             // fp32 [R][L] by original row id
+  float* ssq_out;           // fp32 [R][L/32]
+  int32_t* ctr;             // [65] zero at launch: per-group counts of finished gate/up items, then
+                            // the number of CTAs done with their down items
+  Status* st;
+  // the layer's norm and weighted sum (null zb: the experts alone)
+  const int32_t* topk_idx;  // [T][k]
+  const float* topk_w;      // [T][k]
+  const uint16_t* norm_g;   // bf16 [E][L]
+  uint16_t* zb;             // out bf16 [T][L]
+  float eps;
+  int T, latent, inter, top_k, n_experts, rows;
+  int early;                // 1: the routing table was written before the preceding kernel ran
+};
+int launch_fused_experts(const FusedExpertArgs& a, cudaStream_t s, int num_sms);
+
 // ---- gemv.cu --------------------------------------------------------------
 // When the kernel waits for the preceding kernel of the stream (programmatic
 // dependent launch): before anything (0); after issuing the weight copies of its

@@ -12,8 +12,8 @@ import torch
 
 import oracle
 import synth
-from parity_util import (check_indices, check_out, device_weights, host_weights, router_regime, to_dev, to_host,
-                         ws_for, ws_view)
+from parity_util import (bf, check_indices, check_out, device_weights, host_weights, router_regime, to_dev,
+                         to_host, ws_for, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -136,4 +136,10 @@ def test_two_layer_stack_from_a_cuda_graph(lm, orc, name, T):
     lay = lm.lmoe_workspace_layout(dims)
     gidx2 = to_host(ws_view(ws[1], lay.topk_idx, torch.int32, (d.T, d.k)))
     assert np.array_equal(gidx2, ref2["topk_idx"]), "layer 2 routed differently from the oracle applied twice"
-    check_out(out_h, ref2["out"], "two layers against the oracle applied twice")
+    # two layers' errors add: the layer-2 input already differs from the oracle's by layer 1's
+    # rounding, so the element-wise bar is twice one layer's; the normwise and cosine bars stay
+    g, r = bf(out_h), bf(ref2["out"])
+    dd = g - r
+    assert np.abs(dd).max() / np.abs(r).max() <= 2e-2
+    assert float((g * r).sum() / (np.linalg.norm(g) * np.linalg.norm(r))) >= 0.9999
+    assert np.all(np.abs(dd) <= 4e-2 * (np.abs(r) + np.sqrt((r * r).mean())))

@@ -270,14 +270,15 @@ LMOE_API const char* lmoe_last_launch_name(int i);
  * an embedded runtime with a memory budget fixed at start-up).  The pages
  * have no counterpart: this is a deployment variant of lmoe_route.
  *   Same arguments and outputs as lmoe_route, minus ws/ws_bytes, and the same
- *   dimension rules (LMOE_EINVAL, LMOE_EUNSUPPORTED).  It always runs the
- *   CUDA-core router (fp32 FMA, split-K), so its results are bit-identical to
- *   lmoe_route's wherever lmoe_route runs that router too: below 64 tokens,
- *   or when n_experts is not a multiple of 32.  From 64 tokens with
- *   n_experts % 32 == 0, lmoe_route computes the logits on the tensor cores,
- *   which sums the same exact fp32 products in another order; the picks then
- *   agree except where two logits lie within that rounding of each other,
- *   and the weights agree to fp32 rounding.
+ *   dimension rules (LMOE_EINVAL, LMOE_EUNSUPPORTED).  It runs lmoe_route's
+ *   CUDA-core routers (fp32 FMA: the one-launch routing up to 16 tokens, the
+ *   split-K partials above), so its results are bit-identical to lmoe_route's
+ *   wherever lmoe_route runs those too: below 64 tokens, or when n_experts is
+ *   not a multiple of 32.  From 64 tokens with n_experts % 32 == 0, lmoe_route
+ *   computes the logits on the tensor cores, which sums the same exact fp32
+ *   products in another order; the picks then agree except where two logits
+ *   lie within that rounding of each other, and the weights agree to fp32
+ *   rounding.
  *   Its scratch is a fixed array inside the library (about 1.1 MB, held on
  *   every GPU that loads the library until the process exits), so it accepts
  *   at most T = 64 tokens and n_experts <= 256, and returns LMOE_ENOSCRATCH

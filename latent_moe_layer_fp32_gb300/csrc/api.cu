@@ -47,6 +47,11 @@ int check_dims(const lmoe_dims* d) {
   return LMOE_OK;
 }
 
+int fast_route_ks(int H) {
+  const int ks = H % 1024 == 0 ? 1024 : (H % 512 == 0 ? 512 : (H % 256 == 0 ? 256 : 0));
+  return (ks > 0 && H / ks <= 16) ? ks : 0;
+}
+
 int router_splits(int T, int E, int H, int sms, int max_split) {
   const int base = ((E + 31) / 32) * ((T + 7) / 8);
   int ns = 1;
@@ -151,6 +156,7 @@ int set_carveouts() {
   if (done >> (dev & 63) & 1ull) return LMOE_OK;
   const void* fns[] = {
       reinterpret_cast<const void*>(route_small_kernel), reinterpret_cast<const void*>(router_partial_kernel),
+      reinterpret_cast<const void*>(route_fast_kernel),
       reinterpret_cast<const void*>(topk_kernel),        reinterpret_cast<const void*>(table_kernel),
       reinterpret_cast<const void*>(topk_hist_kernel),   reinterpret_cast<const void*>(table_scan_kernel),
       reinterpret_cast<const void*>(table_scatter_kernel), reinterpret_cast<const void*>(table_hist_kernel),
@@ -287,7 +293,15 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
   Status* st = at<Status>(ws, w.pub.status);
   float* part = at<float>(ws, w.part);
   if (T <= 16) {
-    // one launch: router partials, then the last CTAs finish the routing
+    // one launch: router partials with every weight load in flight at once, then the last CTA
+    // finishes the routing
+    const int KS = fast_route_ks(H);
+    if (KS > 0) {
+      LAUNCH(dim3((E + 7) / 8, H / KS), dim3(256), s, route_fast_kernel, x, router_w, router_bias, part, T, H, E, k, KS,
+             group_rows(T), topk_idx, topk_w, offsets, sorted_rows, row_pos, at<int4>(ws, w.groups),
+             at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st, pre_g, rinv);
+      return LMOE_OK;
+    }
     LAUNCH(dim3((E + 31) / 32, (T + 7) / 8, w.nsplit), dim3(256), s, route_small_kernel, x, router_w, router_bias,
            part, T, H, E, k, H / w.nsplit, group_rows(T), topk_idx, topk_w, offsets, sorted_rows, row_pos,
            at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<int32_t>(ws, w.route_count), st, pre_g, rinv);

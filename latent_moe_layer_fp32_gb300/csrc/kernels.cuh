@@ -11,6 +11,8 @@ namespace lmoe {
 int check_dims(const lmoe_dims* d);
 // split-K factor of the CUDA-core router: enough CTAs for the GPU, at most max_split
 int router_splits(int T, int E, int H, int sms, int max_split);
+// K range per warp of route_fast_kernel (at most 16 ranges), or 0 when H does not allow it
+int fast_route_ks(int H);
 // per-call launch count and names (lmoe_last_launch_count / _name) and the optional
 // per-launch timing events (lmoe_profile_events)
 void calls_begin();
@@ -30,6 +32,10 @@ __global__ void route_small_kernel(const uint16_t* x, const float* wr, const flo
                                    int32_t* offsets, int32_t* sorted_rows, int32_t* row_pos, int4* groups,
                                    int32_t* n_groups, int32_t* tickets, Status* st, const uint16_t* g,
                                    const float* rinv);
+__global__ void route_fast_kernel(const uint16_t* x, const float* wr, const float* bias, float* part, int T, int H,
+                                  int E, int k, int KS, int G, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                                  int32_t* sorted_rows, int32_t* row_pos, int4* groups, int32_t* n_groups,
+                                  int32_t* tickets, Status* st, const uint16_t* g, const float* rinv);
 __global__ void router_split_kernel(const float* wr, int E, int H, uint16_t* w3, int dup);
 constexpr int kChunkTok = 32;  // tokens per chunk of the many-token routing table
 __global__ void topk_hist_kernel(const float* part, int nsplit, const float* bias, int T, int E, int k,

@@ -102,9 +102,19 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
   int32_t* n_groups = reinterpret_cast<int32_t*>(scratch + 16);
   float* part = reinterpret_cast<float*>(scratch + kStatusBytes);
   int4* groups = reinterpret_cast<int4*>(scratch + kStatusBytes + kPartBytes);
-  // the status word must start at zero; everything else is written before it is read
-  if (cudaMemsetAsync(st, 0, sizeof(Status), s) != cudaSuccess) return LMOE_ECUDA;
-  // the split rule of lmoe_route (at most 16 splits, which the scratch holds)
+  // the status word and the routing ticket must start at zero; everything else is written before it is read
+  if (cudaMemsetAsync(st, 0, 128, s) != cudaSuccess) return LMOE_ECUDA;
+  // lmoe_route's router for this T: the one-launch routing up to 16 tokens (its ticket counter
+  // sits in the zeroed status region), else the split-K partials (at most 16 splits, which the
+  // scratch holds) and the separate top-k and table kernels
+  const int KS = fast_route_ks(H);
+  if (T <= 16 && KS > 0) {
+    rc = launch(dim3((E + 7) / 8, H / KS), dim3(256), s, "route_fast_kernel", route_fast_kernel, x, router_w,
+                router_bias, part, T, H, E, k, KS, expert_max_group(T), topk_idx, topk_w, expert_offsets, sorted_rows,
+                row_pos, groups, n_groups, reinterpret_cast<int32_t*>(scratch + 64), st, (const uint16_t*)nullptr,
+                (const float*)nullptr);
+    return post_call(s, rc);
+  }
   const int ns = router_splits(T, E, H, sms, kNoAllocMaxSplit);
   rc = launch(dim3((E + 31) / 32, (T + 7) / 8, ns), dim3(256), s, "router_partial_kernel", router_partial_kernel, x,
               router_w, part, T, H, E, H / ns, (const uint16_t*)nullptr);

@@ -414,6 +414,139 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------
+// Small-T routing in one launch, all weight loads in flight at once.
+// Grid (ceil(E/8), nsplit): warp w of CTA (b, s) owns expert b*8 + w and the
+// K range [s*KS, (s+1)*KS) (KS = H/nsplit, a multiple of 128, at most 1024):
+// every lane issues its KS/128 16-byte weight loads before any arithmetic, so
+// the whole router matrix is requested in the first microseconds.  The CTA
+// stages its K range of up to four tokens at a time in shared memory (bf16)
+// and each lane keeps one fp32 FMA chain per token in element order; the warp
+// then adds its lanes in a fixed tree and stores the partial.  The last CTA to
+// finish (a ticket counter) sums every logit's partials in split order (times
+// rinv, + bias), selects the top k of every token (one warp per token) and
+// builds the table from the picks it holds in shared memory.
+// tickets[0] starts at zero.  Requires T <= 16 and nsplit <= 16.
+// ---------------------------------------------------------------------------
+constexpr int kFastKS = 1024;  // largest K range per warp: 8 loads of 16 bytes per lane
+constexpr int kFastTok = 4;    // tokens staged per pass
+
+struct FastRouteSmem {
+  union {
+    uint16_t xs[kFastTok][kFastKS];  // the CTA's K range of up to four tokens (bf16 bits)
+    struct {
+      float lg[16][256];             // last CTA: logits
+      int pick[16 * 8];
+      TableSmem<256> tab;
+    } tail;
+  };
+};
+
+__global__ void __launch_bounds__(256) route_fast_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                         const float* __restrict__ bias, float* __restrict__ part,
+                                                         int T, int H, int E, int k, int KS, int G,
+                                                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ sorted_rows,
+                                                         int32_t* __restrict__ row_pos, int4* __restrict__ groups,
+                                                         int32_t* __restrict__ n_groups, int32_t* tickets,
+                                                         Status* st, const uint16_t* __restrict__ g,
+                                                         const float* __restrict__ rinv) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ FastRouteSmem sm;
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp, split = blockIdx.y, k0 = split * KS;
+  const int nv = KS / 128;  // 16-byte weight loads per lane
+  // every weight load of this warp first
+  float4 w[kFastKS / 128];
+#pragma unroll
+  for (int i = 0; i < kFastKS / 128; ++i)
+    w[i] = (i < nv && e < E) ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)e * H + k0 + i * 128 + lane * 4))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t0 = 0; t0 < T; t0 += kFastTok) {
+    const int nt = min(kFastTok, T - t0);
+    __syncthreads();  // the previous pass's reads of the staging buffer are done
+    for (int u = threadIdx.x; u < nt * (KS / 8); u += blockDim.x) {
+      const int tt = u / (KS / 8), c = u % (KS / 8);
+      *reinterpret_cast<uint4*>(&sm.xs[tt][c * 8]) =
+          __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0 + c * 8));
+    }
+    __syncthreads();
+    float acc[kFastTok];
+#pragma unroll
+    for (int tt = 0; tt < kFastTok; ++tt) acc[tt] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kFastKS / 128; ++i) {
+      if (i < nv) {
+        const int kk = i * 128 + lane * 4;
+        float g4[4] = {1.f, 1.f, 1.f, 1.f};
+        if (g) {
+          const uint2 gv = __ldg(reinterpret_cast<const uint2*>(g + k0 + kk));
+          g4[0] = bf16_bits_to_f32(gv.x & 0xffffu);
+          g4[1] = bf16_bits_to_f32(gv.x >> 16);
+          g4[2] = bf16_bits_to_f32(gv.y & 0xffffu);
+          g4[3] = bf16_bits_to_f32(gv.y >> 16);
+        }
+#pragma unroll
+        for (int tt = 0; tt < kFastTok; ++tt) {
+          if (tt < nt) {
+            const uint2 xv = *reinterpret_cast<const uint2*>(&sm.xs[tt][kk]);
+            float x4[4] = {bf16_bits_to_f32(xv.x & 0xffffu), bf16_bits_to_f32(xv.x >> 16),
+                           bf16_bits_to_f32(xv.y & 0xffffu), bf16_bits_to_f32(xv.y >> 16)};
+            if (g) {  // exact products
+#pragma unroll
+              for (int c = 0; c < 4; ++c) x4[c] = __fmul_rn(x4[c], g4[c]);
+            }
+            float a = acc[tt];
+            a = fmaf(x4[0], w[i].x, a);
+            a = fmaf(x4[1], w[i].y, a);
+            a = fmaf(x4[2], w[i].z, a);
+            a = fmaf(x4[3], w[i].w, a);
+            acc[tt] = a;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kFastTok; ++tt) {
+      const float v = warp_sum(acc[tt]);
+      if (lane == 0 && tt < nt && e < E) part[((size_t)split * T + t0 + tt) * E + e] = v;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's partials before its ticket
+    s_last = (atomicAdd(&tickets[0], 1) == (int)(gridDim.x * gridDim.y) - 1);
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // last CTA: logits (splits in order, times rinv, + bias), top k, table
+  const int nsplit = gridDim.y;
+  if ((int)threadIdx.x < E) {
+    const int ee = threadIdx.x;
+    for (int t = 0; t < T; ++t) {
+      float v[16];
+#pragma unroll
+      for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? __ldcg(part + ((size_t)sp * T + t) * E + ee) : 0.f;
+      float a = v[0];
+#pragma unroll
+      for (int sp = 1; sp < 16; ++sp)
+        if (sp < nsplit) a += v[sp];
+      if (rinv) a = __fmul_rn(a, rinv[t]);
+      if (bias) a = a + bias[ee];
+      sm.tail.lg[t][ee] = a;
+    }
+  }
+  __syncthreads();
+  for (int t = warp; t < T; t += 8)
+    topk_one_token(sm.tail.lg[t], E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k, lane, sm.tail.pick + t * k);
+  __syncthreads();
+  build_table<256>(sm.tail.pick, T * k, E, G, offsets, sorted_rows, row_pos, groups, n_groups, st, sm.tail.tab);
+}
+
+// ---------------------------------------------------------------------------
 // Router weights for the tensor-core router: w = w1 + w2 + w3 exactly, each a
 // bf16 holding the next 8 significant bits of the fp32 value (w1, w2 by
 // truncation, w3 by rounding the last 8 bits, which it holds exactly for any

@@ -79,8 +79,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int tiles = L / 32;
   if (warp < k) {
     const int r = t * k + warp;
+    // every load of the lane first (up to 8 of its tiles), then the sum in tile order
     float s = 0.f;
-    for (int i = lane; i < tiles; i += 32) s += ssq[(size_t)r * tiles + i];
+    for (int i0 = lane; i0 < tiles; i0 += 32 * 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (i0 + 32 * u < tiles) ? ssq[(size_t)r * tiles + i0 + 32 * u] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + 32 * u < tiles) s += v[u];
+    }
     s = warp_sum(s);
     if (lane == 0) {
       int e = topk_idx[r];
@@ -97,12 +105,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int span = L / gridDim.y, c_end = (blockIdx.y + 1) * span;
   for (int l = blockIdx.y * span + 4 * tid; l < c_end; l += 4 * 256) {
     float z[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const float4 yv = __ldcs(reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * L + l));
-      const uint2 gw = *reinterpret_cast<const uint2*>(norm_g + (size_t)s_e[j] * L + l);
-      const float yy[4] = {yv.x, yv.y, yv.z, yv.w};
-      const float gg[4] = {bf16_bits_to_f32(gw.x & 0xFFFFu), bf16_bits_to_f32(gw.x >> 16),
-                           bf16_bits_to_f32(gw.y & 0xFFFFu), bf16_bits_to_f32(gw.y >> 16)};
+    // every route's y and gain loads first (k <= 8), then the sum in route order
+    float4 yv[8];
+    uint2 gw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k) {
+        yv[j] = __ldcs(reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * L + l));
+        gw[j] = *reinterpret_cast<const uint2*>(norm_g + (size_t)s_e[j] * L + l);
+      }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= k) break;
+      const float yy[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+      const float gg[4] = {bf16_bits_to_f32(gw[j].x & 0xFFFFu), bf16_bits_to_f32(gw[j].x >> 16),
+                           bf16_bits_to_f32(gw[j].y & 0xFFFFu), bf16_bits_to_f32(gw[j].y >> 16)};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float yh = __fmul_rn(__fmul_rn(yy[q], s_rinv[j]), gg[q]);

@@ -313,18 +313,10 @@ def run_stage(args, d, name, lm, dev):
             call()
         n = lm.lmoe_last_launch_count()
         names = [lm.lmoe_last_launch_name(j) for j in range(n)]
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         per = [[] for _ in range(n)]
-        lm.lmoe_profile_events(evs)
-        try:
-            for _ in range(args.steps):
-                flush.zero_()
-                call()
-                torch.cuda.synchronize()
-                for j in range(n):
-                    per[j].append(evs[j].elapsed_time(evs[j + 1]))
-        finally:
-            lm.lmoe_profile_events(None)
+        for _ in range(args.steps):
+            for j, v in enumerate(per_launch_ms(lm, call, n, 1, flush)):
+                per[j] += v
         rc = lm.lmoe_status_check(ws)
         if rc != 0:
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")
@@ -404,7 +396,7 @@ def time_steps(call, steps, flush):
 def per_launch_ms(lm, call, n_launch, reps, flush):
     """Mean device time of each kernel launch of one call (CUDA events between launches)."""
     import torch
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launch)]
     per = [[] for _ in range(n_launch)]
     lm.lmoe_profile_events(evs)
     try:
@@ -412,8 +404,8 @@ def per_launch_ms(lm, call, n_launch, reps, flush):
             flush.zero_()
             call()
             torch.cuda.synchronize()
-            for j in range(n_launch):
-                per[j].append(evs[j].elapsed_time(evs[j + 1]))
+            for j in range(n_launch):  # events 2j, 2j+1 bracket launch j on its own stream
+                per[j].append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
     finally:
         lm.lmoe_profile_events(None)
     return per
@@ -669,19 +661,8 @@ def main():
                                           sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / 1e3)
 
         # ---- dominant kernel, per-launch events ----
-        nev = launches_per_step + 1
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
-        per_launch = [[] for _ in range(launches_per_step)]
-        lm.lmoe_profile_events(evs)
-        try:
-            for i in range(max(5, min(args.steps, 20))):
-                flush.zero_()
-                forward(x_dev, out)
-                torch.cuda.synchronize()
-                for j in range(launches_per_step):
-                    per_launch[j].append(evs[j].elapsed_time(evs[j + 1]))
-        finally:
-            lm.lmoe_profile_events(None)
+        per_launch = per_launch_ms(lm, lambda: forward(x_dev, out), launches_per_step,
+                                   max(5, min(args.steps, 20)), flush)
         rc = lm.lmoe_status_check(ws)
         if rc != 0:
             raise RuntimeError(f"device status {rc}: {lm.lmoe_error_string(rc)}")

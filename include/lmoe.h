@@ -296,11 +296,15 @@ LMOE_API int lmoe_route_noalloc(const lmoe_dims* dims, const uint16_t* x, const 
                                 lmoe_stream_t stream);
 
 /* Optional per-launch timing: while set, every kernel launch i of the
- * following lmoe_* calls on this host thread is preceded by
- * cudaEventRecord(events[i], stream), and the end of each call records
- * events[launches] (as far as n allows).  `events` holds cudaEvent_t handles
- * owned by the caller; pass n = 0 to switch off.  Recording events between
- * launches serialises the kernels, so use it only to time kernels. */
+ * following lmoe_* calls on this host thread is bracketed by
+ * cudaEventRecord(events[2i]) before it and cudaEventRecord(events[2i + 1])
+ * after it, both on the stream that launch runs on (as far as n allows), so
+ * the device time of launch i is the time between events 2i and 2i + 1.
+ * Above 16 tokens a call runs its routing launches on a second stream beside
+ * the pooler, so events of different launches need not be ordered.
+ * `events` holds cudaEvent_t handles owned by the caller; pass n = 0 to switch
+ * off.  Recording events between launches serialises the kernels of one
+ * stream, so use it only to time kernels. */
 LMOE_API int lmoe_profile_events(void* const* events, int n);
 
 /* Regime switches (process-wide; they apply to calls issued after the

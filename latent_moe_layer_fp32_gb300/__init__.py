@@ -295,7 +295,8 @@ _event_array = None
 
 
 def lmoe_profile_events(events):
-    """Record events[i] before launch i of the following calls (None to stop).
+    """Bracket launch i of the following calls with events[2i] (before) and
+    events[2i + 1] (after), both on that launch's stream (None to stop).
     `events` are torch.cuda.Event(enable_timing=True) objects."""
     global _event_array
     if not events:

@@ -16,20 +16,21 @@ constexpr int kMaxNamed = 32;
 thread_local const char* g_names[kMaxNamed];
 thread_local void* const* g_events = nullptr;
 thread_local int g_nevents = 0;
+thread_local cudaStream_t g_cur_stream = nullptr;  // the stream of the launch being issued
 
 void calls_begin() { g_launches = 0; }
 
 void pre_launch(cudaStream_t s, const char* name) {
   if (g_launches < kMaxNamed) g_names[g_launches] = name;
-  if (g_events && g_launches < g_nevents) cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
+  g_cur_stream = s;
+  if (g_events && 2 * g_launches + 1 < g_nevents)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_events[2 * g_launches]), s);
 }
 
-void launched() { ++g_launches; }
-
-int post_call(cudaStream_t s, int rc) {
-  if (rc == LMOE_OK && g_events && g_launches < g_nevents)
-    cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_launches]), s);
-  return rc;
+void launched() {
+  if (g_events && 2 * g_launches + 1 < g_nevents)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_events[2 * g_launches + 1]), g_cur_stream);
+  ++g_launches;
 }
 
 int check_dims(const lmoe_dims* d) {
@@ -631,8 +632,8 @@ int lmoe_route(const lmoe_dims* d, const uint16_t* x, const float* router_w, con
   if (!aligned16(x) || !aligned16(router_w) || !topk_idx || !topk_w || !expert_offsets || !sorted_rows ||
       !row_pos || (router_bias && !aligned16(router_bias)))
     return LMOE_EINVAL;
-  return post_call(s, run_route(d, w, di, x, router_w, router_bias, topk_idx, topk_w, expert_offsets, sorted_rows,
-                                row_pos, ws, s));
+  return run_route(d, w, di, x, router_w, router_bias, topk_idx, topk_w, expert_offsets, sorted_rows,
+                                row_pos, ws, s);
 }
 
 int lmoe_pool(const lmoe_dims* d, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat, void* ws,
@@ -643,7 +644,7 @@ int lmoe_pool(const lmoe_dims* d, const uint16_t* x, const uint16_t* pooler_w, u
   CHECK(prologue(d, ws, ws_bytes, &di, &w, s, ws != nullptr));
   if (!aligned16(x) || !aligned16(pooler_w) || !aligned16(x_lat) || !x || !pooler_w || !x_lat) return LMOE_EINVAL;
   Status* st = ws ? at<Status>(ws, w.pub.status) : nullptr;
-  return post_call(s, run_pool(d, di, x, pooler_w, x_lat, st, s));
+  return run_pool(d, di, x, pooler_w, x_lat, st, s);
 }
 
 int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
@@ -659,7 +660,7 @@ int lmoe_experts_mxfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t*
   const int R = d->T * d->top_k;
   LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
          group_rows(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
-  return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s));
+  return run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s);
 }
 
 int lmoe_norm_combine_unpool(const lmoe_dims* d, const float* y, const int32_t* topk_idx, const float* topk_w,
@@ -672,7 +673,7 @@ int lmoe_norm_combine_unpool(const lmoe_dims* d, const float* y, const int32_t* 
   const void* ptrs[] = {y, topk_idx, topk_w, norm_g, unpooler_w, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return LMOE_EINVAL;
-  return post_call(s, run_combine_unpool(d, w, di, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, s, false));
+  return run_combine_unpool(d, w, di, y, topk_idx, topk_w, norm_g, unpooler_w, out, ws, s, false);
 }
 
 int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, uint16_t* out, void* ws,
@@ -684,7 +685,7 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   if (!x || !out || !aligned16(x) || !aligned16(out)) return LMOE_EINVAL;
   CHECK(check_weights(wt));
   CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s));
-  return post_call(s, LMOE_OK);
+  return LMOE_OK;
 }
 
 int lmoe_forward_nvfp4(const lmoe_dims* d, const lmoe_weights* wt, const lmoe_nvfp4_scales* nv, const uint16_t* x,
@@ -696,7 +697,7 @@ int lmoe_forward_nvfp4(const lmoe_dims* d, const lmoe_weights* wt, const lmoe_nv
   if (!x || !out || !aligned16(x) || !aligned16(out) || !nv || !nv->w13_gs || !nv->w2_gs) return LMOE_EINVAL;
   CHECK(check_weights(wt));
   CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s, nv));
-  return post_call(s, LMOE_OK);
+  return LMOE_OK;
 }
 
 int lmoe_experts_nvfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t* expert_offsets,
@@ -714,8 +715,8 @@ int lmoe_experts_nvfp4(const lmoe_dims* d, const uint16_t* x_lat, const int32_t*
   const int R = d->T * d->top_k;
   LAUNCH(dim3(1), dim3(256), s, groups_from_offsets_kernel, expert_offsets, sorted_rows, d->n_experts, R,
          group_rows(d->T), at<int4>(ws, w.groups), at<int32_t>(ws, w.n_groups), at<Status>(ws, w.pub.status));
-  return post_call(s, run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s, false, false,
-                                  w13_gs, w2_gs));
+  return run_experts(d, w, di, x_lat, sorted_rows, w13_q, w13_s, w2_q, w2_s, y, ws, s, false, false,
+                                  w13_gs, w2_gs);
 }
 
 size_t lmoe_block_workspace_bytes(const lmoe_dims* d) {
@@ -746,7 +747,7 @@ int lmoe_block_forward(const lmoe_dims* d, const lmoe_weights* wt, const lmoe_bl
   CHECK(run_layer(d, wt, w, di, x, nb, nm->pre_g, rinv, usplit, lout, ws, s));
   // post-norm of the layer's output and the residual
   LAUNCH(dim3(T), dim3(256), s, postnorm_residual_kernel, (const uint16_t*)lout, x, nm->post_g, nm->eps, H, y);
-  return post_call(s, LMOE_OK);
+  return LMOE_OK;
 }
 
 int lmoe_forward_routed(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, const int32_t* topk_idx,
@@ -795,7 +796,7 @@ int lmoe_forward_routed(const lmoe_dims* d, const lmoe_weights* wt, const uint16
   CHECK(run_experts(d, w, di, x_lat, srows, wt->w13_q, wt->w13_s, wt->w2_q, wt->w2_s, y, ws, s, false, !fork,
                     nullptr, nullptr, &nz));
   CHECK(run_combine_unpool(d, w, di, y, topk_idx, topk_w, wt->norm_g, wt->unpooler_w, out, ws, s, true, z_ready));
-  return post_call(s, LMOE_OK);
+  return LMOE_OK;
 }
 
 int lmoe_status_check(const void* ws, lmoe_stream_t stream) {

@@ -18,7 +18,6 @@ int fast_route_ks(int H);
 void calls_begin();
 void pre_launch(cudaStream_t s, const char* name);
 void launched();
-int post_call(cudaStream_t s, int rc);
 
 // ---- route.cu -------------------------------------------------------------
 // g (optional): the sandwich block's pre-norm gain, the router input becomes x * g;

@@ -113,7 +113,7 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
                 router_bias, part, T, H, E, k, KS, expert_max_group(T), topk_idx, topk_w, expert_offsets, sorted_rows,
                 row_pos, groups, n_groups, reinterpret_cast<int32_t*>(scratch + 64), st, (const uint16_t*)nullptr,
                 (const float*)nullptr);
-    return post_call(s, rc);
+    return rc;
   }
   const int ns = router_splits(T, E, H, sms, kNoAllocMaxSplit);
   rc = launch(dim3((E + 31) / 32, (T + 7) / 8, ns), dim3(256), s, "router_partial_kernel", router_partial_kernel, x,
@@ -124,5 +124,5 @@ extern "C" LMOE_API int lmoe_route_noalloc(const lmoe_dims* d, const uint16_t* x
   if (rc == LMOE_OK)
     rc = launch(dim3(1), dim3(1024), s, "table_kernel", table_kernel, (const int32_t*)topk_idx, T * k, E,
                 expert_max_group(T), expert_offsets, sorted_rows, row_pos, groups, n_groups, st);
-  return post_call(s, rc);
+  return rc;
 }

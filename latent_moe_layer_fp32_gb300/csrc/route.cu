@@ -99,71 +99,80 @@ __global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __r
 // logit[e] = sum over splits in order (+ bias); candidates e = lane + 32*i.
 // Ties go to the lower expert index.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// A 64-bit key per logit whose unsigned order is the selection order: the
+// float's bits mapped to an order-preserving unsigned value (sign bit set for
+// non-negative values, all bits flipped for negative ones) above the bit-
+// inverted expert index, so that equal logits rank the lower index first.
+// v + 0 turns -0 into +0 (the two compare equal as floats).  Key 0 marks an
+// absent slot; every finite or infinite logit has a larger key.  A NaN logit
+// ranks above every number: logits are expected to be finite.
+__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
+  unsigned u = __float_as_uint(__fadd_rn(v, 0.0f));
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | static_cast<unsigned>(~e);
+}
+
+__device__ __forceinline__ float topk_key_value(unsigned hi) {
+  return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7fffffffu) : ~hi);
+}
+
+__device__ __forceinline__ void key_cx(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
 }
 
 // Top-k of one token by one warp, logits lg_s[0..E) in shared memory.
 // Writes topk_idx[k], topk_w[k] for the token (softmax over all E,
 // renormalised over the k picks; ties to the lower expert index).
+// Lane l holds experts l, l+32, ..., l+224, sorts its eight keys (a 19-
+// comparator network), and each pick is one warp-wide maximum over the lanes'
+// leading keys (the high words, then the low words of the lanes that reach
+// the maximum), after which the owning lane drops its leading key.
 __device__ __forceinline__ void topk_one_token(const float* lg_s, int E, int k, int32_t* topk_idx, float* topk_w,
                                                int lane, int* s_pick = nullptr) {
-  float lg[8];
-  bool taken[8];
+  unsigned long long q[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    lg[i] = e < E ? lg_s[e] : -INFINITY;
-    taken[i] = (e >= E);
+    q[i] = e < E ? topk_key(lg_s[e], e) : 0ull;
   }
-  float mx = -INFINITY;
+  key_cx(q[0], q[2]); key_cx(q[1], q[3]); key_cx(q[4], q[6]); key_cx(q[5], q[7]);
+  key_cx(q[0], q[4]); key_cx(q[1], q[5]); key_cx(q[2], q[6]); key_cx(q[3], q[7]);
+  key_cx(q[0], q[1]); key_cx(q[2], q[3]); key_cx(q[4], q[5]); key_cx(q[6], q[7]);
+  key_cx(q[2], q[4]); key_cx(q[3], q[5]);
+  key_cx(q[1], q[4]); key_cx(q[3], q[6]);
+  key_cx(q[1], q[2]); key_cx(q[3], q[4]); key_cx(q[5], q[6]);
+  float mx = 0.f, v = 0.f;
+  int e = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx = fmaxf(mx, lg[i]);
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const unsigned hi = static_cast<unsigned>(q[0] >> 32), lo = static_cast<unsigned>(q[0]);
+      const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+      const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+      const int ej = static_cast<int>(~ml);
+      const float vj = topk_key_value(mh);
+      if (j == 0) mx = vj;  // the largest logit
+      if (lane == j) {
+        v = vj;
+        e = ej;
+      }
+      if (lane == (ej & 31)) {  // the owner drops its leading key
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sel_p[8];
-  int sel_e[8];
+        for (int i = 0; i < 7; ++i) q[i] = q[i + 1];
+        q[7] = 0ull;
+      }
+    }
+  }
+  // softmax over the picks, summed in pick order
+  const float p = lane < k ? expf(v - mx) : 0.f;
   float den = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    sel_p[j] = 0.f;
-    sel_e[j] = 0;
-    if (j < k) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (!taken[i] && (bi == 0x7fffffff || better(lg[i], e, bv, bi))) {
-          bv = lg[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (lane + 32 * i == bi) taken[i] = true;
-      sel_e[j] = bi;
-      sel_p[j] = expf(bv - mx);
-      den += sel_p[j];
-    }
+    const float pj = __shfl_sync(0xffffffffu, p, j);
+    if (j < k) den += pj;
   }
-  float p = 0.f;
-  int e = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (j == lane) {
-      p = sel_p[j];
-      e = sel_e[j];
-    }
   if (lane < k) {
     topk_idx[lane] = e;
     topk_w[lane] = p / den;
@@ -441,6 +450,34 @@ struct FastRouteSmem {
   };
 };
 
+// Logits of expert ee for every token from the split partials: the partials of
+// TC tokens (NS >= nsplit splits each) are all loaded before any is summed;
+// each logit sums its splits in split order, then times rinv, then + bias.
+template <int TC, int NS>
+__device__ __forceinline__ void tail_logits(const float* part, int nsplit, int T, int E, int ee,
+                                            const float* bias, const float* rinv, float (*lg)[256]) {
+  for (int t0 = 0; t0 < T; t0 += TC) {
+    float v[TC][NS];
+#pragma unroll
+    for (int tt = 0; tt < TC; ++tt)
+#pragma unroll
+      for (int sp = 0; sp < NS; ++sp)
+        v[tt][sp] = (t0 + tt < T && sp < nsplit) ? __ldcg(part + ((size_t)sp * T + t0 + tt) * E + ee) : 0.f;
+#pragma unroll
+    for (int tt = 0; tt < TC; ++tt) {
+      if (t0 + tt < T) {
+        float a = v[tt][0];
+#pragma unroll
+        for (int sp = 1; sp < NS; ++sp)
+          if (sp < nsplit) a += v[tt][sp];
+        if (rinv) a = __fmul_rn(a, rinv[t0 + tt]);
+        if (bias) a = a + bias[ee];
+        lg[t0 + tt][ee] = a;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) route_fast_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                                                          const float* __restrict__ bias, float* __restrict__ part,
                                                          int T, int H, int E, int k, int KS, int G,
@@ -523,21 +560,11 @@ __global__ void __launch_bounds__(256) route_fast_kernel(const uint16_t* __restr
   __syncthreads();
   if (!s_last) return;
   // last CTA: logits (splits in order, times rinv, + bias), top k, table
-  const int nsplit = gridDim.y;
   if ((int)threadIdx.x < E) {
-    const int ee = threadIdx.x;
-    for (int t = 0; t < T; ++t) {
-      float v[16];
-#pragma unroll
-      for (int sp = 0; sp < 16; ++sp) v[sp] = sp < nsplit ? __ldcg(part + ((size_t)sp * T + t) * E + ee) : 0.f;
-      float a = v[0];
-#pragma unroll
-      for (int sp = 1; sp < 16; ++sp)
-        if (sp < nsplit) a += v[sp];
-      if (rinv) a = __fmul_rn(a, rinv[t]);
-      if (bias) a = a + bias[ee];
-      sm.tail.lg[t][ee] = a;
-    }
+    if (gridDim.y <= 8)
+      tail_logits<4, 8>(part, gridDim.y, T, E, threadIdx.x, bias, rinv, sm.tail.lg);
+    else
+      tail_logits<2, 16>(part, gridDim.y, T, E, threadIdx.x, bias, rinv, sm.tail.lg);
   }
   __syncthreads();
   for (int t = warp; t < T; t += 8)

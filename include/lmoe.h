@@ -323,14 +323,24 @@ LMOE_API int lmoe_profile_events(void* const* events, int n);
  *    64 route rows) the MXFP4 experts run as one persistent launch: gate/up +
  *    SwiGLU, a device-wide hand-off, then down, with the weight stream kept
  *    going across the hand-off; above it (or with value 0), as two
- *    weight-streaming launches.  Default 8.
+ *    weight-streaming launches.  Default 0 (off: measured no faster).
+ *  LMOE_OPT_DOWN_Z_MAX_TOKENS: up to this many tokens (and at most 64 route
+ *    rows) the streaming down launch also applies the post-expert norm and
+ *    forms the weighted sum z, after a device-wide count of its CTAs; above
+ *    it (or with value 0), a separate combine launch does.  The two give
+ *    bit-identical z (same arithmetic, same order).  Default 1.
  *
  * Both implementations of a stage give bf16 (or fp32) of an fp32 sum per
  * output and differ only in the order of that sum.  value <= 0 restores the
- * default (for LMOE_OPT_FUSED_MAX_TOKENS, value < 0 does and 0 switches the
- * persistent launch off).  Returns the previous value, or LMOE_EINVAL for an
- * unknown key. */
-enum { LMOE_OPT_DENSE_MIN_TOKENS = 1, LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2, LMOE_OPT_FUSED_MAX_TOKENS = 3 };
+ * default (for LMOE_OPT_FUSED_MAX_TOKENS and LMOE_OPT_DOWN_Z_MAX_TOKENS,
+ * value < 0 does and 0 switches the in-launch form off).  Returns the
+ * previous value, or LMOE_EINVAL for an unknown key. */
+enum {
+  LMOE_OPT_DENSE_MIN_TOKENS = 1,
+  LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2,
+  LMOE_OPT_FUSED_MAX_TOKENS = 3,
+  LMOE_OPT_DOWN_Z_MAX_TOKENS = 4
+};
 LMOE_API int lmoe_set_option(int key, int value);
 
 /* Failure-detection self-check: enqueues one kernel whose single thread waits

@@ -281,6 +281,7 @@ def lmoe_last_launch_name(i: int) -> str | None:
 LMOE_OPT_DENSE_MIN_TOKENS = 1
 LMOE_OPT_EXPERT_TC_MIN_TOKENS = 2
 LMOE_OPT_FUSED_MAX_TOKENS = 3
+LMOE_OPT_DOWN_Z_MAX_TOKENS = 4
 
 
 def lmoe_set_option(key: int, value: int) -> int:

@@ -70,18 +70,26 @@ constexpr int kDenseMinTokensDefault = 64;
 constexpr int kExpertTcMinTokensDefault = 352;
 // decode sizes: gate/up and down in one persistent launch up to this many tokens
 constexpr int kFusedMaxTokensDefault = 0;
+// the post-expert norm and weighted sum inside the down launch up to this many tokens; measured
+// on GB300 against the separate combine launch: the same step time at T = 1 (99.7 against 99.0 us,
+// within the run-to-run spread), about 2 us slower at T = 4 and 8 (the down CTAs hold their SMs
+// through the z step, so the unpooler's CTAs start later)
+constexpr int kDownZMaxTokensDefault = 1;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
 std::atomic<int> g_fused_max_t{kFusedMaxTokensDefault};
+std::atomic<int> g_downz_max_t{kDownZMaxTokensDefault};
 // the options as read once at the start of the current call on this thread, so
 // that every decision inside one call sees the same regime
 thread_local int t_dense_min_t = kDenseMinTokensDefault;
 thread_local int t_expert_tc_min_t = kExpertTcMinTokensDefault;
 thread_local int t_fused_max_t = kFusedMaxTokensDefault;
+thread_local int t_downz_max_t = kDownZMaxTokensDefault;
 void snapshot_options() {
   t_dense_min_t = g_dense_min_t.load(std::memory_order_relaxed);
   t_expert_tc_min_t = g_expert_tc_min_t.load(std::memory_order_relaxed);
   t_fused_max_t = g_fused_max_t.load(std::memory_order_relaxed);
+  t_downz_max_t = g_downz_max_t.load(std::memory_order_relaxed);
 }
 
 // the router as a tensor-core GEMM: above the fused small-T routing, from the
@@ -95,6 +103,8 @@ bool experts_tc(int T) { return T >= t_expert_tc_min_t; }
 bool experts_fused(const lmoe_dims* d, bool nvfp4) {
   return !nvfp4 && !experts_tc(d->T) && d->T <= t_fused_max_t && d->T <= 8 && d->T * d->top_k <= 64;
 }
+// the streaming down kernel also forms z: at most 64 route rows
+bool down_forms_z(const lmoe_dims* d) { return d->T <= t_downz_max_t && d->T * d->top_k <= 64; }
 // rows per group of the routing table: what the expert kernels of this regime consume
 int group_rows(int T) { return experts_tc(T) ? kTcExpertGroup : expert_max_group(T); }
 
@@ -497,6 +507,16 @@ int run_experts(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const 
   a.y_out = y;
   a.ssq_out = at<float>(ws, w.ssq);
   a.early = 1;  // the gate/up kernel waited for whatever wrote the group list
+  if (nz && down_forms_z(d)) {
+    a.zb = at<uint16_t>(ws, w.pub.z);
+    a.topk_idx = nz->topk_idx;
+    a.topk_w = nz->topk_w;
+    a.norm_g = nz->norm_g;
+    a.zctr = at<int32_t>(ws, w.ctr) + 64;
+    a.eps = d->eps;
+    a.T = T;
+    *nz->z_ready = true;
+  }
   pre_launch(s, "expert_down");
   CHECK(launch_down(a, T, G, s, di.sms));
   launched();
@@ -836,6 +856,8 @@ int lmoe_set_option(int key, int value) {
       return g_expert_tc_min_t.exchange(value > 0 ? value : kExpertTcMinTokensDefault);
     case LMOE_OPT_FUSED_MAX_TOKENS:
       return g_fused_max_t.exchange(value >= 0 ? value : kFusedMaxTokensDefault);
+    case LMOE_OPT_DOWN_Z_MAX_TOKENS:
+      return g_downz_max_t.exchange(value >= 0 ? value : kDownZMaxTokensDefault);
     default:
       return LMOE_EINVAL;
   }

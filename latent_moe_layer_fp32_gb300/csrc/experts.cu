@@ -251,6 +251,100 @@ struct Smem {
   static __host__ __device__ int bytes(int K, int D) { return D * Lay::kSlot + fixed(K) + 1024; }
 };
 
+// Down at decode sizes: the post-expert norm and the fp32 weighted sum in the
+// same launch ("Muse Spark Open on Gaudi 2", "The latent MoE: A' with a
+// per-expert norm").  Once every CTA has counted itself done (its y rows and
+// their per-tile sums of squares written; a device-wide counter, bounded
+// wait), CTA b forms z for the 32-column slices b, b + gridDim, ... of the
+// latent width, one token per calling warp:
+//   rinv[r] = 1/sqrt(sum of row r's tile sums (tile order) / L + eps),
+//   z[t][l] = sum over j in order of w[t][j] * ((y[t*k+j][l] * rinv) * g[e][l]),
+// the same arithmetic in the same order as combine_kernel.  The routes'
+// experts, weights and gains (ready since the routing) are read before the
+// wait; after it, one round of loads brings the rows' tile sums and y.
+// `wid` numbers the calling warps 0..NW-1; `scratch` is shared memory no
+// other warp still uses.
+template <int NW>
+__device__ void down_z_step(const ExpertArgs& a, float* scratch, int wid, int lane) {
+  const int L = a.latent, k = a.top_k, tiles = L / kRows, nsl = L / 32;
+  if ((int)blockIdx.x >= nsl) return;  // no slice here (CTA-uniform)
+  int* s_ok = reinterpret_cast<int*>(scratch);
+  // the first token's routes and its gains in the first slice, before the wait
+  int er[8];
+  float wr[8], g0[8];
+  auto routes = [&](int t) {
+    int e = 0;
+    float wv = 0.f;
+    if (lane < k) {
+      e = a.topk_idx[t * k + lane];
+      if (e < 0 || e >= a.n_experts) {
+        set_error(a.st, LMOE_EDEVICE_CHECK, 103);
+        e = 0;
+      }
+      wv = a.topk_w[t * k + lane];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      er[j] = __shfl_sync(0xffffffffu, e, j);
+      wr[j] = __shfl_sync(0xffffffffu, wv, j);
+    }
+  };
+  if (wid < a.T) {
+    routes(wid);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      g0[j] = j < k ? bf16_bits_to_f32(a.norm_g[(size_t)er[j] * L + blockIdx.x * 32 + lane]) : 0.f;
+  }
+  named_bar(1, NW * 32);  // every calling warp is past its last use of the scratch
+  if (wid == 0 && lane == 0) *s_ok = counter_wait(a.zctr, gridDim.x, a.st, 60) ? 1 : 0;
+  named_bar(1, NW * 32);
+  if (!*s_ok) return;
+  for (int t = wid; t < a.T; t += NW) {
+    if (t != wid) routes(t);
+    // every tile sum of the token's k rows and their y in the first slice, then the sums
+    float v[8][8], yv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = t * k + j;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[j][u] = (j < k && lane + 32 * u < tiles) ? __ldcg(a.ssq_out + (size_t)r * tiles + lane + 32 * u) : 0.f;
+      yv[j] = j < k ? __ldcg(a.y_out + (size_t)r * L + blockIdx.x * 32 + lane) : 0.f;
+    }
+    float rinv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float sq = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (lane + 32 * u < tiles) sq += v[j][u];
+      sq = warp_sum(sq);
+      rinv[j] = 1.0f / sqrtf(sq / (float)L + a.eps);
+    }
+    for (int sl = blockIdx.x; sl < nsl; sl += gridDim.x) {
+      const int l = sl * 32 + lane;
+      float gv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (sl == (int)blockIdx.x && t == wid) {
+          gv[j] = g0[j];
+        } else {
+          gv[j] = j < k ? bf16_bits_to_f32(a.norm_g[(size_t)er[j] * L + l]) : 0.f;
+          if (j < k && sl != (int)blockIdx.x) yv[j] = __ldcg(a.y_out + ((size_t)t * k + j) * L + l);
+        }
+      }
+      float z = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        const float yh = __fmul_rn(__fmul_rn(yv[j], rinv[j]), gv[j]);
+        z = __fadd_rn(z, __fmul_rn(wr[j], yh));
+      }
+      a.zb[(size_t)t * L + l] = f32_to_bf16_bits(z);
+    }
+  }
+}
+
 template <int MODE, int G, int Q, int FMT>
 __global__ void __launch_bounds__(32 * (Q + 2), 1)
     expert_kernel(const ExpertArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
@@ -551,6 +645,13 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
         }
       }
     }
+    if (MODE == MODE_DOWN && a.zb) {
+      // this CTA's y rows and sums of squares are written: count the CTA (release)
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) counter_add_release(a.zctr, 1);
+      down_z_step<Q + 1>(a, red, Q, lane);
+    }
     return;
   }
 
@@ -738,6 +839,7 @@ __global__ void __launch_bounds__(32 * (Q + 2), 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&rfull[pb]);
   }
+  if (MODE == MODE_DOWN && a.zb) down_z_step<Q + 1>(a, red, warp, lane);
 }
 
 // ---------------------------------------------------------------------------

@@ -74,6 +74,15 @@ struct ExpertArgs {
   int rows;                 // R = T * k: entries of sorted_rows
   int early;                // 1: the group list comes from a kernel before the preceding one, so the
                             // first weights stream before the programmatic-launch wait; 0: wait first
+  // down only, at most 64 route rows: the post-expert norm and the weighted sum
+  // in the same launch (after a device-wide count of the CTAs done), else null
+  uint16_t* zb;             // bf16 [T][L] z
+  const int32_t* topk_idx;  // [T][k]
+  const float* topk_w;      // [T][k]
+  const uint16_t* norm_g;   // bf16 [E][L]
+  int32_t* zctr;            // zeroed before the launch
+  float eps;
+  int T;
 };
 
 int launch_gateup(const ExpertArgs& a, int T, int max_group, cudaStream_t s, int num_sms);

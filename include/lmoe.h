@@ -328,7 +328,8 @@ LMOE_API int lmoe_profile_events(void* const* events, int n);
  *    rows) the streaming down launch also applies the post-expert norm and
  *    forms the weighted sum z, after a device-wide count of its CTAs; above
  *    it (or with value 0), a separate combine launch does.  The two give
- *    bit-identical z (same arithmetic, same order).  Default 1.
+ *    bit-identical z (same arithmetic, same order).  Default 0 (off:
+ *    measured no faster than the combine launch).
  *
  * Both implementations of a stage give bf16 (or fp32) of an fp32 sum per
  * output and differ only in the order of that sum.  value <= 0 restores the

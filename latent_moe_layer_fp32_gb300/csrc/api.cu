@@ -70,11 +70,12 @@ constexpr int kDenseMinTokensDefault = 64;
 constexpr int kExpertTcMinTokensDefault = 352;
 // decode sizes: gate/up and down in one persistent launch up to this many tokens
 constexpr int kFusedMaxTokensDefault = 0;
-// the post-expert norm and weighted sum inside the down launch up to this many tokens; measured
-// on GB300 against the separate combine launch: the same step time at T = 1 (99.7 against 99.0 us,
-// within the run-to-run spread), about 2 us slower at T = 4 and 8 (the down CTAs hold their SMs
-// through the z step, so the unpooler's CTAs start later)
-constexpr int kDownZMaxTokensDefault = 1;
+// the post-expert norm and weighted sum inside the down launch up to this many tokens (0: off).
+// Measured on GB300 against the separate combine launch it was no faster: 99.7 against 99.0 us
+// per T = 1 step and about 2 us slower at T = 4 and 8; a per-kernel timeline of the T = 1 step
+// put z 1.3 us later and the unpooler's end 2.5 us later (the down CTAs hold their SMs through
+// the z step, and its loads queue behind the unpooler's early weight stream).
+constexpr int kDownZMaxTokensDefault = 0;
 std::atomic<int> g_dense_min_t{kDenseMinTokensDefault};
 std::atomic<int> g_expert_tc_min_t{kExpertTcMinTokensDefault};
 std::atomic<int> g_fused_max_t{kFusedMaxTokensDefault};

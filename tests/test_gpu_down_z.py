@@ -65,9 +65,9 @@ def test_down_forms_z(lm, orc, name, T):
     out_c, names_c = forward(lm, d, w, x, 0)
     in_down = d.T <= 8 and d.T * d.k <= 64
     assert ("combine_kernel" not in names_z) == in_down, names_z
-    # the default: in the down launch at one token only
+    # the default: the combine launch
     out_d, names_d = forward(lm, d, w, x, -1)
-    assert ("combine_kernel" not in names_d) == (d.T == 1), names_d
+    assert "combine_kernel" in names_d, names_d
     assert torch.equal(out_d.view(torch.int16), out_c.view(torch.int16))
     assert "combine_kernel" in names_c, names_c
     assert torch.equal(out_z.view(torch.int16), out_c.view(torch.int16)), "z in the down launch differs"

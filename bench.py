@@ -11,7 +11,9 @@ post_expert_norm, weighted sum, unpooler) over one batch of T tokens.
           device time from CUDA events, L2 flushed (512 MB write) between steps
           outside the timed events
   e2e     same metric with the x upload from pinned host memory and the
-          output download inside the timed region
+          output download inside the timed region: lmoe_forward_host (copy
+          kernels over the host link) for the one-layer MXFP4 layer, else
+          copy-engine transfers around the device call
   roofline  the dominant kernel (largest device time) timed live with per-launch
           CUDA events: algorithmic bytes per launch / mean launch duration,
           against the measured HBM copy bandwidth
@@ -546,6 +548,11 @@ def main():
     wts = wts_layers[0]
     dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
     ws_bytes = lm.lmoe_block_workspace_bytes(dims) if args.block else lm.lmoe_workspace_bytes(dims)
+    # the one-layer MXFP4 layer takes its end-to-end step through lmoe_forward_host (tokens and output
+    # in pinned host memory); its workspace also holds the two staging buffers
+    host_api = not (args.nvfp4 or args.block or args.routed or args.graph or args.layers > 1)
+    if host_api:
+        ws_bytes = max(ws_bytes, lm.lmoe_host_workspace_bytes(dims))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     x_dev = to_dev(x)
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
@@ -642,18 +649,21 @@ def main():
         clocks = clk.summary()
 
         # ---- end to end: host input upload and output download inside the timed region ----
+        def e2e_step():
+            if host_api:  # the public call for host buffers: copy kernels over the host link
+                lm.lmoe_forward_host(dims, wts, x_host, out_host, ws)
+            else:
+                x_dev.copy_(x_host, non_blocking=True)
+                step(x_dev, out)
+                out_host.copy_(out, non_blocking=True)
         for _ in range(2):
-            x_dev.copy_(x_host, non_blocking=True)
-            step(x_dev, out)
-            out_host.copy_(out, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize()
         barrier(world)
         for i in range(args.steps):
             flush.zero_()
             e0[i].record()
-            x_dev.copy_(x_host, non_blocking=True)
-            step(x_dev, out)
-            out_host.copy_(out, non_blocking=True)
+            e2e_step()
             e1[i].record()
         torch.cuda.synchronize()
         barrier(world)
@@ -708,7 +718,8 @@ def main():
         "step_ms_percentiles": {"p10": float(np.percentile(step_ms, 10)), "median": float(np.median(step_ms)),
                                 "p90": float(np.percentile(step_ms, 90))},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d.T * d.H * 2,
-                "d2h_bytes_per_step": d.T * d.H * 2},
+                "d2h_bytes_per_step": d.T * d.H * 2,
+                "call": "lmoe_forward_host" if host_api else "copies + device call"},
         "gpu_launches": launches_per_step * n_layers * args.steps,
         "clocks": clocks,
     }

@@ -176,6 +176,26 @@ LMOE_API int lmoe_norm_combine_unpool(const lmoe_dims* dims, const float* y, con
 LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x, uint16_t* out,
                  void* ws, size_t ws_bytes, lmoe_stream_t stream);
 
+/* The whole layer with its input and output in pinned host memory, for a
+ * caller that holds the tokens on the host (a serving loop at decode sizes).
+ * No counterpart in the pages: it moves the T x H bf16 tokens in and the
+ * T x H bf16 output back with two small kernels that read and write the host
+ * buffers over the host link, in place of two copy-engine transfers.
+ *   x_host    bf16 [T][H], page-locked host memory (cudaMallocHost /
+ *             cudaHostAlloc, or cudaHostRegister'ed), 16-byte aligned
+ *   out_host  out bf16 [T][H], page-locked host memory, 16-byte aligned;
+ *             complete once the stream has reached the end of the call
+ *   ws        at least lmoe_host_workspace_bytes(dims) bytes: the layer's
+ *             workspace followed by a device staging buffer for the tokens
+ *             and one for the output
+ * The first kernel also zeroes the workspace's status and counter words, so
+ * the call issues no memset.  The result is bit-identical to lmoe_forward on
+ * the same tokens.  Device, managed or pageable pointers for x_host or
+ * out_host return LMOE_EINVAL; a short workspace returns LMOE_EWORKSPACE. */
+LMOE_API size_t lmoe_host_workspace_bytes(const lmoe_dims* dims);
+LMOE_API int lmoe_forward_host(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x_host,
+                               uint16_t* out_host, void* ws, size_t ws_bytes, lmoe_stream_t stream);
+
 /* The whole layer with caller-supplied routing ("Muse Spark Open on Gaudi 2",
  * "The latent MoE: A' with a per-expert norm": the experts, the per-route
  * post_expert_norm, the fp32 weighted sum and the unpooler all take the

@@ -19,7 +19,8 @@ from ._build import build, up_to_date
 __all__ = [
     "LmoeDims", "LmoeWeights", "LmoeWsLayout", "LmoeError", "build", "load",
     "lmoe_workspace_bytes", "lmoe_workspace_layout", "lmoe_route", "lmoe_route_noalloc", "lmoe_pool", "lmoe_experts_mxfp4",
-    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_routed", "lmoe_block_workspace_bytes",
+    "lmoe_norm_combine_unpool", "lmoe_forward", "lmoe_forward_host", "lmoe_host_workspace_bytes", "lmoe_forward_routed",
+    "lmoe_block_workspace_bytes",
     "lmoe_block_forward", "norms_of", "lmoe_experts_nvfp4", "lmoe_forward_nvfp4", "nvfp4_of",
     "lmoe_status_check", "lmoe_error_string",
     "lmoe_last_launch_count", "lmoe_selftest_e2m1", "lmoe_selftest_timeout", "lmoe_profile_events", "dims_of",
@@ -86,6 +87,9 @@ def load(path: str | None = None):
                                        sz, vp]
     lib.lmoe_norm_combine_unpool.argtypes = [dp] + [vp] * 6 + [vp, sz, vp]
     lib.lmoe_forward.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
+    lib.lmoe_forward_host.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, sz, vp]
+    lib.lmoe_host_workspace_bytes.argtypes = [dp]
+    lib.lmoe_host_workspace_bytes.restype = sz
     lib.lmoe_forward_routed.argtypes = [dp, ctypes.POINTER(LmoeWeights), vp, vp, vp, vp, vp, sz, vp]
     lib.lmoe_block_workspace_bytes.argtypes = [dp]
     lib.lmoe_block_workspace_bytes.restype = sz
@@ -107,7 +111,8 @@ def load(path: str | None = None):
     for f in ("lmoe_workspace_layout", "lmoe_route", "lmoe_pool", "lmoe_experts_mxfp4", "lmoe_norm_combine_unpool",
               "lmoe_forward", "lmoe_forward_routed", "lmoe_block_forward", "lmoe_forward_nvfp4", "lmoe_experts_nvfp4",
               "lmoe_status_check", "lmoe_last_launch_count", "lmoe_selftest_e2m1",
-              "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option", "lmoe_selftest_dequant_bf16"):
+              "lmoe_profile_events", "lmoe_route_noalloc", "lmoe_set_option", "lmoe_selftest_dequant_bf16",
+              "lmoe_forward_host"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -239,6 +244,27 @@ def lmoe_norm_combine_unpool(dims, y, topk_idx, topk_w, norm_g, unpooler_w, out,
 def lmoe_forward(dims, weights: LmoeWeights, x, out, ws, stream=None):
     _check(load().lmoe_forward(ctypes.byref(dims), ctypes.byref(weights), _ptr(x, _BF16), _ptr(out, _BF16),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "lmoe_forward")
+
+
+def _host_ptr(t):
+    """A pinned CPU tensor's address (the library checks that it is page-locked)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if t.is_cuda or not t.is_contiguous() or t.dtype not in _BF16:
+        raise ValueError("expected a contiguous bf16 CPU tensor in pinned memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def lmoe_host_workspace_bytes(dims: LmoeDims) -> int:
+    return int(load().lmoe_host_workspace_bytes(ctypes.byref(dims)))
+
+
+def lmoe_forward_host(dims, weights: LmoeWeights, x_host, out_host, ws, stream=None):
+    """The layer with x and out in pinned host memory (CPU tensors from
+    pin_memory()); ws from lmoe_host_workspace_bytes."""
+    _check(load().lmoe_forward_host(ctypes.byref(dims), ctypes.byref(weights), _host_ptr(x_host),
+                                    _host_ptr(out_host), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "lmoe_forward_host")
 
 
 def lmoe_forward_routed(dims, weights: LmoeWeights, x, topk_idx, topk_w, out, ws, stream=None):

@@ -621,6 +621,33 @@ int run_layer(const lmoe_dims* d, const lmoe_weights* wt, const WsLayout& w, con
   return LMOE_OK;
 }
 
+// lmoe_forward_host: the layer's workspace, then the token staging buffer and the
+// output staging buffer (T x H bf16 each)
+struct HostIo {
+  size_t xin, xout, total;
+};
+HostIo host_io_layout(const lmoe_dims* d, const WsLayout& w) {
+  HostIo h;
+  const size_t rows = (size_t)d->T * d->hidden * 2;
+  h.xin = al(w.pub.total);
+  h.xout = al(h.xin + rows);
+  h.total = al(h.xout + rows);
+  return h;
+}
+
+// A device-usable address of pinned (page-locked) host memory, or null for any
+// other kind of pointer (device, managed, pageable host memory).
+const void* pinned_device_ptr(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // an unregistered pointer can leave an error behind on older runtimes
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
 }  // namespace
 
 extern "C" {
@@ -706,6 +733,41 @@ int lmoe_forward(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x, 
   if (!x || !out || !aligned16(x) || !aligned16(out)) return LMOE_EINVAL;
   CHECK(check_weights(wt));
   CHECK(run_layer(d, wt, w, di, x, x, nullptr, nullptr, nullptr, out, ws, s));
+  return LMOE_OK;
+}
+
+size_t lmoe_host_workspace_bytes(const lmoe_dims* d) {
+  DevInfo di;
+  int sms = (dev_info(&di) == LMOE_OK) ? di.sms : 148;
+  WsLayout w;
+  if (layout(d, sms, &w) != LMOE_OK) return 0;
+  return host_io_layout(d, w).total;
+}
+
+int lmoe_forward_host(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t* x_host, uint16_t* out_host,
+                      void* ws, size_t ws_bytes, lmoe_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DevInfo di;
+  WsLayout w;
+  CHECK(prologue(d, ws, ws_bytes, &di, &w, s, false));
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
+  const HostIo h = host_io_layout(d, w);
+  if (ws_bytes < h.total) return LMOE_EWORKSPACE;
+  const void* xh = pinned_device_ptr(x_host);
+  void* oh = const_cast<void*>(pinned_device_ptr(out_host));
+  if (!xh || !oh || !aligned16(xh) || !aligned16(oh)) return LMOE_EINVAL;
+  CHECK(check_weights(wt));
+  const size_t n16 = (size_t)d->T * d->hidden * 2 / 16;
+  uint16_t* xin = at<uint16_t>(ws, h.xin);
+  uint16_t* xout = at<uint16_t>(ws, h.xout);
+  // the zeroed region and the tokens in one launch (in place of the memset and an upload)
+  const size_t blocks = (n16 + 255) / 256, cap = (size_t)di.sms * 4;
+  const unsigned gin = (unsigned)(blocks < cap ? blocks : cap);
+  LAUNCH(dim3(max(gin, (unsigned)((w.zero_bytes / 16 + 255) / 256))), dim3(256), s, io_in_kernel,
+         static_cast<const uint4*>(xh), reinterpret_cast<uint4*>(xin), n16, static_cast<uint4*>(ws),
+         (int)(w.zero_bytes / 16));
+  CHECK(run_layer(d, wt, w, di, xin, xin, nullptr, nullptr, nullptr, xout, ws, s));
+  LAUNCH(dim3(gin), dim3(256), s, io_out_kernel, reinterpret_cast<const uint4*>(xout), static_cast<uint4*>(oh), n16);
   return LMOE_OK;
 }
 

@@ -1,6 +1,7 @@
 // Small kernels around the streaming ones: the group list for caller-supplied
-// routing tables, post_expert_norm + weighted sum, and the E2M1 conversion
-// self-test.
+// routing tables, post_expert_norm + weighted sum, the copies between pinned
+// host memory and the workspace for lmoe_forward_host, and the E2M1
+// conversion self-test.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -158,6 +159,28 @@ __global__ void __launch_bounds__(32) timeout_selftest_kernel(Status* st, unsign
     if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) break;
   }
   set_error(st, LMOE_ETIMEOUT, 99);
+}
+
+// Host I/O for lmoe_forward_host.  io_in_kernel zeroes the workspace's zeroed
+// region (in place of the call's memset) and copies the tokens from pinned host
+// memory into the device staging buffer; io_out_kernel, after the unpooler,
+// copies the output rows back to pinned host memory.  16-byte accesses,
+// grid-stride; n16 counts 16-byte units.
+__global__ void __launch_bounds__(256) io_in_kernel(const uint4* __restrict__ x_host, uint4* __restrict__ x_dev,
+                                                    size_t n16, uint4* __restrict__ zero, int nzero16) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x, step = (size_t)gridDim.x * blockDim.x;
+  if (i0 < (size_t)nzero16) zero[i0] = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = i0; i < n16; i += step) x_dev[i] = __ldcs(x_host + i);
+}
+
+__global__ void __launch_bounds__(256) io_out_kernel(const uint4* __restrict__ out_dev, uint4* __restrict__ out_host,
+                                                     size_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x, step = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = i0; i < n16; i += step) out_host[i] = __ldcs(out_dev + i);
 }
 
 }  // namespace lmoe

@@ -188,10 +188,11 @@ LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, co
  *   ws        at least lmoe_host_workspace_bytes(dims) bytes: the layer's
  *             workspace followed by a device staging buffer for the tokens
  *             and one for the output
- * The first kernel also zeroes the workspace's status and counter words, so
- * the call issues no memset.  The result is bit-identical to lmoe_forward on
- * the same tokens.  Device, managed or pageable pointers for x_host or
- * out_host return LMOE_EINVAL; a short workspace returns LMOE_EWORKSPACE. */
+ * The first kernel also zeroes the workspace's status and counter words (the
+ * other entry points launch a small kernel for that).  The result is
+ * bit-identical to lmoe_forward on the same tokens.  Device, managed or
+ * pageable pointers for x_host or out_host return LMOE_EINVAL; a short
+ * workspace returns LMOE_EWORKSPACE. */
 LMOE_API size_t lmoe_host_workspace_bytes(const lmoe_dims* dims);
 LMOE_API int lmoe_forward_host(const lmoe_dims* dims, const lmoe_weights* weights, const uint16_t* x_host,
                                uint16_t* out_host, void* ws, size_t ws_bytes, lmoe_stream_t stream);

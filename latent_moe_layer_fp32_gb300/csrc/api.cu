@@ -289,7 +289,8 @@ int prologue(const lmoe_dims* d, void* ws, size_t ws_bytes, DevInfo* di, WsLayou
   if (need_ws) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LMOE_EINVAL;
     if (ws_bytes < w->pub.total) return LMOE_EWORKSPACE;
-    if (cudaMemsetAsync(ws, 0, w->zero_bytes, s) != cudaSuccess) return LMOE_ECUDA;
+    // the status word and counters: a kernel, not a memset, so the routing launch can start early
+    LAUNCH(dim3(1), dim3(64), s, ws_zero_kernel, static_cast<uint4*>(ws), (int)(w->zero_bytes / 16));
   }
   return LMOE_OK;
 }
@@ -367,7 +368,7 @@ int run_route(const lmoe_dims* d, const WsLayout& w, const DevInfo& di, const ui
 // x_sorted: when set (tensor-core pooler only), x_lat rows are also written in
 // expert-sorted order (row_pos = each route row's sorted position)
 // wait_mode (decode regime): kWaitAtEnd when nothing earlier in the stream can
-// still be writing x (in lmoe_forward it follows the call's own memset and routing)
+// still be writing x (in lmoe_forward it follows the call's own zeroing kernel and routing)
 int run_pool(const lmoe_dims* d, const DevInfo& di, const uint16_t* x, const uint16_t* pooler_w, uint16_t* x_lat,
              Status* st, cudaStream_t s, const int32_t* row_pos = nullptr,
              uint16_t* x_sorted = nullptr, int wait_mode = kWaitFirst) {
@@ -760,7 +761,7 @@ int lmoe_forward_host(const lmoe_dims* d, const lmoe_weights* wt, const uint16_t
   const size_t n16 = (size_t)d->T * d->hidden * 2 / 16;
   uint16_t* xin = at<uint16_t>(ws, h.xin);
   uint16_t* xout = at<uint16_t>(ws, h.xout);
-  // the zeroed region and the tokens in one launch (in place of the memset and an upload)
+  // the zeroed region and the tokens in one launch (in place of the zeroing kernel and an upload)
   const size_t blocks = (n16 + 255) / 256, cap = (size_t)di.sms * 4;
   const unsigned gin = (unsigned)(blocks < cap ? blocks : cap);
   LAUNCH(dim3(max(gin, (unsigned)((w.zero_bytes / 16 + 255) / 256))), dim3(256), s, io_in_kernel,

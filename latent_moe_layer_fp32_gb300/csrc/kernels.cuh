@@ -185,6 +185,7 @@ __global__ void dequant_selftest_kernel(const uint8_t* codes, const uint8_t* sca
 __global__ void groups_from_offsets_kernel(const int32_t* offsets, const int32_t* sorted_rows, int E, int R, int G,
                                            int4* groups, int32_t* n_groups, Status* st);
 __global__ void ssq_kernel(const float* y, int R, int L, float* ssq);
+__global__ void ws_zero_kernel(uint4* p, int n16);
 __global__ void io_in_kernel(const uint4* x_host, uint4* x_dev, size_t n16, uint4* zero, int nzero16);
 __global__ void io_out_kernel(const uint4* out_dev, uint4* out_host, size_t n16);
 __global__ void timeout_selftest_kernel(Status* st, unsigned long long limit_ns);

@@ -161,8 +161,17 @@ __global__ void __launch_bounds__(32) timeout_selftest_kernel(Status* st, unsign
   set_error(st, LMOE_ETIMEOUT, 99);
 }
 
+// The workspace's status and counter words, zeroed at the start of a call (a
+// programmatic-launch chain can start the next kernel early, which a memset
+// would not allow).  One CTA; n16 counts 16-byte units.
+__global__ void __launch_bounds__(64) ws_zero_kernel(uint4* __restrict__ p, int n16) {
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Host I/O for lmoe_forward_host.  io_in_kernel zeroes the workspace's zeroed
-// region (in place of the call's memset) and copies the tokens from pinned host
+// region (in place of ws_zero_kernel) and copies the tokens from pinned host
 // memory into the device staging buffer; io_out_kernel, after the unpooler,
 // copies the output rows back to pinned host memory.  16-byte accesses,
 // grid-stride; n16 counts 16-byte units.

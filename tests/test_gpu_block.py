@@ -66,7 +66,8 @@ def test_block_matches_oracle(lm, orc, name, T, dense):
     x_dev = to_dev(x)
     y_dev = torch.empty_like(x_dev)
     dims, ws, names = run_block(lm, d, w, nw_dev, x_dev, y_dev, dense)
-    assert names[0] == "prenorm_kernel" and names[-1] == "postnorm_residual_kernel", names
+    assert names[0] == "ws_zero_kernel" and names[1] == "prenorm_kernel", names
+    assert names[-1] == "postnorm_residual_kernel", names
     if dense == 1:
         assert "router_tc_gemm" in names, names
     lay = lm.lmoe_workspace_layout(dims)

@@ -519,8 +519,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tmem_ld32(tb + kXAcc + c0, u);
           tmem_ld_wait();
           uint16_t* hp = a.h_out + (size_t)(x.p0 + c0) * a.inter + f;
-          // silu(g) * u with the fast exponential and reciprocal (relative error
-          // ~1e-6, far below the bf16 rounding of h that follows)
+          // silu(g) * u with the fast exponential and the approximate reciprocal
+          // (relative error ~1e-6, far below the bf16 rounding of h that follows;
+          // the correctly rounded reciprocal cost the epilogue ~40% more time, and
+          // the MMAs wait for the epilogue at every item)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (c0 + i < x.n) {
@@ -529,7 +531,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 gv *= gsc;
                 uv *= gsc;
               }
-              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv * __frcp_rn(1.0f + __expf(-gv)) * uv);
+              float r;
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-gv)));
+              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv * r * uv);
             }
           }
         } else {

@@ -518,22 +518,54 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tmem_ld32(tb + c0, g);
           tmem_ld32(tb + kXAcc + c0, u);
           tmem_ld_wait();
-          uint16_t* hp = a.h_out + (size_t)(x.p0 + c0) * a.inter + f;
           // silu(g) * u with the fast exponential and the approximate reciprocal
           // (relative error ~1e-6, far below the bf16 rounding of h that follows;
           // the correctly rounded reciprocal cost the epilogue ~40% more time, and
           // the MMAs wait for the epilogue at every item)
+          float hv[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (c0 + i < x.n) {
-              float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-              if (FMT == 1) {
-                gv *= gsc;
-                uv *= gsc;
+            float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+            if (FMT == 1) {
+              gv *= gsc;
+              uv *= gsc;
+            }
+            float r;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-gv)));
+            hv[i] = gv * r * uv;
+          }
+          // Lane l holds feature f (= f0 + l) of columns c0..c0+31.  Per block of 8
+          // columns, an 8 x 8 transpose inside each group of 8 lanes (three
+          // butterfly exchanges) leaves lane l with features f0 + 8(l/8) .. +7 of
+          // column c0 + 8b + l%8: one 16-byte store instead of eight 2-byte ones.
+          const int j = lane & 7;
+          const int f0 = f - lane + 8 * (lane >> 3);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = hv[8 * b + k];
+#pragma unroll
+            for (int sh = 4; sh >= 1; sh >>= 1) {
+              const bool hi = (j & sh) != 0;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (k & sh) continue;
+                const float recv = __shfl_xor_sync(0xffffffffu, hi ? v[k] : v[k | sh], sh);
+                if (hi)
+                  v[k] = recv;
+                else
+                  v[k | sh] = recv;
               }
-              float r;
-              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-gv)));
-              hp[(size_t)i * a.inter] = f32_to_bf16_bits(gv * r * uv);
+            }
+            const int col = c0 + 8 * b + j;
+            if (col < x.n) {
+              uint4 pk;
+              pk.x = (uint32_t)f32_to_bf16_bits(v[0]) | ((uint32_t)f32_to_bf16_bits(v[1]) << 16);
+              pk.y = (uint32_t)f32_to_bf16_bits(v[2]) | ((uint32_t)f32_to_bf16_bits(v[3]) << 16);
+              pk.z = (uint32_t)f32_to_bf16_bits(v[4]) | ((uint32_t)f32_to_bf16_bits(v[5]) << 16);
+              pk.w = (uint32_t)f32_to_bf16_bits(v[6]) | ((uint32_t)f32_to_bf16_bits(v[7]) << 16);
+              *reinterpret_cast<uint4*>(a.h_out + (size_t)(x.p0 + col) * a.inter + f0) = pk;
             }
           }
         } else {

@@ -402,9 +402,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
     int rs = 0, as = 0;
     uint32_t rph = 0, aph = 0;
     bool ok = true;
-    // the TMEM store of a step completes while the next step is dequantised:
-    // its full[] arrival is deferred until then (pend_as = its stage, or -1)
-    int pend_as = -1;
     int4 g_next = x_group(a, blockIdx.x, nft, n_items);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const int4 g_cur = g_next;
@@ -460,21 +457,19 @@ __global__ void __launch_bounds__(kXThreads, 1)
               dq_block(c, sb, o + 16 * bi, fast || (sb >= 2u && sb <= 252u));
             }
           }
-          if (pend_as >= 0) {
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[pend_as]);
-          }
           if (!mbar_wait(&empty[as], aph ^ 1, a.st, 71)) {
             ok = false;
-            pend_as = -1;
             break;
           }
           tc_fence_after();
           const uint32_t acol = tmem + lane_base + kXACol + (uint32_t)(as * C::NMAT + m) * 32u;
           tmem_st32(acol, o);
-          pend_as = as;
+          // the stage is complete once the store lands: arrive at once (deferring the
+          // arrival past the next step's dequantisation made the MMAs wait longer)
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[as]);
           if (++as == C::ST) {
             as = 0;
             aph ^= 1;
@@ -487,12 +482,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
           rph ^= 1;
         }
       }
-    }
-    if (pend_as >= 0) {
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[pend_as]);
     }
   } else {
     // ---------------- epilogue: TMEM -> h (gate/up) or y, ssq (down) ----------------

@@ -178,9 +178,10 @@ LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, co
 
 /* The whole layer with its input and output in pinned host memory, for a
  * caller that holds the tokens on the host (a serving loop at decode sizes).
- * No counterpart in the pages: it moves the T x H bf16 tokens in and the
- * T x H bf16 output back with two small kernels that read and write the host
- * buffers over the host link, in place of two copy-engine transfers.
+ * No counterpart in the pages: up to 256 KB each way (16 tokens at hidden
+ * 8192) it moves the T x H bf16 tokens in and the output back with two small
+ * kernels that read and write the host buffers over the host link, in place
+ * of two copy-engine transfers; above that, with the copy engines.
  *   x_host    bf16 [T][H], page-locked host memory (cudaMallocHost /
  *             cudaHostAlloc, or cudaHostRegister'ed), 16-byte aligned
  *   out_host  out bf16 [T][H], page-locked host memory, 16-byte aligned;
@@ -188,7 +189,7 @@ LMOE_API int lmoe_forward(const lmoe_dims* dims, const lmoe_weights* weights, co
  *   ws        at least lmoe_host_workspace_bytes(dims) bytes: the layer's
  *             workspace followed by a device staging buffer for the tokens
  *             and one for the output
- * The first kernel also zeroes the workspace's status and counter words (the
+ * The upload kernel also zeroes the workspace's status and counter words (the
  * other entry points launch a small kernel for that).  The result is
  * bit-identical to lmoe_forward on the same tokens.  Device, managed or
  * pageable pointers for x_host or out_host return LMOE_EINVAL; a short

@@ -70,6 +70,26 @@ def test_block_workspace_sizing_without_gpu(lm):
     assert lm.lmoe_block_workspace_bytes(lm.dims_of(0, 512, 256, 256, 16, 4, 1e-6)) == 0
 
 
+def test_host_workspace_sizing_without_gpu(lm):
+    for name, d in synth.CONFIGS.items():
+        dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+        n, nh = lm.lmoe_workspace_bytes(dims), lm.lmoe_host_workspace_bytes(dims)
+        # the layer's workspace plus a staging buffer for the tokens and one for the output, 256-byte aligned
+        rows = 2 * d.T * d.H
+        assert nh >= n + 2 * rows and nh <= n + 2 * rows + 3 * 256, name
+    assert lm.lmoe_host_workspace_bytes(lm.dims_of(0, 512, 256, 256, 16, 4, 1e-6)) == 0
+
+
+def test_host_forward_refuses_bad_arguments_without_gpu(lm):
+    """Argument checks run before any device work: no workspace, null buffers."""
+    d = synth.CONFIGS["tiny"]
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    lib = lm.load()
+    w = lm.LmoeWeights()
+    rc = lib.lmoe_forward_host(ctypes.byref(dims), ctypes.byref(w), None, None, None, 0, None)
+    assert rc != 0
+
+
 @pytest.mark.parametrize("field,value", [("T", 0), ("top_k", 9), ("top_k", 0), ("n_experts", 257),
                                          ("hidden", 100), ("latent", 96), ("inter", 0), ("eps", -1.0)])
 def test_bad_dims_rejected(lm, field, value):

@@ -1,9 +1,10 @@
-"""lmoe_forward captured in a CUDA graph: the memset, the programmatic-launch
+"""lmoe_forward captured in a CUDA graph: the zeroing kernel, the programmatic-launch
 chain and the side-stream fork/join all replay.  A replay equals the eager
 call bit for bit and matches the CPU oracle, also after new input is copied
 into the captured buffer; a two-layer stack captured in one graph (each
 layer's bf16 output the next layer's input) matches the oracle layer by
-layer and the oracle applied twice."""
+layer and the oracle applied twice; the host-buffer entry point replays
+against the same pinned buffers."""
 from __future__ import annotations
 
 import numpy as np
@@ -143,3 +144,44 @@ def test_two_layer_stack_from_a_cuda_graph(lm, orc, name, T):
     assert np.abs(dd).max() / np.abs(r).max() <= 2e-2
     assert float((g * r).sum() / (np.linalg.norm(g) * np.linalg.norm(r))) >= 0.9999
     assert np.all(np.abs(dd) <= 4e-2 * (np.abs(r) + np.sqrt((r * r).mean())))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 600), ("decode_t1", None)],
+                         ids=["tiny_T4", "tiny_T600", "decode_t1"])
+def test_host_buffer_forward_replays_from_a_cuda_graph(lm, name, T):
+    """lmoe_forward_host captured in a graph: the copy kernels (few tokens) or
+    the copy-engine transfers (many) replay against the same pinned buffers,
+    so new tokens written into the host input give the eager result for them."""
+    d = synth.CONFIGS[name] if T is None else synth.with_tokens(synth.CONFIGS[name], T)
+    wts = lm.weights_of(device_weights(d))
+    dims = lm.dims_of(d.T, d.H, d.L, d.I, d.E, d.k, d.eps)
+    x, x2 = to_dev(synth.make_x(d)), to_dev(synth.make_x(d, token0=d.T))
+    ref = torch.empty(d.T, d.H, dtype=torch.bfloat16, device="cuda")
+    ref2 = torch.empty_like(ref)
+    ws_dev = ws_for(lm, dims)
+    lm.lmoe_forward(dims, wts, x, ref, ws_dev)
+    lm.lmoe_forward(dims, wts, x2, ref2, ws_dev)
+    torch.cuda.synchronize()
+
+    ws = torch.empty(lm.lmoe_host_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    x_host = x.cpu().pin_memory()
+    out_host = torch.zeros(d.T, d.H, dtype=torch.bfloat16).pin_memory()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first-use setup outside the capture
+        lm.lmoe_forward_host(dims, wts, x_host, out_host, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lm.lmoe_forward_host(dims, wts, x_host, out_host, ws)
+    out_host.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lm.lmoe_status_check(ws) == 0
+    assert torch.equal(out_host.view(torch.int16), ref.cpu().view(torch.int16))
+    x_host.copy_(x2.cpu())
+    g.replay()
+    torch.cuda.synchronize()
+    assert lm.lmoe_status_check(ws) == 0
+    assert torch.equal(out_host.view(torch.int16), ref2.cpu().view(torch.int16))
